@@ -1,0 +1,400 @@
+#!/usr/bin/env python3
+"""Benchmark of the MatMulNBits hot path on GB300.
+
+Default workload: the int4 decode GEMV, M=1, K=4096, N=11008, bf16 X/Y, f16
+scales, uint8 zero points (block 32), metric GB/s (algorithmic bytes / time).
+``--config 4`` selects the M=512 prefill GEMM (metric TFLOP/s).  The default
+run also reports the M=512 GEMM as a secondary object.
+
+A step is one mnb_matmul call over one batch (the decode step of one
+projection).  Weights are rotated over enough distinct copies that every
+step streams them from HBM (copies x bytes >= 3 x L2).  Steps are replayed
+from a CUDA graph (one graph node per call, as a serving loop would) and
+timed with CUDA events on the launching stream, with a barrier and a device
+synchronise on both sides.  Under torchrun each rank runs its own replica
+(weak scaling, no data-path collective); the time is the max over ranks.
+
+Prints ONE JSON line on rank 0.  ``--impl reference`` times the CPU oracle
+(the reference arm of this build) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_quantized_weight_matmulnbits_gb300 import workloads as wl  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=20000)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--kernel", default="auto")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def metric_of(w: wl.Workload):
+    if w.M >= 64:
+        return "TFLOP/s", w.flops() / 1e12
+    return "GB/s", w.algorithmic_bytes() / 1e9
+
+
+# ---- clocks ----------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = str(device_index)
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.dev = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            if vis:
+                self.dev = vis.split(",")[device_index]
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, n = [], None, set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            n += 1
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ---- CPU oracle timing -----------------------------------------------------
+
+def cpu_oracle_rate(w: wl.Workload, data, seconds: float):
+    """Time the oracle (as it stands) on this host's cores over a bounded sample
+    of the workload; return (value in the metric's unit, cores, sample text)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    x64 = wl.widen_f64(data["x"], w.act_dtype)
+    s32 = wl.widen_f32(data["scales"], w.scale_dtype)
+    cores = oracle.threads()
+    unit, per_full = metric_of(w)
+    # sample: all rows of x against a prefix of the output columns, sized to ~seconds
+    n_cols = max(1, min(w.N, 64))
+    done_cols, t_total = 0, 0.0
+    rng = np.random.default_rng(1)
+    while t_total < seconds and done_cols < 50 * w.N:
+        cols = rng.integers(0, w.N, n_cols)
+        ms = np.repeat(np.arange(w.M), n_cols)
+        ns = np.tile(cols, w.M)
+        t0 = time.perf_counter()
+        oracle.matmul_points(x64, data["b"], s32, data["zp"], w.N, w.K, w.bits, w.bs, ms, ns)
+        dt = time.perf_counter() - t0
+        t_total += dt
+        done_cols += n_cols
+        if dt < 0.5 * seconds / 4:
+            n_cols = min(w.N * 8, n_cols * 2)
+    frac = done_cols / w.N
+    value = per_full * frac / t_total
+    sample = (f"{done_cols} output columns x all {w.M} rows (={frac:.3g} of the workload) in {t_total:.2f} s, "
+              f"fp64 oracle, OpenMP over outputs")
+    return value, cores, sample
+
+
+# ---- GPU arm ---------------------------------------------------------------
+
+def traffic_for(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source
+    it was taken from is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e:
+        return None
+    src = os.path.join(ROOT, e["source"])
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return e["bytes_per_launch"] if h == e["source_sha256_16"] else None
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import block_quantized_weight_matmulnbits_gb300 as mnb
+
+    TORCH_DT = {wl.F32: torch.float32, wl.F16: torch.float16, wl.BF16: torch.bfloat16}
+
+    def to_dev(stored, dtype):
+        a = np.ascontiguousarray(stored)
+        if dtype == wl.F32:
+            return torch.from_numpy(a.astype(np.float32)).cuda()
+        return torch.from_numpy(a.view(np.int16)).cuda().view(TORCH_DT[dtype])
+
+    def aligned_empty(nbytes, align=256):
+        raw = torch.empty(nbytes + align, dtype=torch.uint8, device="cuda")
+        off = (-raw.data_ptr()) % align
+        return raw[off:off + nbytes]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    mnb.load()
+    pk, pk_src = peaks()
+
+    def measure(w: wl.Workload, steps: int, warmup: int, kernel: str, want_e2e: bool):
+        data = wl.generate(w)
+        x = to_dev(data["x"], w.act_dtype)
+        b = torch.from_numpy(np.ascontiguousarray(data["b"])).cuda()
+        s0 = to_dev(data["scales"], w.scale_dtype)
+        zp0 = None if data["zp"] is None else torch.from_numpy(np.ascontiguousarray(data["zp"])).cuda()
+        packed = aligned_empty(mnb.mnb_packed_size(w.N, w.K, w.bits, w.bs))
+        mnb.mnb_pack_weights(b, packed, w.N, w.K, w.bits, w.bs)
+        del b
+        chosen = kernel if kernel != "auto" else mnb.mnb_select_kernel(w.M, w.N, w.K, w.bits, w.bs,
+                                                                       w.act_dtype)
+        # weight copies so that each step streams from HBM
+        l2 = torch.cuda.get_device_properties(local).L2_cache_size
+        wbytes = packed.numel() + s0.numel() * s0.element_size() + (zp0.numel() if zp0 is not None else 0)
+        R = max(2, math.ceil(3 * l2 / wbytes))
+        copies = [(packed, s0, zp0)]
+        for _ in range(R - 1):
+            pb = aligned_empty(packed.numel())
+            pb.copy_(packed)
+            copies.append((pb, s0.clone(), None if zp0 is None else zp0.clone()))
+        yb = torch.empty((w.M, w.N), dtype=TORCH_DT[w.out_dtype], device="cuda")
+        stream = torch.cuda.Stream()
+
+        def call(i, xin=None, yout=None):
+            pb, s, zp = copies[i % R]
+            mnb.mnb_matmul_ex(x if xin is None else xin, pb, s, zp, yb if yout is None else yout, w.M, w.N,
+                              w.K, w.bits, w.bs, w.act_dtype, w.out_dtype, w.scale_dtype, kernel=kernel,
+                              stream=stream)
+
+        with torch.cuda.stream(stream):
+            for i in range(R):
+                call(i)
+        torch.cuda.synchronize()
+
+        def capture(n):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                for i in range(n):
+                    call(i)
+            return gr
+
+        g = capture(R)
+        rem = steps % R
+        g_rem = capture(rem) if rem else None
+        reps = steps // R
+        steps_eff = steps
+        clocks = ClockSampler(local)
+        clocks.start()
+        for _ in range(warmup // R):
+            g.replay()
+        with torch.cuda.stream(stream):
+            for i in range(warmup % R):
+                call(i)
+        barrier()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
+        barrier()
+        ck = clocks.stop()
+        t = ev0.elapsed_time(ev1) / 1e3
+        if dist is not None:
+            tt = torch.tensor([t], device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            t = float(tt.item())
+        unit, per_step = metric_of(w)
+        value = world * steps_eff * per_step / t
+        per_launch_s = t / steps_eff
+        out = {"value": value, "unit": unit, "steps": steps_eff, "ms_per_step": per_launch_s * 1e3,
+               "kernel": chosen, "clocks": ck, "weight_copies": R, "launches": steps_eff}
+        if unit == "GB/s":
+            peak = pk["hbm_gbs"]
+            out["roofline"] = {"bound": "hbm", "achieved": per_step / per_launch_s, "peak": peak, "unit": "GB/s",
+                               "frac": per_step / per_launch_s / peak,
+                               "traffic": traffic_for(f"{chosen}:{w.name}"),
+                               "peak_source": f"{pk_src} hbm_gbs"}
+        else:
+            peak = pk["bf16_tflops"]
+            out["roofline"] = {"bound": "tensor", "achieved": per_step / per_launch_s, "peak": peak,
+                               "unit": "TFLOP/s", "frac": per_step / per_launch_s / peak,
+                               "traffic": traffic_for(f"{chosen}:{w.name}"),
+                               "peak_source": f"{pk_src} bf16_tflops (burst)"}
+        if want_e2e:
+            # End to end through the C ABI: pinned host X -> device, the call, device Y -> pinned host.
+            xh = x.cpu().pin_memory()
+            yh = torch.empty((w.M, w.N), dtype=TORCH_DT[w.out_dtype]).pin_memory()
+            xd = torch.empty_like(x)
+            ge = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                for i in range(R):
+                    xd.copy_(xh, non_blocking=True)
+                    call(i, xin=xd)
+                    yh.copy_(yb, non_blocking=True)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(ge, stream=stream):
+                for i in range(R):
+                    xd.copy_(xh, non_blocking=True)
+                    call(i, xin=xd)
+                    yh.copy_(yb, non_blocking=True)
+            ge.replay()
+            barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(max(1, reps)):
+                ge.replay()
+            e1.record(stream)
+            barrier()
+            te = e0.elapsed_time(e1) / 1e3
+            if dist is not None:
+                tt = torch.tensor([te], device="cuda")
+                dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+                te = float(tt.item())
+            out["e2e"] = {"value": world * reps * R * per_step / te, "unit": unit,
+                          "h2d_bytes_per_step": x.numel() * x.element_size(),
+                          "d2h_bytes_per_step": yb.numel() * yb.element_size(),
+                          "mode": "CUDA graph of (H2D X from pinned host, mnb_matmul, D2H Y to pinned host) per step"}
+        return out, data
+
+    w = wl.config(args.config)
+    main, data = measure(w, args.steps, args.warmup, args.kernel, True)
+    res = {
+        "metric": "int4 MatMulNBits GB/s at M=1, TFLOP/s at M=512; % of roofline",
+        "value": main["value"], "unit": main["unit"], "n_gpus": world, "steps": main["steps"],
+        "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 accumulate (int%d weights, %s activations)" % (w.bits, wl.DTYPE_NAMES[w.act_dtype]),
+        "data": "synthetic (seeded, LLM-projection shaped; no trained weights)",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "bits": w.bits, "block_size": w.bs,
+                   "zero_points": w.zp is not None, "kernel": main["kernel"],
+                   "l2": f"inputs larger than L2: {main['weight_copies']} rotating weight copies (>= 3 x L2)",
+                   "launch": "CUDA graph replay, one kernel per step"},
+        "roofline": main["roofline"], "clocks": main["clocks"], "e2e": main["e2e"],
+        "gpu_launches": main["launches"],
+    }
+    if args.config == 1 and not args.no_secondary:
+        w2 = wl.config(4)
+        sec, _ = measure(w2, max(20, args.steps // 20), max(3, args.warmup // 20), "auto", False)
+        res["m512"] = {"workload": w2.name, "value": sec["value"], "unit": sec["unit"], "kernel": sec["kernel"],
+                       "ms_per_step": sec["ms_per_step"], "roofline": sec["roofline"], "clocks": sec["clocks"]}
+        res["gpu_launches"] += sec["launches"]
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = cpu_oracle_rate(w, data, args.cpu_seconds)
+        res["cpu_baseline"] = {"value": v, "unit": main["unit"], "cores": cores, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = wl.config(args.config)
+    data = wl.generate(w)
+    unit, _ = metric_of(w)
+    per = max(0.5, min(10.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_oracle_rate(w, data, per)
+    vals = []
+    t0 = time.perf_counter()
+    cores, sample = None, None
+    for _ in range(args.steps):
+        v, cores, sample = cpu_oracle_rate(w, data, per)
+        vals.append(v)
+    wall = time.perf_counter() - t0
+    value = statistics.median(vals)
+    res = {"impl": "reference", "metric": "int4 MatMulNBits GB/s at M=1, TFLOP/s at M=512; % of roofline",
+           "value": value, "unit": unit, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": wall / max(1, args.steps) * 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64 (CPU oracle)", "data": "synthetic (seeded)",
+           "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "bits": w.bits, "block_size": w.bs},
+           "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                            "sample": f"per step: {sample}"},
+           "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)

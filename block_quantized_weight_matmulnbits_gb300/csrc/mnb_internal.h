@@ -1,0 +1,63 @@
+// Internal launch interface between the C ABI (capi.cu) and the kernel files.
+// Every launcher enqueues on `stream` and returns the cudaError_t of the launch.
+#pragma once
+
+#include <cstdint>
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "mnb_common.cuh"
+
+namespace mnb {
+
+struct MatmulParams {
+    const void* x;
+    const uint8_t* packed;   // tile data (header already skipped)
+    const void* packed_hdr;  // start of the packed buffer (header)
+    const void* scales;
+    const uint8_t* zp;
+    const int32_t* g_idx;
+    const void* bias;
+    void* y;
+    int64_t M;
+    Layout L;
+    int act_dtype, out_dtype, scale_dtype, bias_dtype;
+    int* status;             // device status word
+    void* workspace;
+    size_t workspace_bytes;
+};
+
+cudaError_t launch_pack(const uint8_t* b_ort, uint8_t* packed_hdr, const Layout& L, cudaStream_t s);
+cudaError_t launch_unpack(const uint8_t* packed, uint8_t* b_ort, const Layout& L, cudaStream_t s);
+cudaError_t launch_dequant(const uint8_t* packed, const void* scales, int scale_dtype, const uint8_t* zp,
+                           float* w, const Layout& L, cudaStream_t s);
+
+cudaError_t launch_generic(const MatmulParams& p, cudaStream_t s);
+
+// Decode GEMV (M == 1).  Returns cudaErrorNotSupported when the shape is
+// outside what the kernel handles (the caller then reports UNSUPPORTED).
+bool gemv_supported(const MatmulParams& p);
+cudaError_t launch_gemv(const MatmulParams& p, cudaStream_t s);
+
+bool gemv_mma_supported(const MatmulParams& p);
+cudaError_t launch_gemv_mma(const MatmulParams& p, cudaStream_t s);
+
+bool gemm_tc_supported(const MatmulParams& p);
+cudaError_t launch_gemm_tc(const MatmulParams& p, cudaStream_t s);
+
+size_t i8_workspace_bytes(int64_t M, const Layout& L);
+bool gemv_i8_supported(const MatmulParams& p);
+cudaError_t launch_quant_act(const void* x, int act_dtype, int8_t* qa, float* sa, int64_t M, const Layout& L,
+                             cudaStream_t s);
+cudaError_t launch_gemv_i8(const MatmulParams& p, cudaStream_t s);
+
+// Device properties of the current device (cached per device).
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int major, minor;
+    size_t smem_optin;
+};
+const DeviceInfo& device_info();
+
+}  // namespace mnb

@@ -1,0 +1,204 @@
+/*
+ * mnb.h -- C ABI of libmnb, block-quantized weight-only matmul (MatMulNBits)
+ * for NVIDIA GB300 (sm_103a).
+ *
+ *     Y[M, N] = X[M, K] . dequant(B)^T
+ *
+ * The operation and its storage format are those of the ONNX Runtime
+ * com.microsoft::MatMulNBits operator as restated by onnx-runtime-ep-cpu
+ * 0.1.0-dev.5, src/kernels/matmul_nbits.rs (module doc; MatMulNBitsFactory::
+ * create; MatMulNBitsKernel::execute; fn dequantize_nbits_value):
+ *
+ *   - B is uint8 [N, KB, blob] with KB = ceil(K / block_size) and
+ *     blob = block_size * bits / 8.  Codes are packed least-significant bits
+ *     first: element i of block kb of row n sits at bit i*bits of that blob.
+ *   - scales is [N, KB] (f32, f16 or bf16), one per (row, K-block).
+ *   - zero_points is uint8 [N, ceil(KB * bits / 8)], packed at `bits` width,
+ *     least-significant bits first, or NULL, in which case every zero point
+ *     is 2^(bits-1) (8 for 4-bit, 128 for 8-bit, 2 for 2-bit).
+ *   - w[n, k] = (q[n, k] - zp[n, k / bs]) * scale[n, k / bs], evaluated in f32.
+ *   - bits is 2, 4 or 8; block_size is a power of two >= 16.
+ *   - When K is not a multiple of block_size the last block is partial; its
+ *     codes past K are ignored.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers documented as "device" must point to memory the current CUDA
+ *     device can access (cudaMalloc, or a torch CUDA tensor's data_ptr()).
+ *     The caller owns every buffer; the library allocates no device memory
+ *     and keeps no state between calls other than a per-device status word.
+ *   - All work is enqueued on `stream` (NULL = the legacy default stream) and
+ *     is asynchronous.  A returned MNB_OK means the arguments were valid and
+ *     the launch was accepted; faults during execution surface at the
+ *     caller's next synchronisation, and kernel-detected problems (a packed
+ *     buffer whose header does not match, a bounded wait that ran out) are
+ *     recorded in the device status word read by mnb_get_device_error().
+ *   - Arguments are validated on the host before anything is launched.  A
+ *     non-OK status means nothing was enqueued.  The library never aborts,
+ *     exits or prints unless MNB_LOG=1 is set in the environment.
+ *   - Device pointers must be 16-byte aligned unless stated otherwise.
+ */
+#ifndef MNB_H_
+#define MNB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MNB_ABI_VERSION 1
+
+/* Symbols of the shared library; everything else in it is hidden. */
+#if defined(__GNUC__)
+#define MNB_API __attribute__((visibility("default")))
+#else
+#define MNB_API
+#endif
+
+/* Same type as cudaStream_t; declared here so this header needs no CUDA headers. */
+typedef struct CUstream_st* mnb_stream_t;
+
+typedef enum mnb_status {
+    MNB_OK = 0,
+    MNB_ERR_INVALID_ARG = 1,      /* a pointer, size, dtype or alignment is invalid */
+    MNB_ERR_UNSUPPORTED = 2,      /* valid for the operator, but no kernel here handles it */
+    MNB_ERR_CUDA = 3,             /* a CUDA runtime call failed (launch, attribute query) */
+    MNB_ERR_NO_MEM = 4,           /* a caller-provided buffer is too small */
+    MNB_ERR_TIMEOUT = 5,          /* (device status) a bounded wait inside a kernel ran out */
+    MNB_ERR_LAYOUT_MISMATCH = 6   /* (device status) packed buffer header does not match N, K, bits, bs */
+} mnb_status;
+
+typedef enum mnb_dtype { MNB_F32 = 0, MNB_F16 = 1, MNB_BF16 = 2 } mnb_dtype;
+
+/* Kernel families.  MNB_KERNEL_AUTO lets the library choose from M, dtypes and
+ * accuracy level; the others force one (tests and benchmarks).  Forcing a
+ * kernel that cannot handle the call returns MNB_ERR_UNSUPPORTED. */
+typedef enum mnb_kernel {
+    MNB_KERNEL_AUTO = 0,
+    MNB_KERNEL_GEMV = 1,      /* M == 1 decode GEMV, CUDA cores, TMA-streamed weights */
+    MNB_KERNEL_GEMV_MMA = 2,  /* 1 <= M <= 16, bf16/f16 X, warp-level tensor-core MMA on registers */
+    MNB_KERNEL_GEMM_TC = 3,   /* M >= 1 prefill GEMM, bf16/f16 X, tcgen05 + TMEM + TMA */
+    MNB_KERNEL_GENERIC = 4,   /* any shape and dtype, CUDA cores, shared-memory tiles */
+    MNB_KERNEL_GEMV_I8 = 5    /* int8-activation path (accuracy_level 4), integer dot products */
+} mnb_kernel;
+
+/* ---- weight layout (one-time re-tiling) -------------------------------- */
+
+/* Bytes of the packed weight buffer for (N, K, bits, block_size), or 0 if the
+ * arguments are invalid.  The buffer is a 256-byte header followed by the
+ * codes of B re-tiled into 512-byte tiles of 16 rows, each tile holding one
+ * 16-byte slice per lane of a 32-lane warp; the code values are unchanged,
+ * so packing is a pure permutation (plus zero padding of the row count to a
+ * multiple of 16 and of the padded K to a multiple of 256/bits). */
+MNB_API size_t mnb_packed_size(int64_t N, int64_t K, int bits, int block_size);
+
+/* Re-tile B (ORT layout, device, [N, KB, blob] uint8, any alignment) into
+ * packed_b (device, 256-byte aligned, packed_bytes >= mnb_packed_size()).
+ * Writes the header and every byte of the buffer.  MNB_ERR_NO_MEM if
+ * packed_bytes is too small.  Follows the storage rule of
+ * onnx-runtime-ep-cpu matmul_nbits.rs (module doc, fn dequantize_nbits_value). */
+MNB_API mnb_status mnb_pack_weights(const uint8_t* b_ort, void* packed_b, size_t packed_bytes,
+                            int64_t N, int64_t K, int bits, int block_size, mnb_stream_t stream);
+
+/* Inverse of mnb_pack_weights: write the ORT-layout bytes of B (device,
+ * [N, KB, blob] uint8) back from packed_b.  pack followed by unpack returns
+ * the original bytes exactly, padding codes of a partial last block included. */
+MNB_API mnb_status mnb_unpack_codes(const void* packed_b, uint8_t* b_ort, int64_t N, int64_t K, int bits,
+                            int block_size, mnb_stream_t stream);
+
+/* Dequantised weight w_nk (device, [N, K] f32, row-major, 4-byte aligned):
+ * w = (f32(q) - f32(zp)) * f32(scale), one f32 rounding, bit-identical to
+ * onnx-runtime-ep-cpu matmul_nbits.rs fn dequantize_nbits_value.  scales is
+ * device [N, KB] of scale_dtype (natural alignment); zero_points may be NULL. */
+MNB_API mnb_status mnb_dequantize(const void* packed_b, const void* scales, const uint8_t* zero_points,
+                          float* w_nk, int64_t N, int64_t K, int bits, int block_size,
+                          mnb_dtype scale_dtype, mnb_stream_t stream);
+
+/* ---- the matmul -------------------------------------------------------- */
+
+/* Y = X . dequant(B)^T.
+ *   x           device [M, K] act_dtype, row-major (16-byte aligned)
+ *   packed_b    device, written by mnb_pack_weights for the same N, K, bits, block_size
+ *   scales      device [N, KB] scale_dtype (natural alignment)
+ *   zero_points device [N, ceil(KB*bits/8)] uint8, or NULL (=> 2^(bits-1))
+ *   y           device [M, N] out_dtype, row-major (16-byte aligned)
+ * Accumulation is in f32 (fp32 accumulator, f32 or exact-integer partial
+ * products); the result is rounded once to out_dtype with round-to-nearest-even.
+ * The reduction order is fixed for a given launch configuration, so repeated
+ * calls give bit-identical results.  M == 0 is a no-op. */
+MNB_API mnb_status mnb_matmul(const void* x, const void* packed_b, const void* scales,
+                      const uint8_t* zero_points, void* y, int64_t M, int64_t N, int64_t K, int bits,
+                      int block_size, mnb_dtype act_dtype, mnb_dtype out_dtype, mnb_dtype scale_dtype,
+                      mnb_stream_t stream);
+
+/* Extended call: everything of mnb_matmul plus
+ *   g_idx          device int32 [K] or NULL: group (scale/zero-point column) of
+ *                  each depth, each in [0, KB) (onnx-runtime-ep-cpu matmul_nbits.rs,
+ *                  MatMulNBitsKernel::dequantize_weight, grouped path).  Values are
+ *                  not range-checked on the device; out-of-range values are the
+ *                  caller's error.  Only MNB_KERNEL_GENERIC handles g_idx.
+ *   bias           device [N] of bias_dtype or NULL, added after the product
+ *                  (MatMulNBitsKernel::execute).
+ *   accuracy_level 0..3: float path.  4: activations quantised per K-block to
+ *                  int8 (scale = max|x|/127, round half away from zero), exact
+ *                  integer block dot, then one f32 rescale (fn
+ *                  quantize_activation_signed, fn int8_row).  Needs workspace.
+ *   workspace      device scratch of at least mnb_workspace_size() bytes
+ *                  (256-byte aligned) or NULL when that size is 0.
+ *   kernel         MNB_KERNEL_AUTO or a forced family. */
+typedef struct mnb_matmul_args {
+    const void* x;
+    const void* packed_b;
+    const void* scales;
+    const uint8_t* zero_points;
+    const int32_t* g_idx;
+    const void* bias;
+    void* y;
+    int64_t M, N, K;
+    int bits;
+    int block_size;
+    mnb_dtype act_dtype;
+    mnb_dtype out_dtype;
+    mnb_dtype scale_dtype;
+    mnb_dtype bias_dtype;
+    int accuracy_level;
+    void* workspace;
+    size_t workspace_bytes;
+    mnb_kernel kernel;
+    mnb_stream_t stream;
+} mnb_matmul_args;
+
+MNB_API mnb_status mnb_matmul_ex(const mnb_matmul_args* args);
+
+/* Scratch bytes mnb_matmul_ex needs for this call (0 for the float path). */
+MNB_API size_t mnb_workspace_size(int64_t M, int64_t N, int64_t K, int bits, int block_size, int accuracy_level);
+
+/* Per-(row, K-block) int8 activation quantisation on its own (the first step
+ * of accuracy_level 4): qa device int8 [M, KB*bs] (tail past K zero), sa
+ * device f32 [M, KB].  Bit-identical to the definition in the mnb_matmul_ex
+ * comment above. */
+MNB_API mnb_status mnb_quantize_activations(const void* x, int8_t* qa, float* sa, int64_t M, int64_t K,
+                                    int block_size, mnb_dtype act_dtype, mnb_stream_t stream);
+
+/* ---- diagnostics ------------------------------------------------------- */
+
+/* The family mnb_matmul_ex would run with kernel == MNB_KERNEL_AUTO (host
+ * only, no GPU needed).  Thresholds: MNB_GEMV_MAX_M (default 16) and the
+ * environment override of the same name. */
+MNB_API mnb_kernel mnb_select_kernel(int64_t M, int64_t N, int64_t K, int bits, int block_size,
+                             mnb_dtype act_dtype, int accuracy_level);
+
+/* Read and clear the current device's status word (an mnb_status value set
+ * by a kernel; MNB_OK if none).  Synchronises the device. */
+MNB_API mnb_status mnb_get_device_error(int* code);
+
+MNB_API const char* mnb_status_string(mnb_status s);
+MNB_API const char* mnb_kernel_name(mnb_kernel k);
+MNB_API int mnb_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MNB_H_ */

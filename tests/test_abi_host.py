@@ -1,0 +1,110 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds for
+sm_103a, loads, exports every symbol include/mnb.h declares, sizes the packed
+buffer as documented, chooses kernels as documented, and rejects invalid
+arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_quantized_weight_matmulnbits_gb300 as mnb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return mnb.load()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "mnb.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mnb_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_binding_exports():
+    assert declared_symbols() == sorted(mnb.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert getattr(lib, name) is not None
+
+
+def test_abi_version(lib):
+    assert mnb.mnb_abi_version() == 1
+
+
+@pytest.mark.parametrize("N,K,bits,bs", [(11008, 4096, 4, 32), (4096, 11008, 8, 128), (14336, 4096, 2, 64),
+                                         (37, 40, 4, 32), (1, 1, 2, 16), (17, 300, 8, 16)])
+def test_packed_size_formula(N, K, bits, bs):
+    KB = -(-K // bs)
+    KT = 256 // bits
+    ktiles = -(-(KB * bs) // KT)
+    nt = -(-N // 16)
+    assert mnb.mnb_packed_size(N, K, bits, bs) == 256 + nt * ktiles * 512
+    # the packed buffer never holds less than the ORT bytes
+    assert mnb.mnb_packed_size(N, K, bits, bs) >= N * KB * bs * bits // 8
+
+
+@pytest.mark.parametrize("bad", [(0, 64, 4, 32), (8, 0, 4, 32), (8, 64, 3, 32), (8, 64, 4, 24), (8, 64, 4, 8),
+                                 (8, 64, 16, 32), (-1, 64, 4, 32)])
+def test_packed_size_rejects_invalid(bad):
+    assert mnb.mnb_packed_size(*bad) == 0
+
+
+def test_kernel_selection():
+    assert mnb.mnb_select_kernel(1, 11008, 4096, 4, 32, mnb.MNB_BF16) == "gemv"
+    assert mnb.mnb_select_kernel(8, 14336, 4096, 2, 64, mnb.MNB_BF16) == "gemv_mma"
+    assert mnb.mnb_select_kernel(16, 4096, 4096, 4, 32, mnb.MNB_F16) == "gemv_mma"
+    assert mnb.mnb_select_kernel(17, 4096, 4096, 4, 32, mnb.MNB_BF16) == "gemm_tc"
+    assert mnb.mnb_select_kernel(512, 4096, 4096, 4, 32, mnb.MNB_BF16) == "gemm_tc"
+    assert mnb.mnb_select_kernel(8, 4096, 4096, 4, 32, mnb.MNB_F32) == "generic"
+    assert mnb.mnb_select_kernel(1, 4096, 4096, 4, 32, mnb.MNB_BF16, 4) == "gemv_i8"
+
+
+FAKE = 1 << 20  # aligned, never dereferenced: validation fails before any CUDA call
+
+
+def _ex(lib, **kw):
+    a = mnb.MatmulArgs()
+    d = dict(x=FAKE, packed_b=FAKE, scales=FAKE, y=FAKE, M=1, N=64, K=64, bits=4, block_size=32,
+             act_dtype=2, out_dtype=2, scale_dtype=1, bias_dtype=0, accuracy_level=0, kernel=0)
+    d.update(kw)
+    for k, v in d.items():
+        setattr(a, k, v)
+    return lib.mnb_matmul_ex(ctypes.byref(a))
+
+
+@pytest.mark.parametrize("kw", [
+    dict(bits=3), dict(block_size=48), dict(block_size=8), dict(N=0), dict(K=0), dict(M=-1),
+    dict(act_dtype=7), dict(out_dtype=-1), dict(scale_dtype=3), dict(accuracy_level=5),
+    dict(x=0), dict(packed_b=0), dict(scales=0), dict(y=0), dict(x=FAKE + 8), dict(y=FAKE + 4),
+    dict(packed_b=FAKE + 16), dict(scales=FAKE + 1), dict(g_idx=FAKE + 2),
+])
+def test_matmul_ex_rejects_invalid_arguments(lib, kw):
+    assert _ex(lib, **kw) == mnb.MNB_ERR_INVALID_ARG
+
+
+def test_matmul_m0_is_noop(lib):
+    assert _ex(lib, M=0, x=0, y=0) == mnb.MNB_OK
+
+
+def test_other_entry_points_reject_invalid(lib):
+    assert lib.mnb_pack_weights(FAKE, FAKE, 1 << 30, 64, 64, 5, 32, None) == mnb.MNB_ERR_INVALID_ARG
+    assert lib.mnb_pack_weights(None, FAKE, 1 << 30, 64, 64, 4, 32, None) == mnb.MNB_ERR_INVALID_ARG
+    assert lib.mnb_pack_weights(FAKE, FAKE + 16, 1 << 30, 64, 64, 4, 32, None) == mnb.MNB_ERR_INVALID_ARG
+    assert lib.mnb_pack_weights(FAKE, FAKE, 100, 64, 64, 4, 32, None) == mnb.MNB_ERR_NO_MEM
+    assert lib.mnb_unpack_codes(FAKE, None, 64, 64, 4, 32, None) == mnb.MNB_ERR_INVALID_ARG
+    assert lib.mnb_dequantize(FAKE, FAKE, None, FAKE + 2, 64, 64, 4, 32, 1, None) == mnb.MNB_ERR_INVALID_ARG
+    assert lib.mnb_quantize_activations(FAKE, FAKE, FAKE, 1, 64, 24, 2, None) == mnb.MNB_ERR_INVALID_ARG
+    assert lib.mnb_workspace_size(1, 64, 64, 4, 32, 0) == 0
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert mnb.mnb_status_string(s)
+    assert mnb.mnb_kernel_name(3) == "gemm_tc"
