@@ -259,19 +259,20 @@ def run_ours(args):
         steps_eff = steps
         clocks = ClockSampler(local)
         clocks.start()
-        for _ in range(warmup // R):
-            g.replay()
         with torch.cuda.stream(stream):
+            for _ in range(warmup // R):
+                g.replay()
             for i in range(warmup % R):
                 call(i)
         barrier()
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        ev1.record(stream)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            ev1.record(stream)
         barrier()
         ck = clocks.stop()
         t = ev0.elapsed_time(ev1) / 1e3
@@ -313,13 +314,15 @@ def run_ours(args):
                     xd.copy_(xh, non_blocking=True)
                     call(i, xin=xd)
                     yh.copy_(yb, non_blocking=True)
-            ge.replay()
+            with torch.cuda.stream(stream):
+                ge.replay()
             barrier()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(max(1, reps)):
-                ge.replay()
-            e1.record(stream)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(max(1, reps)):
+                    ge.replay()
+                e1.record(stream)
             barrier()
             te = e0.elapsed_time(e1) / 1e3
             if dist is not None:

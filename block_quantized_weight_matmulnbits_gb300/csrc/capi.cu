@@ -196,8 +196,7 @@ mnb_kernel mnb_select_kernel(int64_t M, int64_t N, int64_t K, int bits, int bloc
     (void)block_size;
     const int64_t gemv_max_m = env_int("MNB_GEMV_MAX_M", 16);
     if (accuracy_level == 4) return MNB_KERNEL_GEMV_I8;
-    if (M == 1) return MNB_KERNEL_GEMV;
-    if (act_dtype == MNB_F32) return MNB_KERNEL_GENERIC;
+    if (act_dtype == MNB_F32) return M == 1 ? MNB_KERNEL_GEMV : MNB_KERNEL_GENERIC;
     if (M <= gemv_max_m) return MNB_KERNEL_GEMV_MMA;
     return MNB_KERNEL_GEMM_TC;
 }
@@ -244,7 +243,8 @@ mnb_status mnb_matmul_ex(const mnb_matmul_args* a) {
         // kernel takes every float-path call.
         if (a->g_idx && a->accuracy_level != 4) k = MNB_KERNEL_GENERIC;
         if (k == MNB_KERNEL_GEMV && !gemv_supported(p)) k = MNB_KERNEL_GENERIC;
-        if (k == MNB_KERNEL_GEMV_MMA && !gemv_mma_supported(p)) k = MNB_KERNEL_GEMM_TC;
+        if (k == MNB_KERNEL_GEMV_MMA && !gemv_mma_supported(p)) k = a->M == 1 ? MNB_KERNEL_GEMV : MNB_KERNEL_GEMM_TC;
+        if (k == MNB_KERNEL_GEMV && !gemv_supported(p)) k = MNB_KERNEL_GENERIC;
         if (k == MNB_KERNEL_GEMM_TC && !gemm_tc_supported(p)) k = MNB_KERNEL_GENERIC;
     }
     if (a->accuracy_level == 4 && k != MNB_KERNEL_GEMV_I8) return MNB_ERR_UNSUPPORTED;

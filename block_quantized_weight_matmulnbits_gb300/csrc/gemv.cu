@@ -26,6 +26,7 @@
 //  * Partial sums of the warps are reduced in a fixed order through shared
 //    memory, so results are bit-identical run to run.
 #include <cstdio>
+#include <cstdlib>
 
 #include "mnb_internal.h"
 
@@ -34,64 +35,59 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kSlots = 12;      // ring slots per warp
-constexpr int kChunkTiles = 2;  // 512-byte tiles per bulk copy
+constexpr int kMaxSlots = 12;   // ring slots per warp (as many as shared memory allows, >= kMinSlots)
+constexpr int kMinSlots = 4;
+constexpr int kChunkTiles = 4;  // 512-byte tiles per bulk copy
 constexpr int kChunkBytes = kChunkTiles * kTileBytes;
+constexpr int kRawSlots = 4;    // row-tiles of raw scales / zero points in flight
 constexpr uint32_t kMagic23 = 0x4B000000u;  // 2^23
-constexpr int kStageRegs = 8;   // staged (row, block) entries per thread prefetched into registers
+
 
 struct GemvGeom {
     int64_t kblocks_pad;  // staged blocks per row (covers KTILES * KT depths)
     int64_t ktw;          // k-tiles per warp slice
-    int64_t nch;          // chunks per warp slice
-    size_t xs_bytes, ring_bytes, stage_bytes, red_bytes, bar_bytes, total_bytes;
+    int slots;            // ring slots per warp
+    int stage_bufs;       // 2: convert the next row-tile while others finish; 1: extra barrier
+    int raw_scale_bytes;  // scales of one row-tile (16 rows)
+    int raw_zp_bytes;     // zero points of one row-tile (0 when absent)
+    size_t ring_bytes, xs_bytes, raw_bytes, stage_bytes, red_bytes, bar_bytes, total_bytes;
 };
 
-__host__ GemvGeom gemv_geom(const Layout& L) {
+// Tuning overrides (environment, read per call): MNB_GEMV_STAGE_BUFS = 1 or 2,
+// MNB_GEMV_MAX_SLOTS = 4..12.  Defaults pick the deepest ring that fits.
+static int env_or(const char* name, int dflt) {
+    const char* v = std::getenv(name);
+    return (v && *v) ? std::atoi(v) : dflt;
+}
+
+__host__ GemvGeom gemv_geom(const Layout& L, int scale_dtype, bool has_zp, size_t smem_limit) {
+    const int force_bufs = env_or("MNB_GEMV_STAGE_BUFS", 0);
+    int max_slots = env_or("MNB_GEMV_MAX_SLOTS", kMaxSlots);
+    max_slots = max_slots < kMinSlots ? kMinSlots : (max_slots > kMaxSlots ? kMaxSlots : max_slots);
     GemvGeom g;
     g.kblocks_pad = (L.KTILES * L.KT + L.bs - 1) / L.bs;
-    g.ktw = (L.KTILES + kWarps - 1) / kWarps;
-    g.nch = (g.ktw + kChunkTiles - 1) / kChunkTiles;
+    // whole chunks per warp slice, so quantisation blocks never straddle a chunk
+    g.ktw = ((L.KTILES + kWarps - 1) / kWarps + kChunkTiles - 1) / kChunkTiles * kChunkTiles;
+    g.raw_scale_bytes = (int)(16 * L.KB * (scale_dtype == kF32 ? 4 : 2));
+    g.raw_zp_bytes = has_zp ? (int)(16 * L.zp_row) : 0;
     g.xs_bytes = (size_t)L.KTILES * L.KT * 4;
-    g.ring_bytes = (size_t)kWarps * kSlots * kChunkBytes;
-    g.stage_bytes = (size_t)2 * 16 * (g.kblocks_pad | 1) * 16;
+    g.raw_bytes = (size_t)kRawSlots * (round16(g.raw_scale_bytes) + round16(g.raw_zp_bytes));
     g.red_bytes = (size_t)2 * kWarps * 16 * 4;
-    g.bar_bytes = (size_t)kWarps * kSlots * 8;
-    g.total_bytes = g.ring_bytes + g.xs_bytes + g.stage_bytes + g.red_bytes + g.bar_bytes + 128;
+    g.bar_bytes = (size_t)(kWarps * kMaxSlots + kRawSlots) * 8;
+    // Prefer a double-buffered stage and the deepest ring that fits.
+    for (int bufs = 2; bufs >= 1; --bufs) {
+        if (force_bufs && bufs != force_bufs) continue;
+        g.stage_bufs = bufs;
+        g.stage_bytes = (size_t)bufs * 16 * (g.kblocks_pad | 1) * 16;
+        const size_t fixed = g.xs_bytes + g.raw_bytes + g.stage_bytes + g.red_bytes + g.bar_bytes + 128;
+        int slots = max_slots;
+        while (slots > kMinSlots && fixed + (size_t)kWarps * slots * kChunkBytes > smem_limit) --slots;
+        g.slots = slots;
+        g.ring_bytes = (size_t)kWarps * slots * kChunkBytes;
+        g.total_bytes = g.ring_bytes + fixed;
+        if (g.total_bytes <= smem_limit && (bufs == 1 || slots >= 6)) break;
+    }
     return g;
-}
-
-__host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
-
-__device__ __forceinline__ uint64_t pack2(float a, float b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t pack2u(uint32_t a, uint32_t b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(a), "r"(b));
-    return r;
-}
-__device__ __forceinline__ float2 unpack2(uint64_t v) {
-    float2 r;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-    return r;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
 }
 
 // Staged per-(row, block) entry: the pair to subtract, (2^23 + zp, 2^23 + zp*2^pb)
@@ -161,77 +157,166 @@ struct Unpack<8> {
     static constexpr int kStepsPerTile = 2;
 };
 
-template <int BITS>
+// SPB_LOG: log2 of the k-steps per quantisation block when the block
+// structure inside a chunk is static (blocks of 1, 2, 4 or 8 k-steps that tile
+// the chunk); -1 handles any block size with run-time checks.
+template <int BITS, int SPB_LOG>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(MatmulParams p, GemvGeom geo) {
     using U = Unpack<BITS>;
     const Layout& L = p.L;
     extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t* ring = smem;                                                   // [warps][slots][chunk]
-    float* xs = reinterpret_cast<float*>(smem + geo.ring_bytes);            // permuted x'
-    StageEntry* stage = reinterpret_cast<StageEntry*>(smem + geo.ring_bytes + geo.xs_bytes);
-    float* red = reinterpret_cast<float*>(smem + geo.ring_bytes + geo.xs_bytes + geo.stage_bytes);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + geo.ring_bytes + geo.xs_bytes + geo.stage_bytes +
-                                                 geo.red_bytes);
+    uint8_t* ring = smem;                                               // [warps][slots][chunk]
+    float* xs = reinterpret_cast<float*>(smem + geo.ring_bytes);        // permuted x'
+    uint8_t* raw = smem + geo.ring_bytes + geo.xs_bytes;                // [kRawSlots][scales | zp]
+    StageEntry* stage = reinterpret_cast<StageEntry*>(raw + geo.raw_bytes);
+    float* red = reinterpret_cast<float*>(raw + geo.raw_bytes + geo.stage_bytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(raw + geo.raw_bytes + geo.stage_bytes + geo.red_bytes);
+    uint64_t* rbars = bars + kWarps * kMaxSlots;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int64_t NT = L.NT;
-    const int64_t my_tiles = (NT - blockIdx.x + gridDim.x - 1) / gridDim.x;  // row-tiles of this CTA
+    const int my_tiles = (int)((L.NT - blockIdx.x + gridDim.x - 1) / gridDim.x);  // row-tiles of this CTA
     if (my_tiles <= 0) return;
+    const int S_SLOTS = geo.slots;
 
-    // This warp's K-slice of every row-tile.
+    // ---- weight stream: this warp's K-slice of every row-tile of the CTA ----
     const int64_t kt_begin = imin64((int64_t)warp * geo.ktw, L.KTILES);
     const int64_t kt_end = imin64(kt_begin + geo.ktw, L.KTILES);
-    const int64_t nch = (kt_end - kt_begin + kChunkTiles - 1) / kChunkTiles;
-    const int64_t total_chunks = nch * my_tiles;
-    uint64_t* wbars = bars + warp * kSlots;
-    uint8_t* wring = ring + (size_t)warp * kSlots * kChunkBytes;
-
-    auto issue = [&](int64_t qi) {  // lane 0 only
-        const int64_t i = qi / nch, c = qi - i * nch;
-        const int64_t rt = blockIdx.x + i * gridDim.x;
-        const int64_t kt = kt_begin + c * kChunkTiles;
+    const int nch = (int)((kt_end - kt_begin + kChunkTiles - 1) / kChunkTiles);
+    const int total_chunks = nch * my_tiles;
+    uint64_t* wbars = bars + warp * kMaxSlots;
+    uint8_t* wring = ring + (size_t)warp * S_SLOTS * kChunkBytes;
+    int iss_i = 0, iss_c = 0, iss_slot = 0, issued = 0;  // next chunk to issue (row-tile, chunk, slot)
+    auto issue_next = [&]() {  // lane 0 only; caller checks issued < total_chunks
+        const int64_t rt = blockIdx.x + (int64_t)iss_i * gridDim.x;
+        const int64_t kt = kt_begin + (int64_t)iss_c * kChunkTiles;
         const uint32_t bytes = (uint32_t)(imin64(kChunkTiles, kt_end - kt) * kTileBytes);
-        const int slot = (int)(qi % kSlots);
-        mbar_arrive_expect_tx(&wbars[slot], bytes);
-        bulk_g2s(wring + slot * kChunkBytes, p.packed + (rt * L.KTILES + kt) * kTileBytes, bytes,
-                 &wbars[slot]);
+        mbar_arrive_expect_tx(&wbars[iss_slot], bytes);
+        bulk_g2s(wring + iss_slot * kChunkBytes, p.packed + (rt * L.KTILES + kt) * kTileBytes, bytes,
+                 &wbars[iss_slot]);
+    };
+    auto advance_issue = [&]() {
+        ++issued;
+        if (++iss_c == nch) { iss_c = 0; ++iss_i; }
+        if (++iss_slot == S_SLOTS) iss_slot = 0;
+    };
+
+    // ---- raw scales / zero points of whole row-tiles, bulk-copied ahead ----
+    const bool raw_ok = ((reinterpret_cast<uintptr_t>(p.scales) & 15) == 0) &&
+                        (p.zp == nullptr || (reinterpret_cast<uintptr_t>(p.zp) & 15) == 0);
+    const int raw_slot_bytes = (int)(round16(geo.raw_scale_bytes) + round16(geo.raw_zp_bytes));
+    auto tile_by_copy = [&](int i) {  // full row-tile with 16-byte aligned sources
+        const int64_t rt = blockIdx.x + (int64_t)i * gridDim.x;
+        return raw_ok && (rt * 16 + 16 <= L.N);
+    };
+    auto issue_raw = [&](int i) {  // thread 0 only
+        if (i >= my_tiles || !tile_by_copy(i)) return;
+        const int64_t rt = blockIdx.x + (int64_t)i * gridDim.x;
+        const int slot = i % kRawSlots;
+        uint8_t* dst = raw + slot * raw_slot_bytes;
+        mbar_arrive_expect_tx(&rbars[slot], (uint32_t)(geo.raw_scale_bytes + geo.raw_zp_bytes));
+        bulk_g2s(dst, static_cast<const uint8_t*>(p.scales) + rt * geo.raw_scale_bytes,
+                 (uint32_t)geo.raw_scale_bytes, &rbars[slot]);
+        if (geo.raw_zp_bytes)
+            bulk_g2s(dst + round16(geo.raw_scale_bytes), p.zp + rt * geo.raw_zp_bytes, (uint32_t)geo.raw_zp_bytes,
+                     &rbars[slot]);
     };
 
     if (lane == 0) {
-        for (int s = 0; s < kSlots; ++s) mbar_init(&wbars[s], 1);
-        fence_barrier_init();
+        for (int s = 0; s < S_SLOTS; ++s) mbar_init(&wbars[s], 1);
     }
-    __syncwarp();
-    // Start streaming at once: the prologue below overlaps the first copies.
-    int64_t issued = imin64(kSlots, total_chunks);
-    if (lane == 0)
-        for (int64_t qi = 0; qi < issued; ++qi) issue(qi);
+    if (tid == 0) {
+        for (int s = 0; s < kRawSlots; ++s) mbar_init(&rbars[s], 1);
+    }
+    fence_barrier_init();
+    __syncthreads();
+    // Start both streams at once: the prologue below overlaps the first copies.
+    if (lane == 0) {
+        while (issued < total_chunks && issued < S_SLOTS) {
+            issue_next();
+            advance_issue();
+        }
+    } else {
+        const int n0 = total_chunks < S_SLOTS ? total_chunks : S_SLOTS;
+        for (int q0 = 0; q0 < n0; ++q0) advance_issue();
+    }
+    if (tid == 0)
+        for (int i = 0; i < kRawSlots; ++i) issue_raw(i);
 
     // x': per k-step S and lane class t, (x[16S+2t], x[16S+2t+1]*2^-pb, x[16S+2t+8], x[16S+2t+9]*2^-pb).
+    // Each thread stages whole k-steps (16 activations, two or four 16-byte
+    // loads), four k-steps per round with every load issued before use.
     {
         const float odd_scale = (U::kPb == 16) ? (1.0f / 65536.0f) : 1.0f;
-        const int64_t ksteps = L.KTILES * L.KT / 16;
-        for (int64_t i = tid; i < ksteps * 4; i += kThreads) {
-            const int64_t S = i >> 2;
-            const int tt = (int)(i & 3);
-            const int64_t k0 = 16 * S + 2 * tt;
-            float v[4];
-            const int64_t ks[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
+        const int ksteps = (int)(L.KTILES * L.KT / 16);
+        const int full_steps = (int)(L.K / 16);  // k-steps lying wholly inside K
+        constexpr int kRound = 4;
+        for (int S0 = tid; S0 < ksteps; S0 += kThreads * kRound) {
+            float v[kRound][16];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = ks[j] < L.K ? load_f32(p.x, ks[j], p.act_dtype) : 0.f;
-            reinterpret_cast<float4*>(xs)[i] = make_float4(v[0], v[1] * odd_scale, v[2], v[3] * odd_scale);
+            for (int u = 0; u < kRound; ++u) {
+                const int S = S0 + u * kThreads;
+                if (S < full_steps) {
+                    if (p.act_dtype == kF32) {
+                        const float4* src = reinterpret_cast<const float4*>(p.x) + (int64_t)S * 4;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float4 f = __ldg(src + j);
+                            v[u][4 * j] = f.x;
+                            v[u][4 * j + 1] = f.y;
+                            v[u][4 * j + 2] = f.z;
+                            v[u][4 * j + 3] = f.w;
+                        }
+                    } else {
+                        const uint4* src = reinterpret_cast<const uint4*>(p.x) + (int64_t)S * 2;
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const uint4 h = __ldg(src + j);
+                            const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const uint32_t lo = hw[e] & 0xFFFFu, hi = hw[e] >> 16;
+                                if (p.act_dtype == kBF16) {
+                                    v[u][8 * j + 2 * e] = __uint_as_float(lo << 16);
+                                    v[u][8 * j + 2 * e + 1] = __uint_as_float(hi << 16);
+                                } else {
+                                    v[u][8 * j + 2 * e] = __half2float(__ushort_as_half((uint16_t)lo));
+                                    v[u][8 * j + 2 * e + 1] = __half2float(__ushort_as_half((uint16_t)hi));
+                                }
+                            }
+                        }
+                    }
+                } else if (S < ksteps) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int64_t k = 16 * (int64_t)S + j;
+                        v[u][j] = k < L.K ? load_f32(p.x, k, p.act_dtype) : 0.f;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kRound; ++u) {
+                const int S = S0 + u * kThreads;
+                if (S < ksteps) {
+#pragma unroll
+                    for (int tt = 0; tt < 4; ++tt)
+                        reinterpret_cast<float4*>(xs)[S * 4 + tt] =
+                            make_float4(v[u][2 * tt], v[u][2 * tt + 1] * odd_scale, v[u][2 * tt + 8],
+                                        v[u][2 * tt + 9] * odd_scale);
+                }
+            }
         }
     }
 
-    // Staging of (subtract constants, scale) per (row, block) of a row-tile.
-    // Entry (r, kb) lives at r * kbs + kb; kbs is odd so the 8 row groups of a
-    // warp hit different banks.
-    const int64_t kbp = geo.kblocks_pad;
-    const int64_t kbs = kbp | 1;
-    const int64_t stage_entries = 16 * kbp;
-    const int64_t stage_stride = 16 * kbs;
+    // Staged entry (r, kb) of a row-tile lives at r * kbs + kb; kbs is odd so the
+    // 8 row groups of a warp read different banks.
+    const int kbp = (int)geo.kblocks_pad;
+    const int kbs = kbp | 1;
+    const int stage_entries = 16 * kbp;
+    const int stage_stride = 16 * kbs;
+    const int sbytes = p.scale_dtype == kF32 ? 4 : 2;
+    const int zmask = code_mask(L.bits);
     auto make_entry = [&](uint32_t z, float sc) {
         StageEntry se;
         se.c0 = kMagic23 | z;
@@ -239,72 +324,65 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(MatmulParams p, GemvG
         se.s0 = se.s1 = sc;
         return se;
     };
-    auto raw_value = [&](int64_t rt, int64_t e, uint32_t* z, float* sc) {
-        const int64_t r = e / kbp, kb = e - r * kbp;
-        const int64_t n = rt * 16 + r;
-        if (n < L.N && kb < L.KB) {
-            *z = (uint32_t)load_zp(p.zp, L, n, kb);
-            *sc = load_f32(p.scales, n * L.KB + kb, p.scale_dtype);
+    // Convert row-tile i's scales and zero points into staged entries of buffer
+    // buf.  Thread (r = tid / 16, j = tid % 16) handles blocks j, j+16, ... of
+    // row r, so the 16 threads of a row read consecutive scales.
+    const int conv_r = tid >> 4, conv_j = tid & 15;
+    auto convert = [&](int i, int buf) {
+        StageEntry* dst = stage + buf * stage_stride + conv_r * kbs;
+        const int64_t rt = blockIdx.x + (int64_t)i * gridDim.x;
+        const int64_t n = rt * 16 + conv_r;
+        const int kbv = (int)L.KB;
+        if (tile_by_copy(i)) {
+            const int slot = i % kRawSlots;
+            mbar_wait(&rbars[slot], (uint32_t)((i / kRawSlots) & 1), p.status);
+            const uint8_t* rs = raw + slot * raw_slot_bytes;
+            const uint8_t* rz = rs + round16(geo.raw_scale_bytes) + conv_r * L.zp_row;
+            const float* rs32 = reinterpret_cast<const float*>(rs) + conv_r * kbv;
+            const uint16_t* rs16 = reinterpret_cast<const uint16_t*>(rs) + conv_r * kbv;
+            const bool has_zp = geo.raw_zp_bytes != 0;
+            for (int kb = conv_j; kb < kbp; kb += 16) {
+                uint32_t z = 0;
+                float sc = 0.f;
+                if (kb < kbv) {
+                    if (sbytes == 4) {
+                        sc = rs32[kb];
+                    } else {
+                        const uint16_t u = rs16[kb];
+                        sc = p.scale_dtype == kF16 ? __half2float(__ushort_as_half(u))
+                                                   : __uint_as_float((uint32_t)u << 16);
+                    }
+                    const int bit = kb * BITS;
+                    z = has_zp ? ((rz[bit >> 3] >> (bit & 7)) & zmask) : (1u << (BITS - 1));
+                }
+                dst[kb] = make_entry(z, sc);
+            }
         } else {
-            *z = 0;
-            *sc = 0.f;
-        }
-    };
-    const bool stage_in_regs = stage_entries <= (int64_t)kStageRegs * kThreads;
-    float pre_s[kStageRegs];
-    uint32_t pre_z[kStageRegs / 4];
-    auto stage_prefetch = [&](int64_t rt) {
-#pragma unroll
-        for (int j = 0; j < kStageRegs; ++j) {
-            const int64_t e = tid + (int64_t)j * kThreads;
-            uint32_t z = 0;
-            float sc = 0.f;
-            if (e < stage_entries) raw_value(rt, e, &z, &sc);
-            pre_s[j] = sc;
-            if ((j & 3) == 0) pre_z[j >> 2] = 0;
-            pre_z[j >> 2] |= z << (8 * (j & 3));
-        }
-    };
-    auto stage_commit = [&](int buf) {
-        StageEntry* dst = stage + buf * stage_stride;
-#pragma unroll
-        for (int j = 0; j < kStageRegs; ++j) {
-            const int64_t e = tid + (int64_t)j * kThreads;
-            if (e < stage_entries) {
-                const int64_t r = e / kbp, kb = e - r * kbp;
-                dst[r * kbs + kb] = make_entry((pre_z[j >> 2] >> (8 * (j & 3))) & 0xFF, pre_s[j]);
+            for (int kb = conv_j; kb < kbp; kb += 16) {
+                uint32_t z = 0;
+                float sc = 0.f;
+                if (n < L.N && kb < kbv) {
+                    z = (uint32_t)load_zp(p.zp, L, n, kb);
+                    sc = load_f32(p.scales, n * L.KB + kb, p.scale_dtype);
+                }
+                dst[kb] = make_entry(z, sc);
             }
         }
     };
-    auto stage_direct = [&](int64_t rt, int buf) {
-        StageEntry* dst = stage + buf * stage_stride;
-        for (int64_t e = tid; e < stage_entries; e += kThreads) {
-            uint32_t z;
-            float sc;
-            raw_value(rt, e, &z, &sc);
-            const int64_t r = e / kbp, kb = e - r * kbp;
-            dst[r * kbs + kb] = make_entry(z, sc);
-        }
-    };
 
-    if (stage_in_regs) {
-        stage_prefetch(blockIdx.x);
-        stage_commit(0);
-    } else {
-        stage_direct(blockIdx.x, 0);
-    }
+    convert(0, 0);
     __syncthreads();
+    if (tid == 0) issue_raw(kRawSlots);  // row-tile 0's raw slot is free again
 
     // Blocks are powers of two >= 16 depths, i.e. 2^spb_log k-steps.
-    const int spb_log = __ffs(L.bs / 16) - 1;
+    const int spb_log = SPB_LOG >= 0 ? SPB_LOG : __ffs(L.bs / 16) - 1;
     const int spb_mask = (1 << spb_log) - 1;
     bool bad = false;
-    int64_t q = 0;  // chunks consumed by this warp
-    for (int64_t i = 0; i < my_tiles; ++i) {
-        const int64_t rt = blockIdx.x + i * gridDim.x;
-        const int buf = (int)(i & 1);
-        const bool has_next = (i + 1) < my_tiles;
-        if (has_next && stage_in_regs) stage_prefetch(rt + gridDim.x);
+    int q = 0, slot = 0;
+    uint32_t parity = 0;  // consumption position in the weight ring
+    for (int i = 0; i < my_tiles; ++i) {
+        const int64_t rt = blockIdx.x + (int64_t)i * gridDim.x;
+        const int buf = geo.stage_bufs == 2 ? (i & 1) : 0;
         const StageEntry* st_g = stage + buf * stage_stride + g * kbs;
         const StageEntry* st_g8 = st_g + 8 * kbs;
 
@@ -314,57 +392,67 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(MatmulParams p, GemvG
         uint64_t cg = 0, cg8 = 0, sg = 0, sg8 = 0;
         bool first = true;
 
-        for (int64_t c = 0; c < nch; ++c, ++q) {
-            const int slot = (int)(q % kSlots);
-            if (!bad) bad = !mbar_wait(&wbars[slot], (uint32_t)((q / kSlots) & 1), p.status);
-            if (bad) continue;
-            const int64_t kt = kt_begin + c * kChunkTiles;
-            const int ntile = (int)imin64(kChunkTiles, kt_end - kt);
-            uint4 wv[kChunkTiles];
-            const uint8_t* sbase = wring + slot * kChunkBytes;
+        for (int c = 0; c < nch; ++c, ++q) {
+            if (!bad) bad = !mbar_wait(&wbars[slot], parity, p.status);
+            if (!bad) {
+                const int64_t kt = kt_begin + (int64_t)c * kChunkTiles;
+                const int ntile = (int)imin64(kChunkTiles, kt_end - kt);
+                uint4 wv[kChunkTiles];
+                const uint8_t* sbase = wring + slot * kChunkBytes;
 #pragma unroll
-            for (int tl = 0; tl < kChunkTiles; ++tl)
-                if (tl < ntile) wv[tl] = reinterpret_cast<const uint4*>(sbase + tl * kTileBytes)[lane];
+                for (int tl = 0; tl < kChunkTiles; ++tl)
+                    if (tl < ntile) wv[tl] = reinterpret_cast<const uint4*>(sbase + tl * kTileBytes)[lane];
 #pragma unroll
-            for (int tl = 0; tl < kChunkTiles; ++tl) {
-                if (tl >= ntile) break;
-                const uint32_t* w = reinterpret_cast<const uint32_t*>(&wv[tl]);
+                for (int tl = 0; tl < kChunkTiles; ++tl) {
+                    if (tl >= ntile) break;
+                    const uint32_t* w = reinterpret_cast<const uint32_t*>(&wv[tl]);
 #pragma unroll
-                for (int s = 0; s < U::kStepsPerTile; ++s, ++S) {
-                    if (first || (S & spb_mask) == 0) {
-                        first = false;
-                        const int kb = S >> spb_log;
-                        const uint4 eg = *reinterpret_cast<const uint4*>(st_g + kb);
-                        const uint4 eg8 = *reinterpret_cast<const uint4*>(st_g8 + kb);
-                        cg = pack2u(eg.x, eg.y);
-                        sg = pack2u(eg.z, eg.w);
-                        cg8 = pack2u(eg8.x, eg8.y);
-                        sg8 = pack2u(eg8.z, eg8.w);
+                    for (int s = 0; s < U::kStepsPerTile; ++s) {
+                        const int ks = tl * U::kStepsPerTile + s;  // k-step inside the chunk
+                        const bool block_start = SPB_LOG >= 0 ? ((ks & ((1 << (SPB_LOG < 0 ? 0 : SPB_LOG)) - 1)) == 0)
+                                                              : (first || ((S + ks) & spb_mask) == 0);
+                        if (block_start) {
+                            first = false;
+                            const int kb = (S + ks) >> spb_log;
+                            const uint4 eg = *reinterpret_cast<const uint4*>(st_g + kb);
+                            const uint4 eg8 = *reinterpret_cast<const uint4*>(st_g8 + kb);
+                            cg = pack2u(eg.x, eg.y);
+                            sg = pack2u(eg.z, eg.w);
+                            cg8 = pack2u(eg8.x, eg8.y);
+                            sg8 = pack2u(eg8.z, eg8.w);
+                        }
+                        const float4 xv = reinterpret_cast<const float4*>(xs)[(S + ks) * 4 + t];
+                        const uint64_t p1 = pack2(xv.x, xv.y), p2 = pack2(xv.z, xv.w);
+                        uint64_t d[4];
+                        U::kstep(w, s, cg, cg8, d);
+                        acc_g = ffma2(p1, d[0], acc_g);
+                        acc_g8 = ffma2(p1, d[1], acc_g8);
+                        acc_g = ffma2(p2, d[2], acc_g);
+                        acc_g8 = ffma2(p2, d[3], acc_g8);
+                        const bool block_end = SPB_LOG >= 0
+                                                   ? (((ks + 1) & ((1 << (SPB_LOG < 0 ? 0 : SPB_LOG)) - 1)) == 0)
+                                                   : (((S + ks + 1) & spb_mask) == 0);
+                        if (block_end) {
+                            y_g = ffma2(sg, acc_g, y_g);
+                            y_g8 = ffma2(sg8, acc_g8, y_g8);
+                            acc_g = 0;
+                            acc_g8 = 0;
+                        }
                     }
-                    const float4 xv = reinterpret_cast<const float4*>(xs)[S * 4 + t];
-                    const uint64_t p1 = pack2(xv.x, xv.y), p2 = pack2(xv.z, xv.w);
-                    uint64_t d[4];
-                    U::kstep(w, s, cg, cg8, d);
-                    acc_g = ffma2(p1, d[0], acc_g);
-                    acc_g8 = ffma2(p1, d[1], acc_g8);
-                    acc_g = ffma2(p2, d[2], acc_g);
-                    acc_g8 = ffma2(p2, d[3], acc_g8);
-                    if (((S + 1) & spb_mask) == 0) {
-                        y_g = ffma2(sg, acc_g, y_g);
-                        y_g8 = ffma2(sg8, acc_g8, y_g8);
-                        acc_g = 0;
-                        acc_g8 = 0;
-                    }
+                }
+                S += kChunkTiles * U::kStepsPerTile;
+                // Refill this slot with the next chunk.  Every lane has used the
+                // values it loaded from the slot, so the slot's reads are done
+                // before the bulk copy overwrites it.
+                __syncwarp();
+                if (issued < total_chunks) {
+                    if (lane == 0) issue_next();
+                    advance_issue();
                 }
             }
-            __syncwarp();
-            // Refill this slot with the chunk kSlots ahead (its data has been consumed).
-            if (issued < total_chunks) {
-                if (lane == 0) {
-                    fence_proxy_async_smem();
-                    issue(issued);
-                }
-                ++issued;
+            if (++slot == S_SLOTS) {
+                slot = 0;
+                parity ^= 1u;
             }
         }
         // Flush a block cut by the end of this warp's slice.
@@ -376,17 +464,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(MatmulParams p, GemvG
         vg8 += __shfl_xor_sync(0xffffffffu, vg8, 1);
         vg += __shfl_xor_sync(0xffffffffu, vg, 2);
         vg8 += __shfl_xor_sync(0xffffffffu, vg8, 2);
-        float* rb = red + buf * kWarps * 16;
+        float* rb = red + (i & 1) * kWarps * 16;
         if (t == 0) {
             rb[warp * 16 + g] = vg;
             rb[warp * 16 + g + 8] = vg8;
         }
-        if (has_next) {
-            if (stage_in_regs) stage_commit(buf ^ 1);
-            else stage_direct(rt + gridDim.x, buf ^ 1);
+        if (i + 1 < my_tiles) {
+            if (geo.stage_bufs == 1) __syncthreads();  // every warp is done with the only stage buffer
+            convert(i + 1, geo.stage_bufs == 2 ? (buf ^ 1) : 0);
         }
         __syncthreads();
-        if (warp == (int)(i % kWarps) && lane < 16) {
+        if (tid == 0) issue_raw(i + 1 + kRawSlots);
+        if (warp == (i % kWarps) && lane < 16) {
             float v = 0.f;
 #pragma unroll
             for (int w2 = 0; w2 < kWarps; ++w2) v += rb[w2 * 16 + lane];
@@ -397,12 +486,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(MatmulParams p, GemvG
             }
         }
     }
-    // After a timed-out wait, give copies still in flight a bounded chance to land before exit.
+    // After a timed-out wait, give copies still in flight a bounded chance to
+    // land before the CTA exits.
     if (bad && lane == 0) {
-        for (int64_t qq = q; qq < issued; ++qq) {
-            const int slot = (int)(qq % kSlots);
+        for (int qq = q; qq < issued; ++qq) {
+            const int sl = qq % S_SLOTS;
+            const uint32_t ph = (uint32_t)((qq / S_SLOTS) & 1);
             for (int it = 0; it < (1 << 16); ++it)
-                if (mbar_try_wait(&wbars[slot], (uint32_t)((qq / kSlots) & 1))) break;
+                if (mbar_try_wait(&wbars[sl], ph)) break;
         }
     }
 }
@@ -411,36 +502,48 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(MatmulParams p, GemvG
 
 bool gemv_supported(const MatmulParams& p) {
     if (p.M != 1 || p.g_idx != nullptr) return false;
-    const GemvGeom g = gemv_geom(p.L);
-    return g.total_bytes <= device_info().smem_optin;
+    const size_t limit = device_info().smem_optin;
+    const GemvGeom g = gemv_geom(p.L, p.scale_dtype, p.zp != nullptr, limit);
+    return g.total_bytes <= limit;
+}
+
+template <int BITS, int SPB_LOG>
+static cudaError_t launch_one(const MatmulParams& p, const GemvGeom& geo, int64_t grid, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<BITS, SPB_LOG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)geo.total_bytes);
+    if (e != cudaSuccess) return e;
+    gemv_kernel<BITS, SPB_LOG><<<(unsigned)grid, kThreads, geo.total_bytes, s>>>(p, geo);
+    return cudaGetLastError();
+}
+
+// The static block structure needs blocks that tile every chunk: k-steps per
+// block dividing the k-steps of a chunk (warp slices are whole chunks).
+template <int BITS>
+static cudaError_t launch_bits(const MatmulParams& p, const GemvGeom& geo, int64_t grid, cudaStream_t s) {
+    constexpr int steps_per_chunk = kChunkTiles * (256 / BITS) / 16;
+    const int spb = p.L.bs / 16;
+    if (spb <= steps_per_chunk) {
+        switch (spb) {
+            case 1: return launch_one<BITS, 0>(p, geo, grid, s);
+            case 2: return launch_one<BITS, 1>(p, geo, grid, s);
+            case 4: return launch_one<BITS, 2>(p, geo, grid, s);
+            case 8: return launch_one<BITS, 3>(p, geo, grid, s);
+            default: break;
+        }
+    }
+    return launch_one<BITS, -1>(p, geo, grid, s);
 }
 
 cudaError_t launch_gemv(const MatmulParams& p, cudaStream_t s) {
-    const GemvGeom geo = gemv_geom(p.L);
     const DeviceInfo& di = device_info();
+    const GemvGeom geo = gemv_geom(p.L, p.scale_dtype, p.zp != nullptr, di.smem_optin);
     const int64_t grid = imin64(p.L.NT, di.sm_count);
-    cudaError_t e = cudaSuccess;
     switch (p.L.bits) {
-        case 2:
-            e = cudaFuncSetAttribute(gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)geo.total_bytes);
-            if (e == cudaSuccess) gemv_kernel<2><<<(unsigned)grid, kThreads, geo.total_bytes, s>>>(p, geo);
-            break;
-        case 4:
-            e = cudaFuncSetAttribute(gemv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)geo.total_bytes);
-            if (e == cudaSuccess) gemv_kernel<4><<<(unsigned)grid, kThreads, geo.total_bytes, s>>>(p, geo);
-            break;
-        case 8:
-            e = cudaFuncSetAttribute(gemv_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)geo.total_bytes);
-            if (e == cudaSuccess) gemv_kernel<8><<<(unsigned)grid, kThreads, geo.total_bytes, s>>>(p, geo);
-            break;
-        default:
-            return cudaErrorInvalidValue;
+        case 2: return launch_bits<2>(p, geo, grid, s);
+        case 4: return launch_bits<4>(p, geo, grid, s);
+        case 8: return launch_bits<8>(p, geo, grid, s);
+        default: return cudaErrorInvalidValue;
     }
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
 }
 
 }  // namespace mnb

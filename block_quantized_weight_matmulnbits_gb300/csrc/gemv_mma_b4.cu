@@ -1,0 +1,9 @@
+// Instantiation of the small-batch tensor-core GEMV for 4-bit codes (one
+// translation unit per code width keeps the build parallel).
+#include "gemv_mma.cuh"
+
+namespace mnb {
+cudaError_t launch_gemv_mma_b4(const MatmulParams& p, const gmma::Geom& geo, int64_t grid, cudaStream_t s) {
+    return gmma::launch_bits<4>(p, geo, grid, s);
+}
+}  // namespace mnb

@@ -4,9 +4,6 @@
 
 namespace mnb {
 
-bool gemv_mma_supported(const MatmulParams&) { return false; }
-cudaError_t launch_gemv_mma(const MatmulParams&, cudaStream_t) { return cudaErrorNotSupported; }
-
 bool gemm_tc_supported(const MatmulParams&) { return false; }
 cudaError_t launch_gemm_tc(const MatmulParams&, cudaStream_t) { return cudaErrorNotSupported; }
 

@@ -76,8 +76,9 @@ typedef enum mnb_dtype { MNB_F32 = 0, MNB_F16 = 1, MNB_BF16 = 2 } mnb_dtype;
  * kernel that cannot handle the call returns MNB_ERR_UNSUPPORTED. */
 typedef enum mnb_kernel {
     MNB_KERNEL_AUTO = 0,
-    MNB_KERNEL_GEMV = 1,      /* M == 1 decode GEMV, CUDA cores, TMA-streamed weights */
-    MNB_KERNEL_GEMV_MMA = 2,  /* 1 <= M <= 16, bf16/f16 X, warp-level tensor-core MMA on registers */
+    MNB_KERNEL_GEMV = 1,      /* M == 1 decode GEMV, any X dtype, CUDA cores, TMA-streamed weights */
+    MNB_KERNEL_GEMV_MMA = 2,  /* 1 <= M <= 16, bf16/f16 X, warp-level tensor-core MMA on registers,
+                                 TMA-streamed weights (the decode default for bf16/f16 X) */
     MNB_KERNEL_GEMM_TC = 3,   /* M >= 1 prefill GEMM, bf16/f16 X, tcgen05 + TMEM + TMA */
     MNB_KERNEL_GENERIC = 4,   /* any shape and dtype, CUDA cores, shared-memory tiles */
     MNB_KERNEL_GEMV_I8 = 5    /* int8-activation path (accuracy_level 4), integer dot products */

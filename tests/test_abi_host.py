@@ -57,7 +57,9 @@ def test_packed_size_rejects_invalid(bad):
 
 
 def test_kernel_selection():
-    assert mnb.mnb_select_kernel(1, 11008, 4096, 4, 32, mnb.MNB_BF16) == "gemv"
+    assert mnb.mnb_select_kernel(1, 11008, 4096, 4, 32, mnb.MNB_BF16) == "gemv_mma"
+    assert mnb.mnb_select_kernel(1, 4096, 11008, 8, 128, mnb.MNB_F16) == "gemv_mma"
+    assert mnb.mnb_select_kernel(1, 256, 256, 4, 32, mnb.MNB_F32) == "gemv"
     assert mnb.mnb_select_kernel(8, 14336, 4096, 2, 64, mnb.MNB_BF16) == "gemv_mma"
     assert mnb.mnb_select_kernel(16, 4096, 4096, 4, 32, mnb.MNB_F16) == "gemv_mma"
     assert mnb.mnb_select_kernel(17, 4096, 4096, 4, 32, mnb.MNB_BF16) == "gemm_tc"

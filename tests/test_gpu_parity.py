@@ -75,6 +75,11 @@ for i, (bits, bs) in enumerate(BITS_BS):
     for asym in (True, False):
         dt = DTYPES[(i + asym) % len(DTYPES)]
         GEMV_CASES.append((bits, bs, asym, dt, 300, 3 * bs + 5))
+# long rows: every warp slice holds whole chunks, so each block size takes the
+# statically unrolled path (1, 2, 4 or 8 k-steps per block)
+for bits in (2, 4, 8):
+    for bs in (16, 32, 64, 128):
+        GEMV_CASES.append((bits, bs, bs != 32, DTYPES[(bits + bs) % len(DTYPES)], 40, 4096 + bs))
 GEMV_CASES += [(4, 32, True, DTYPES[0], 64, 4096), (8, 128, True, DTYPES[1], 48, 11008),
                (2, 64, True, DTYPES[0], 33, 4096), (4, 32, False, DTYPES[2], 16, 32),
                (4, 16, True, DTYPES[3], 1, 16), (8, 16, True, DTYPES[4], 7, 1)]
@@ -88,6 +93,31 @@ def test_matmul_m1(G, bits, bs, asym, dt, N, K, kernel):
     y = P.y64(P.run(kernel))
     ref, mag = P.oracle_full()
     G.assert_within(y, ref, mag, w.out_dtype, f"{kernel} {w.name}")
+
+
+MMA_CASES = []
+for i, (bits, bs) in enumerate(BITS_BS):
+    for M in (1, 3, 8, 9, 16):
+        act = BF16 if (i + M) % 2 else F16
+        MMA_CASES.append((M, bits, bs, (act, [F16, F32, BF16][(i + M) % 3], [BF16, F16, F32][i % 3]),
+                          (i + M) % 3 != 0, 150 + 16 * (i % 3) + M, 3 * bs + 5))
+for bits in (2, 4, 8):
+    for bs in (16, 32, 64, 128):
+        for M in (1, 8):
+            MMA_CASES.append((M, bits, bs, (BF16 if bs != 64 else F16, F16, BF16), bs != 32, 40, 4096 + bs))
+MMA_CASES += [(1, 4, 32, (BF16, F16, BF16), True, 64, 4096), (1, 8, 128, (F16, F32, F16), True, 48, 11008),
+              (8, 2, 64, (BF16, F16, BF16), True, 33, 4096), (16, 4, 32, (F16, F16, F16), False, 16, 32),
+              (2, 4, 16, (BF16, BF16, F32), True, 1, 16), (5, 8, 16, (F16, F16, BF16), True, 7, 1),
+              (12, 8, 32, (BF16, F32, BF16), True, 100, 200)]
+
+
+@pytest.mark.parametrize("M,bits,bs,dt,asym,N,K", MMA_CASES)
+def test_matmul_gemv_mma(G, M, bits, bs, dt, asym, N, K):
+    w = _w(M, N, K, bits, bs, dt, asym, 700 + M * 13 + bits * 7 + bs + N)
+    P = G.Problem(w)
+    y = P.y64(P.run("gemv_mma"))
+    ref, mag = P.oracle_full()
+    G.assert_within(y, ref, mag, w.out_dtype, f"gemv_mma {w.name}")
 
 
 @pytest.mark.parametrize("M", [2, 3, 8, 17, 33, 64])
@@ -117,7 +147,7 @@ def test_bias_and_g_idx_generic(G, mnb):
     G.assert_within(P.y64(y), ref, mag, w.out_dtype, "g_idx+bias")
 
 
-@pytest.mark.parametrize("kernel", ["gemv", "generic"])
+@pytest.mark.parametrize("kernel", ["gemv", "gemv_mma", "generic"])
 def test_bias_m1(G, mnb, kernel):
     w = _w(1, 100, 96, 4, 32, DTYPES[0], True, 310)
     P = G.Problem(w)
@@ -133,7 +163,7 @@ def test_bias_m1(G, mnb, kernel):
 
 # ---- degenerate cases --------------------------------------------------------
 
-@pytest.mark.parametrize("kernel", ["gemv", "generic"])
+@pytest.mark.parametrize("kernel", ["gemv", "gemv_mma", "generic"])
 @pytest.mark.parametrize("bits", [2, 4, 8])
 def test_all_codes_equal_zero_point_give_zero(G, mnb, kernel, bits):
     from tests._golden import pack_matrix_test, pack_zp_test
@@ -165,7 +195,7 @@ def test_one_hot_row_selects_weight(G, mnb, oracle_mod, kernel):
         assert np.array_equal(y, wref[:, k0])
 
 
-@pytest.mark.parametrize("kernel", ["gemv", "generic"])
+@pytest.mark.parametrize("kernel", ["gemv", "gemv_mma", "generic"])
 def test_deterministic_and_n_split_bit_identical(G, mnb, kernel):
     N, K = 96, 1024
     w = _w(1, N, K, 4, 32, DTYPES[0], True, 420)
