@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--kernel", default="auto")
+    ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -211,6 +212,8 @@ def run_ours(args):
     mnb.load()
     pk, pk_src = peaks()
 
+    flags = 0 if args.no_pdl else mnb.MNB_FLAG_PDL
+
     def measure(w: wl.Workload, steps: int, warmup: int, kernel: str, want_e2e: bool):
         data = wl.generate(w)
         x = to_dev(data["x"], w.act_dtype)
@@ -238,7 +241,7 @@ def run_ours(args):
             pb, s, zp = copies[i % R]
             mnb.mnb_matmul_ex(x if xin is None else xin, pb, s, zp, yb if yout is None else yout, w.M, w.N,
                               w.K, w.bits, w.bs, w.act_dtype, w.out_dtype, w.scale_dtype, kernel=kernel,
-                              stream=stream)
+                              stream=stream, flags=flags)
 
         with torch.cuda.stream(stream):
             for i in range(R):

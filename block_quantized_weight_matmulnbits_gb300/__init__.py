@@ -17,6 +17,7 @@ from . import _build
 MNB_OK, MNB_ERR_INVALID_ARG, MNB_ERR_UNSUPPORTED, MNB_ERR_CUDA, MNB_ERR_NO_MEM, MNB_ERR_TIMEOUT, \
     MNB_ERR_LAYOUT_MISMATCH = range(7)
 MNB_F32, MNB_F16, MNB_BF16 = 0, 1, 2
+MNB_FLAG_PDL = 1
 KERNELS = {"auto": 0, "gemv": 1, "gemv_mma": 2, "gemm_tc": 3, "generic": 4, "gemv_i8": 5}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 
@@ -42,7 +43,7 @@ class MatmulArgs(ctypes.Structure):
         ("bits", ctypes.c_int), ("block_size", ctypes.c_int), ("act_dtype", ctypes.c_int),
         ("out_dtype", ctypes.c_int), ("scale_dtype", ctypes.c_int), ("bias_dtype", ctypes.c_int),
         ("accuracy_level", ctypes.c_int), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-        ("kernel", ctypes.c_int), ("stream", ctypes.c_void_p),
+        ("kernel", ctypes.c_int), ("stream", ctypes.c_void_p), ("flags", ctypes.c_int),
     ]
 
 
@@ -146,7 +147,7 @@ def mnb_matmul(x, packed_b, scales, zero_points, y, M, N, K, bits, block_size, a
 
 def mnb_matmul_ex(x, packed_b, scales, zero_points, y, M, N, K, bits, block_size, act_dtype, out_dtype,
                   scale_dtype, g_idx=None, bias=None, bias_dtype=MNB_F32, accuracy_level=0, workspace=None,
-                  kernel="auto", stream=None):
+                  kernel="auto", stream=None, flags=0):
     a = MatmulArgs()
     a.x, a.packed_b, a.scales, a.zero_points = _ptr(x), _ptr(packed_b), _ptr(scales), _ptr(zero_points)
     a.g_idx, a.bias, a.y = _ptr(g_idx), _ptr(bias), _ptr(y)
@@ -157,6 +158,7 @@ def mnb_matmul_ex(x, packed_b, scales, zero_points, y, M, N, K, bits, block_size
     a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     a.kernel = KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
     a.stream = _stream(stream)
+    a.flags = flags
     _check(load().mnb_matmul_ex(ctypes.byref(a)), f"mnb_matmul_ex[{kernel}]")
 
 

@@ -235,6 +235,7 @@ mnb_status mnb_matmul_ex(const mnb_matmul_args* a) {
     p.status = pd->status;
     p.workspace = a->workspace;
     p.workspace_bytes = a->workspace_bytes;
+    p.flags = a->flags;
 
     mnb_kernel k = a->kernel;
     if (k == MNB_KERNEL_AUTO) {

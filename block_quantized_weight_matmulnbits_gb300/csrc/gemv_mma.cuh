@@ -7,23 +7,28 @@
 // GB300 design.
 //
 // Why tensor cores for an HBM-bound GEMV: exact unpacking costs at least two
-// issue slots per weight (mask into a float's mantissa, subtract), and a CUDA-
-// core FMA per weight on top of that exceeds the issue budget GB300 leaves per
-// weight when HBM3e streams ~7 TB/s.  With W rows as the MMA's M dimension
-// (16 rows) and activation rows as its N dimension (8 or 16), one mma.sync
-// m16n8k16 consumes 256 weights per warp, so the contraction costs almost no
-// issue slots and the unpack dominates:
+// issue slots per weight (mask into a float's mantissa, subtract), and a
+// CUDA-core FMA per weight on top of that exceeds the issue budget GB300
+// leaves per weight when HBM3e streams ~7 TB/s.  With W rows as the MMA's M
+// dimension (16 rows) and activation rows as its N dimension (8 or 16), one
+// mma.sync m16n8k16 consumes 256 weights per warp, so the contraction costs
+// almost no issue slots and the unpack dominates:
 //   * the packed layout gives each lane its A fragment directly: a 16-bit
 //     code pair is masked into the mantissa of 128.0 (bf16) or 1024.0 (f16),
 //     and one packed 16-bit subtract of (magic + zp) yields (q - zp) exactly;
-//   * the MMA accumulates one quantisation block in f32 (products of bf16 or
-//     f16 integers and activations are exact), then the fragment is scaled by
-//     the block's f32 scale into the running sum;
-//   * weights stream through a per-warp ring of shared-memory slots filled by
-//     1-D bulk copies (cp.async.bulk, TMA engine), scales and zero points of
-//     whole row-tiles are bulk-copied ahead and converted once per CTA.
-// Partial sums of the warps (K-slices) are reduced in a fixed order, so
-// results are bit-identical run to run.
+//   * the MMA accumulates one quantisation block in f32 (products of small
+//     integers and bf16/f16 activations are exact), then the fragment is
+//     scaled by the block's f32 scale into the running sum.
+//
+// Work decomposition (measured on GB300: many resident CTAs with loads in
+// registers stream a ~26 MB weight faster per launch than persistent
+// bulk-copy rings): one CTA of 8 warps per (16-row tile, K-split); each warp
+// issues all its 16-byte weight loads (up to 8 tiles) before anything else,
+// then stages the CTA's activations and per-block scales / zero points in
+// shared memory, then computes.  When K needs more than one CTA the K-splits
+// of a row tile form a thread-block cluster and are summed through
+// distributed shared memory in a fixed order; no global scratch is used.
+// Every reduction order is fixed, so results are bit-identical run to run.
 #pragma once
 
 #include <cstdlib>
@@ -33,25 +38,24 @@
 namespace mnb {
 namespace gmma {
 
-constexpr int kMaxSlots = 12;
-constexpr int kMinSlots = 3;
-constexpr int kRawSlots = 4;
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxTPW = 8;       // tiles per warp per round (all loads in flight together)
+constexpr int kMaxCluster = 8;   // portable cluster size
 constexpr uint32_t kMagic23 = 0x4B000000u;
 
 struct Geom {
-    int warps;            // consumer warps per CTA (8 or 16)
-    int chunk_tiles;      // 512-byte tiles per bulk copy (1, 2 or 4)
-    int slots;            // ring slots per warp
-    int stage_bufs;       // 1 or 2
-    int64_t ktw;          // k-tiles per warp slice (multiple of chunk_tiles)
-    int64_t kblocks_pad;  // staged blocks per row
-    int64_t ks_total;     // k-steps per row (KTILES * KT / 16)
-    int raw_scale_bytes, raw_zp_bytes;
-    size_t ring_bytes, xb_bytes, raw_bytes, stage_bytes, red_bytes, bar_bytes, total_bytes;
+    int C;            // K-splits = cluster size
+    int tiles_cta;    // k-tiles per CTA (a multiple of kWarps * tpw, except the last split)
+    int tpw;          // k-tiles per warp per round
+    int rounds;       // rounds per warp
+    int kb_cta;       // staged blocks per CTA (covers tiles_cta * KT depths)
+    int ks_cta;       // k-steps per CTA
+    size_t xb_bytes, stage_bytes, red_bytes, part_bytes, total_bytes;
 };
 
 struct __align__(8) Entry {
-    uint32_t zc;  // subtraction constant for the row-block (see unpack)
+    uint32_t zc;  // subtraction constant for the row-block (see Unpack::zconst)
     float s;      // scale
 };
 
@@ -69,6 +73,13 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
     uint32_t d;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
     return d;
+}
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
 
 template <bool BF16X>
@@ -98,18 +109,18 @@ struct Unpack {
     static constexpr int kStepsPerTile = 16 / BITS;  // 4-bit: 4, 2-bit: 8, 8-bit: 2
     static constexpr uint32_t kMagic16x2 = BF16X ? 0x43004300u : 0x64006400u;  // 128.0 / 1024.0 pairs
 
-    // Subtraction constant of a row-block with zero point z.
     __device__ __forceinline__ static uint32_t zconst(uint32_t z) {
         if constexpr (BITS == 8 && BF16X) {
-            return kMagic23 | z;  // f32 2^23 + z
+            return kMagic23 | z;  // f32 2^23 + z (8-bit codes do not fit a bf16 mantissa)
         } else {
-            const uint32_t h = (kMagic16x2 & 0xFFFFu) + z;  // magic + z, one 16-bit lane
+            const uint32_t h = (kMagic16x2 & 0xFFFFu) + z;  // magic + z in one 16-bit lane
             return h | (h << 16);
         }
     }
 
-    __device__ __forceinline__ static void kstep(const uint32_t* w, int s, uint32_t zg, uint32_t zg8,
+    __device__ __forceinline__ static void kstep(const uint4& wv, int s, uint32_t zg, uint32_t zg8,
                                                  uint32_t (&a)[4]) {
+        const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
         if constexpr (BITS == 4) {
             const uint32_t word = w[s];
 #pragma unroll
@@ -150,413 +161,404 @@ inline int env_or(const char* name, int dflt) {
     return (v && *v) ? std::atoi(v) : dflt;
 }
 
-// Host-side geometry: the widest CTA and deepest ring that fit shared memory.
-// Overrides for tuning: MNB_MMA_WARPS (8/16), MNB_MMA_CHUNK (1/2/4 tiles),
-// MNB_MMA_SLOTS (max ring slots per warp), MNB_MMA_STAGE_BUFS (1/2).
-inline Geom make_geom(const Layout& L, int64_t M, int scale_dtype, bool has_zp, size_t smem_limit, int MT) {
-    Geom best{};
-    best.total_bytes = (size_t)-1;
-    const int fw = env_or("MNB_MMA_WARPS", 0), fc = env_or("MNB_MMA_CHUNK", 0);
-    const int fs = env_or("MNB_MMA_SLOTS", kMaxSlots), fb = env_or("MNB_MMA_STAGE_BUFS", 0);
-    const int warps_opts[2] = {16, 8};
-    for (int wi = 0; wi < 2; ++wi) {
-        const int W = warps_opts[wi];
-        if (fw && fw != W) continue;
-        for (int ct = 4; ct >= 1; ct >>= 1) {
-            if (fc && fc != ct) continue;
-            Geom g{};
-            g.warps = W;
-            g.chunk_tiles = ct;
-            const int64_t per = (L.KTILES + W - 1) / W;
-            g.ktw = (per + ct - 1) / ct * ct;
-            // skip chunk sizes that would leave a quarter or more of the warps idle
-            if ((L.KTILES + g.ktw - 1) / g.ktw < (W * 3 + 3) / 4 && ct > 1) continue;
-            g.kblocks_pad = (L.KTILES * L.KT + L.bs - 1) / L.bs;
-            g.ks_total = L.KTILES * L.KT / 16;
-            g.raw_scale_bytes = (int)(16 * L.KB * (scale_dtype == kF32 ? 4 : 2));
-            g.raw_zp_bytes = has_zp ? (int)(16 * L.zp_row) : 0;
-            g.xb_bytes = (size_t)M * g.ks_total * 32;
-            g.raw_bytes = (size_t)kRawSlots * (round16(g.raw_scale_bytes) + round16(g.raw_zp_bytes));
-            g.red_bytes = (size_t)2 * W * 16 * MT * 4;
-            g.bar_bytes = (size_t)(W * kMaxSlots + kRawSlots) * 8;
-            for (int bufs = 2; bufs >= 1; --bufs) {
-                if (fb && fb != bufs) continue;
-                g.stage_bufs = bufs;
-                g.stage_bytes = (size_t)bufs * 16 * (g.kblocks_pad | 1) * sizeof(Entry);
-                const size_t fixed = g.xb_bytes + g.raw_bytes + g.stage_bytes + g.red_bytes + g.bar_bytes + 128;
-                const size_t chunk = (size_t)ct * kTileBytes;
-                int slots = fs > kMaxSlots ? kMaxSlots : fs;
-                while (slots > kMinSlots && fixed + (size_t)W * slots * chunk > smem_limit) --slots;
-                g.slots = slots;
-                g.ring_bytes = (size_t)W * slots * chunk;
-                g.total_bytes = g.ring_bytes + fixed;
-                if (g.total_bytes <= smem_limit && g.ring_bytes >= (96u << 10)) return g;
-                if (g.total_bytes <= smem_limit && (best.total_bytes == (size_t)-1 || g.ring_bytes > best.ring_bytes))
-                    best = g;
-            }
-        }
+// Host-side geometry.  Each warp takes up to kMaxTPW k-tiles per round; a CTA
+// takes kWarps warps' worth of tiles; the K-splits of a row tile form a
+// cluster of at most kMaxCluster CTAs (more rounds per warp beyond that).
+// MNB_MMA_TPW overrides the tiles per warp (1..8).
+inline Geom make_geom(const Layout& L, int64_t M, int MT) {
+    Geom g{};
+    const int64_t KT = L.KTILES;
+    int tpw = env_or("MNB_MMA_TPW", 0);
+    if (tpw < 1 || tpw > kMaxTPW) {
+        // enough tiles per warp that all warps work, at most kMaxTPW
+        tpw = (int)((KT + kWarps - 1) / kWarps);
+        if (tpw > kMaxTPW) tpw = kMaxTPW;
+        if (tpw < 1) tpw = 1;
     }
-    return best;
+    const int64_t per_round = (int64_t)kWarps * tpw;
+    int64_t rounds_total = (KT + per_round - 1) / per_round;  // CTA-rounds along K
+    int C = (int)(rounds_total < kMaxCluster ? rounds_total : kMaxCluster);
+    if (C < 1) C = 1;
+    const int rounds = (int)((rounds_total + C - 1) / C);
+    g.C = C;
+    g.tpw = tpw;
+    g.rounds = rounds;
+    g.tiles_cta = (int)(per_round * rounds);
+    g.kb_cta = (int)((g.tiles_cta * L.KT + L.bs - 1) / L.bs);
+    g.ks_cta = (int)(g.tiles_cta * L.KT / 16);
+    g.xb_bytes = (size_t)M * g.ks_cta * 32;
+    g.stage_bytes = (size_t)16 * (g.kb_cta | 1) * sizeof(Entry);
+    g.red_bytes = (size_t)kWarps * 16 * MT * 4;
+    g.part_bytes = (size_t)16 * MT * 4;
+    g.total_bytes = g.xb_bytes + g.stage_bytes + g.red_bytes + g.part_bytes + 64;
+    return g;
 }
 
-// SPB_LOG >= 0: blocks of 2^SPB_LOG k-steps tile every chunk (static block
-// structure); -1: any block size, run-time checks.
+// Programmatic dependent launch: wait for the preceding kernel's completion
+// (and memory) / allow the next kernel to be scheduled.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// SPB_LOG >= 0: blocks of 2^SPB_LOG k-steps start at every warp slice (static
+// block structure); -1: any block size, run-time checks.
 template <int BITS, bool BF16X, int MT, int SPB_LOG>
-__global__ void __launch_bounds__(512, 1) gemv_mma_kernel(MatmulParams p, Geom geo) {
+__global__ void __launch_bounds__(kThreads, 3) gemv_mma_kernel(MatmulParams p, Geom geo, int pdl) {
     using U = Unpack<BITS, BF16X>;
     constexpr int NTILE = MT / 8;  // MMA n8 tiles (activation rows 0-7, 8-15)
+    constexpr int SPT = U::kStepsPerTile;
     const Layout& L = p.L;
     extern __shared__ __align__(128) uint8_t smem[];
-    const int W = geo.warps;
-    const int T = W * 32;
-    const int chunk_bytes = geo.chunk_tiles * kTileBytes;
-    uint8_t* ring = smem;
-    uint8_t* xb = smem + geo.ring_bytes;
-    uint8_t* raw = xb + geo.xb_bytes;
-    Entry* stage = reinterpret_cast<Entry*>(raw + geo.raw_bytes);
-    float* red = reinterpret_cast<float*>(raw + geo.raw_bytes + geo.stage_bytes);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(raw + geo.raw_bytes + geo.stage_bytes + geo.red_bytes);
-    uint64_t* rbars = bars + W * kMaxSlots;
+    uint8_t* xb = smem;
+    Entry* stage = reinterpret_cast<Entry*>(smem + geo.xb_bytes);
+    float* red = reinterpret_cast<float*>(smem + geo.xb_bytes + geo.stage_bytes);
+    float* part = red + kWarps * 16 * MT;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
     const int M = (int)p.M;
-    const int my_tiles = (int)((L.NT - blockIdx.x + gridDim.x - 1) / gridDim.x);
-    if (my_tiles <= 0) return;
-    const int S_SLOTS = geo.slots;
-    const int CT = geo.chunk_tiles;
+    const int C = geo.C;
+    const int64_t rt = blockIdx.x / C;
+    const int split = (int)(blockIdx.x - rt * C);
+    const int64_t cta_t0 = (int64_t)split * geo.tiles_cta;  // first k-tile of this CTA
+    const int64_t cta_t1 = imin64(cta_t0 + geo.tiles_cta, L.KTILES);
+    const int tpw = geo.tpw;
 
-    // ---- weight stream of this warp's K-slice ----
-    const int64_t kt_begin = imin64((int64_t)warp * geo.ktw, L.KTILES);
-    const int64_t kt_end = imin64(kt_begin + geo.ktw, L.KTILES);
-    const int nch = (int)((kt_end - kt_begin + CT - 1) / CT);
-    const int total_chunks = nch * my_tiles;
-    uint64_t* wbars = bars + warp * kMaxSlots;
-    uint8_t* wring = ring + (size_t)warp * S_SLOTS * chunk_bytes;
-    int iss_i = 0, iss_c = 0, iss_slot = 0, issued = 0;
-    auto issue_next = [&]() {  // lane 0 only
-        const int64_t rt = blockIdx.x + (int64_t)iss_i * gridDim.x;
-        const int64_t kt = kt_begin + (int64_t)iss_c * CT;
-        const uint32_t bytes = (uint32_t)(imin64(CT, kt_end - kt) * kTileBytes);
-        mbar_arrive_expect_tx(&wbars[iss_slot], bytes);
-        bulk_g2s(wring + iss_slot * chunk_bytes, p.packed + (rt * L.KTILES + kt) * kTileBytes, bytes,
-                 &wbars[iss_slot]);
-    };
-    auto advance_issue = [&]() {
-        ++issued;
-        if (++iss_c == nch) { iss_c = 0; ++iss_i; }
-        if (++iss_slot == S_SLOTS) iss_slot = 0;
-    };
+    const int64_t k_cta0 = cta_t0 * L.KT;
+    const int kb_cta = geo.kb_cta;
+    const int kbs = kb_cta | 1;
+    const int64_t kb0 = k_cta0 / L.bs;
 
-    // ---- raw scales / zero points of whole row-tiles ----
-    const bool raw_ok = ((reinterpret_cast<uintptr_t>(p.scales) & 15) == 0) &&
-                        (p.zp == nullptr || (reinterpret_cast<uintptr_t>(p.zp) & 15) == 0);
-    const int raw_slot_bytes = (int)(round16(geo.raw_scale_bytes) + round16(geo.raw_zp_bytes));
-    auto tile_by_copy = [&](int i) {
-        const int64_t rt = blockIdx.x + (int64_t)i * gridDim.x;
-        return raw_ok && (rt * 16 + 16 <= L.N);
-    };
-    auto issue_raw = [&](int i) {  // thread 0 only
-        if (i >= my_tiles || !tile_by_copy(i)) return;
-        const int64_t rt = blockIdx.x + (int64_t)i * gridDim.x;
-        const int slot = i % kRawSlots;
-        uint8_t* dst = raw + slot * raw_slot_bytes;
-        mbar_arrive_expect_tx(&rbars[slot], (uint32_t)(geo.raw_scale_bytes + geo.raw_zp_bytes));
-        bulk_g2s(dst, static_cast<const uint8_t*>(p.scales) + rt * geo.raw_scale_bytes,
-                 (uint32_t)geo.raw_scale_bytes, &rbars[slot]);
-        if (geo.raw_zp_bytes)
-            bulk_g2s(dst + round16(geo.raw_scale_bytes), p.zp + rt * geo.raw_zp_bytes, (uint32_t)geo.raw_zp_bytes,
-                     &rbars[slot]);
-    };
+    // ---- 1. loads, in the order their data is needed: this thread's run of 8
+    //         (row, block) scales and zero points, then the warp's weight tiles.
+    //         Decoding the small first loads overlaps the weight stream. ----
+    const int runs = (kb_cta + 7) / 8;
+    const bool stage_fast = 16 * runs <= kThreads;  // one run per thread (the common case)
+    const int srow = tid / (runs > 0 ? runs : 1), srun = tid - srow * (runs > 0 ? runs : 1);
+    const int64_t s_n = rt * 16 + srow;
+    const int64_t s_kb = kb0 + (int64_t)srun * 8;
+    const bool s_active = stage_fast && tid < 16 * runs;
+    const bool s_row_ok = s_active && s_n < L.N;
+    const bool s_full = s_row_ok && s_kb + 8 <= L.KB;
+    const int64_t s_si = s_n * L.KB + s_kb;
+    const bool s_vec16 = s_full && p.scale_dtype != kF32 && (s_si & 7) == 0 &&
+                         (reinterpret_cast<uintptr_t>(p.scales) & 15) == 0;
+    const bool s_vec32 = s_full && p.scale_dtype == kF32 && (s_si & 3) == 0 &&
+                         (reinterpret_cast<uintptr_t>(p.scales) & 15) == 0;
+    const uint8_t* s_zsrc = p.zp ? p.zp + s_n * L.zp_row + s_kb * BITS / 8 : nullptr;
+    const bool z_vec = s_full && p.zp && (reinterpret_cast<uintptr_t>(s_zsrc) & (BITS - 1)) == 0;
+    uint4 sv0 = make_uint4(0, 0, 0, 0), sv1 = make_uint4(0, 0, 0, 0);
+    uint64_t zraw = 0;
+    if (s_vec16) {
+        sv0 = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.scales) + s_si));
+    } else if (s_vec32) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const float*>(p.scales) + s_si);
+        sv0 = __ldg(src);
+        sv1 = __ldg(src + 1);
+    }
+    if (z_vec) {
+        if (BITS == 2) zraw = __ldg(reinterpret_cast<const uint16_t*>(s_zsrc));
+        else if (BITS == 4) zraw = __ldg(reinterpret_cast<const uint32_t*>(s_zsrc));
+        else zraw = __ldg(reinterpret_cast<const unsigned long long*>(s_zsrc));
+    }
 
-    if (lane == 0)
-        for (int s = 0; s < S_SLOTS; ++s) mbar_init(&wbars[s], 1);
-    if (tid == 0)
-        for (int s = 0; s < kRawSlots; ++s) mbar_init(&rbars[s], 1);
-    fence_barrier_init();
-    __syncthreads();
-    {
-        const int n0 = total_chunks < S_SLOTS ? total_chunks : S_SLOTS;
-        for (int q0 = 0; q0 < n0; ++q0) {
-            if (lane == 0) issue_next();
-            advance_issue();
+    const uint8_t* wrow = p.packed + (rt * L.KTILES) * kTileBytes + lane * 16;
+    auto warp_tile0 = [&](int round) { return cta_t0 + ((int64_t)round * kWarps + warp) * tpw; };
+    uint4 wv[kMaxTPW];
+    auto load_round = [&](int round) {
+        const int64_t t0 = warp_tile0(round);
+#pragma unroll
+        for (int j = 0; j < kMaxTPW; ++j)
+            if (j < tpw && t0 + j < cta_t1) wv[j] = ldg_stream(wrow + (t0 + j) * kTileBytes);
+    };
+    load_round(0);
+    if (pdl) griddep_launch_dependents();  // the next kernel may start filling SMs as CTAs retire
+
+    // ---- 2. per (row, block) subtraction constant and scale; entry (r, j) at r * kbs + j ----
+    auto decode_run = [&](int r, int run, int64_t n, int64_t kbr, bool vec16, bool vec32, bool zv,
+                          const uint4& a0, const uint4& a1, uint64_t zr) {
+        const bool row_ok = n < L.N;
+        const int64_t si = n * L.KB + kbr;
+        float sc[8];
+        uint32_t z[8];
+        if (vec16) {
+            const uint32_t h[4] = {a0.x, a0.y, a0.z, a0.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t lo = h[j] & 0xFFFFu, hi = h[j] >> 16;
+                if (p.scale_dtype == kF16) {
+                    sc[2 * j] = __half2float(__ushort_as_half((uint16_t)lo));
+                    sc[2 * j + 1] = __half2float(__ushort_as_half((uint16_t)hi));
+                } else {
+                    sc[2 * j] = __uint_as_float(lo << 16);
+                    sc[2 * j + 1] = __uint_as_float(hi << 16);
+                }
+            }
+        } else if (vec32) {
+            sc[0] = __uint_as_float(a0.x); sc[1] = __uint_as_float(a0.y);
+            sc[2] = __uint_as_float(a0.z); sc[3] = __uint_as_float(a0.w);
+            sc[4] = __uint_as_float(a1.x); sc[5] = __uint_as_float(a1.y);
+            sc[6] = __uint_as_float(a1.z); sc[7] = __uint_as_float(a1.w);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                sc[j] = (row_ok && kbr + j < L.KB) ? load_f32(p.scales, si + j, p.scale_dtype) : 0.f;
+        }
+        uint64_t packed = zr;
+        if (p.zp != nullptr && !zv) {
+            packed = 0;
+            const uint8_t* zsrc = p.zp + n * L.zp_row + kbr * BITS / 8;
+#pragma unroll
+            for (int j = 0; j < BITS; ++j) {
+                // byte j holds blocks kbr + 8j/BITS ...; read it only if its first block exists
+                if (row_ok && kbr + (8 * j) / BITS < L.KB) packed |= (uint64_t)__ldg(zsrc + j) << (8 * j);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            z[j] = p.zp ? ((uint32_t)(packed >> (j * BITS)) & code_mask(BITS)) : (1u << (BITS - 1));
+        // two entries per 16-byte store
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+            const int jl = run * 8 + j;
+            const bool v0 = row_ok && kbr + j < L.KB, v1 = row_ok && kbr + j + 1 < L.KB;
+            const Entry e0{U::zconst(v0 ? z[j] : 0u), v0 ? sc[j] : 0.f};
+            const Entry e1{U::zconst(v1 ? z[j + 1] : 0u), v1 ? sc[j + 1] : 0.f};
+            Entry* dst = stage + r * kbs + jl;
+            if (jl + 1 < kb_cta) {
+                dst[0] = e0;
+                dst[1] = e1;
+            } else if (jl < kb_cta) {
+                dst[0] = e0;
+            }
+        }
+    };
+    if (stage_fast) {
+        if (s_active) decode_run(srow, srun, s_n, s_kb, s_vec16, s_vec32, z_vec, sv0, sv1, zraw);
+    } else {
+        for (int it = tid; it < 16 * runs; it += kThreads) {
+            const int r = it / runs, run = it - r * runs;
+            decode_run(r, run, rt * 16 + r, kb0 + (int64_t)run * 8, false, false, false, sv0, sv1, 0);
         }
     }
-    if (tid == 0)
-        for (int i = 0; i < kRawSlots; ++i) issue_raw(i);
+    if (pdl) griddep_wait();  // X (and Y) may belong to the previous kernel on the stream
 
-    // ---- B operand: activation row m, k-step S, lane class t -> 8 bytes
-    //      (X[m][16S+2t], X[m][16S+2t+1]) | (X[m][16S+2t+8], X[m][16S+2t+9]) ----
+    // ---- 3. activations (B fragments) of this CTA's k-steps:
+    //         row m, local k-step S, lane class t -> (X[m][k+2t..], X[m][k+2t+8..]);
+    //         item (m, S) is 32 bytes written as two 16-byte stores ----
     {
-        const int64_t KS = geo.ks_total;
-        const int64_t items = (int64_t)M * KS;
+        const int KS = geo.ks_cta;
+        const int items = M * KS;
         const bool vec = (L.K % 8) == 0;  // rows of X are 16-byte aligned
         const uint16_t* x16 = static_cast<const uint16_t*>(p.x);
-        constexpr int kRound = 4;
-        for (int64_t i0 = tid; i0 < items; i0 += (int64_t)T * kRound) {
-            uint4 v[kRound][2];
+        for (int it = tid; it < items; it += kThreads) {
+            const int m = it / KS, S = it - m * KS;
+            const int64_t k0 = k_cta0 + 16 * (int64_t)S;
+            uint4 v0, v1;
+            if (vec && k0 + 16 <= L.K) {
+                const uint4* src = reinterpret_cast<const uint4*>(x16 + m * L.K + k0);
+                v0 = __ldg(src);
+                v1 = __ldg(src + 1);
+            } else {
+                uint32_t h[8];
 #pragma unroll
-            for (int u = 0; u < kRound; ++u) {
-                const int64_t it = i0 + (int64_t)u * T;
-                if (it >= items) continue;
-                const int64_t m = it / KS, S = it - m * KS;
-                const int64_t k0 = 16 * S;
-                if (vec && k0 + 16 <= L.K) {
-                    const uint4* src = reinterpret_cast<const uint4*>(x16 + m * L.K + k0);
-                    v[u][0] = __ldg(src);
-                    v[u][1] = __ldg(src + 1);
-                } else {
-                    uint32_t h[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int64_t ka = k0 + 2 * j, kb2 = ka + 1;
-                        const uint32_t lo = ka < L.K ? x16[m * L.K + ka] : 0u;
-                        const uint32_t hi = kb2 < L.K ? x16[m * L.K + kb2] : 0u;
-                        h[j] = lo | (hi << 16);
-                    }
-                    v[u][0] = make_uint4(h[0], h[1], h[2], h[3]);
-                    v[u][1] = make_uint4(h[4], h[5], h[6], h[7]);
+                for (int j = 0; j < 8; ++j) {
+                    const int64_t ka = k0 + 2 * j, kb2 = ka + 1;
+                    const uint32_t lo = ka < L.K ? x16[m * L.K + ka] : 0u;
+                    const uint32_t hi = kb2 < L.K ? x16[m * L.K + kb2] : 0u;
+                    h[j] = lo | (hi << 16);
                 }
+                v0 = make_uint4(h[0], h[1], h[2], h[3]);
+                v1 = make_uint4(h[4], h[5], h[6], h[7]);
             }
-#pragma unroll
-            for (int u = 0; u < kRound; ++u) {
-                const int64_t it = i0 + (int64_t)u * T;
-                if (it >= items) continue;
-                uint2* dst = reinterpret_cast<uint2*>(xb) + it * 4;
-                dst[0] = make_uint2(v[u][0].x, v[u][1].x);
-                dst[1] = make_uint2(v[u][0].y, v[u][1].y);
-                dst[2] = make_uint2(v[u][0].z, v[u][1].z);
-                dst[3] = make_uint2(v[u][0].w, v[u][1].w);
-            }
+            uint4* dst = reinterpret_cast<uint4*>(xb) + (int64_t)it * 2;
+            dst[0] = make_uint4(v0.x, v1.x, v0.y, v1.y);
+            dst[1] = make_uint4(v0.z, v1.z, v0.w, v1.w);
         }
     }
-
-    // ---- staged (constant, scale) per row-block; entry (r, kb) at r * kbs + kb ----
-    const int kbp = (int)geo.kblocks_pad;
-    const int kbs = kbp | 1;
-    const int stage_stride = 16 * kbs;
-    const int sbytes = p.scale_dtype == kF32 ? 4 : 2;
-    const int zmask = code_mask(BITS);
-    const int tpr = T / 16;  // converting threads per row
-    const int conv_r = tid / tpr, conv_j = tid % tpr;
-    auto convert = [&](int i, int buf) {
-        Entry* dst = stage + buf * stage_stride + conv_r * kbs;
-        const int64_t rt = blockIdx.x + (int64_t)i * gridDim.x;
-        const int64_t n = rt * 16 + conv_r;
-        const int kbv = (int)L.KB;
-        if (tile_by_copy(i)) {
-            const int slot = i % kRawSlots;
-            mbar_wait(&rbars[slot], (uint32_t)((i / kRawSlots) & 1), p.status);
-            const uint8_t* rs = raw + slot * raw_slot_bytes;
-            const uint8_t* rz = rs + round16(geo.raw_scale_bytes) + conv_r * L.zp_row;
-            const float* rs32 = reinterpret_cast<const float*>(rs) + conv_r * kbv;
-            const uint16_t* rs16 = reinterpret_cast<const uint16_t*>(rs) + conv_r * kbv;
-            const bool has_zp = geo.raw_zp_bytes != 0;
-            for (int kb = conv_j; kb < kbp; kb += tpr) {
-                uint32_t z = 0;
-                float sc = 0.f;
-                if (kb < kbv) {
-                    if (sbytes == 4) {
-                        sc = rs32[kb];
-                    } else {
-                        const uint16_t u = rs16[kb];
-                        sc = p.scale_dtype == kF16 ? __half2float(__ushort_as_half(u))
-                                                   : __uint_as_float((uint32_t)u << 16);
-                    }
-                    const int bit = kb * BITS;
-                    z = has_zp ? ((rz[bit >> 3] >> (bit & 7)) & zmask) : (1u << (BITS - 1));
-                }
-                dst[kb] = Entry{U::zconst(z), sc};
-            }
-        } else {
-            for (int kb = conv_j; kb < kbp; kb += tpr) {
-                uint32_t z = 0;
-                float sc = 0.f;
-                if (n < L.N && kb < kbv) {
-                    z = (uint32_t)load_zp(p.zp, L, n, kb);
-                    sc = load_f32(p.scales, n * L.KB + kb, p.scale_dtype);
-                }
-                dst[kb] = Entry{U::zconst(z), sc};
-            }
-        }
-    };
-
-    convert(0, 0);
     __syncthreads();
-    if (tid == 0) issue_raw(kRawSlots);
 
-    // Lane's B-operand rows: activation rows g and g + 8, folded into [0, M)
-    // (columns past M compute duplicates that are never stored).
-    const uint2* xrow0 = reinterpret_cast<const uint2*>(xb) + (int64_t)(g % M) * geo.ks_total * 4 + t;
-    const uint2* xrow1 = reinterpret_cast<const uint2*>(xb) + (int64_t)((g + 8) % M) * geo.ks_total * 4 + t;
-
+    // ---- 4. contraction ----
+    const Entry* st_g = stage + g * kbs;
+    const Entry* st_g8 = st_g + 8 * kbs;
+    const uint2* xrow0 = reinterpret_cast<const uint2*>(xb) + (int64_t)(g % M) * geo.ks_cta * 4 + t;
+    const uint2* xrow1 = reinterpret_cast<const uint2*>(xb) + (int64_t)((g + 8) % M) * geo.ks_cta * 4 + t;
     const int spb_log = SPB_LOG >= 0 ? SPB_LOG : __ffs(L.bs / 16) - 1;
     const int spb_mask = (1 << spb_log) - 1;
     constexpr int kStaticMask = SPB_LOG >= 0 ? (1 << (SPB_LOG >= 0 ? SPB_LOG : 0)) - 1 : 0;
-    bool bad = false;
-    int q = 0, slot = 0;
-    uint32_t parity = 0;
-    for (int i = 0; i < my_tiles; ++i) {
-        const int64_t rt = blockIdx.x + (int64_t)i * gridDim.x;
-        const int buf = geo.stage_bufs == 2 ? (i & 1) : 0;
-        const Entry* st_g = stage + buf * stage_stride + g * kbs;
-        const Entry* st_g8 = st_g + 8 * kbs;
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    float y[NTILE][4];
+    float acc[NTILE][4];
+#pragma unroll
+    for (int j = 0; j < NTILE; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) y[j][c] = acc[j][c] = 0.f;
+    uint32_t zg = 0, zg8 = 0;
+    float sg = 0.f, sg8 = 0.f;
+    bool fresh = true, first = true;
 
-        float y[NTILE][4];
-        float acc[NTILE][4];
+    for (int round = 0; round < geo.rounds; ++round) {
+        const int64_t t0 = warp_tile0(round);
+        if (round > 0) load_round(round);
+        const int ntile = (int)imin64(tpw, cta_t1 - t0);  // may be <= 0
+        const int S0 = (int)((t0 - cta_t0) * SPT);        // local k-step of this warp's first tile
 #pragma unroll
-        for (int j = 0; j < NTILE; ++j)
+        for (int j = 0; j < kMaxTPW; ++j) {
+            if (j >= ntile) break;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) y[j][c] = acc[j][c] = 0.f;
-        const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
-        int S = (int)(kt_begin * U::kStepsPerTile);
-        uint32_t zg = 0, zg8 = 0;
-        float sg = 0.f, sg8 = 0.f;
-        bool first = true, fresh = true;
-
-        for (int c = 0; c < nch; ++c, ++q) {
-            if (!bad) bad = !mbar_wait(&wbars[slot], parity, p.status);
-            if (!bad) {
-                const int64_t kt = kt_begin + (int64_t)c * CT;
-                const int ntile = (int)imin64(CT, kt_end - kt);
-                const uint8_t* sbase = wring + slot * chunk_bytes;
+            for (int s = 0; s < SPT; ++s) {
+                const int ks = j * SPT + s;  // k-step inside this warp's slice
+                const int Sk = S0 + ks;      // k-step inside the CTA
+                const bool block_start =
+                    SPB_LOG >= 0 ? ((ks & kStaticMask) == 0) : (first || (Sk & spb_mask) == 0);
+                if (block_start) {
+                    first = false;
+                    const int kbl = Sk >> spb_log;
+                    const Entry eg = st_g[kbl], eg8 = st_g8[kbl];
+                    zg = eg.zc;
+                    sg = eg.s;
+                    zg8 = eg8.zc;
+                    sg8 = eg8.s;
+                }
+                uint32_t a[4];
+                U::kstep(wv[j], s, zg, zg8, a);
+                const bool from_zero = SPB_LOG >= 0 ? ((ks & kStaticMask) == 0) : fresh;
+                const uint2 b0 = xrow0[(int64_t)Sk * 4];
+                if (from_zero) mma16816<BF16X>(acc[0], a, b0.x, b0.y, zero4);
+                else mma16816<BF16X>(acc[0], a, b0.x, b0.y, acc[0]);
+                if constexpr (NTILE == 2) {
+                    const uint2 b1 = xrow1[(int64_t)Sk * 4];
+                    if (from_zero) mma16816<BF16X>(acc[1], a, b1.x, b1.y, zero4);
+                    else mma16816<BF16X>(acc[1], a, b1.x, b1.y, acc[1]);
+                }
+                fresh = false;
+                const bool block_end =
+                    SPB_LOG >= 0 ? (((ks + 1) & kStaticMask) == 0) : (((Sk + 1) & spb_mask) == 0);
+                if (block_end) {
 #pragma unroll
-                for (int tl = 0; tl < 4; ++tl) {
-                    if (tl >= ntile) break;
-                    const uint4 wv = reinterpret_cast<const uint4*>(sbase + tl * kTileBytes)[lane];
-                    const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                    for (int s = 0; s < U::kStepsPerTile; ++s) {
-                        const int ks = tl * U::kStepsPerTile + s;
-                        const int Sk = S + ks;
-                        const bool block_start =
-                            SPB_LOG >= 0 ? ((ks & kStaticMask) == 0) : (first || (Sk & spb_mask) == 0);
-                        if (block_start) {
-                            first = false;
-                            const int kb = Sk >> spb_log;
-                            const Entry eg = st_g[kb], eg8 = st_g8[kb];
-                            zg = eg.zc;
-                            sg = eg.s;
-                            zg8 = eg8.zc;
-                            sg8 = eg8.s;
-                        }
-                        uint32_t a[4];
-                        U::kstep(w, s, zg, zg8, a);
-                        // a block's first MMA starts from zero (static when blocks tile chunks)
-                        const bool from_zero = SPB_LOG >= 0 ? ((ks & kStaticMask) == 0) : fresh;
-                        const uint2 b0 = xrow0[(int64_t)Sk * 4];
-                        if (from_zero) mma16816<BF16X>(acc[0], a, b0.x, b0.y, zero4);
-                        else mma16816<BF16X>(acc[0], a, b0.x, b0.y, acc[0]);
-                        if constexpr (NTILE == 2) {
-                            const uint2 b1 = xrow1[(int64_t)Sk * 4];
-                            if (from_zero) mma16816<BF16X>(acc[1], a, b1.x, b1.y, zero4);
-                            else mma16816<BF16X>(acc[1], a, b1.x, b1.y, acc[1]);
-                        }
-                        fresh = false;
-                        const bool block_end =
-                            SPB_LOG >= 0 ? (((ks + 1) & kStaticMask) == 0) : (((Sk + 1) & spb_mask) == 0);
-                        if (block_end) {
-#pragma unroll
-                            for (int j = 0; j < NTILE; ++j) {
-                                y[j][0] = fmaf(sg, acc[j][0], y[j][0]);
-                                y[j][1] = fmaf(sg, acc[j][1], y[j][1]);
-                                y[j][2] = fmaf(sg8, acc[j][2], y[j][2]);
-                                y[j][3] = fmaf(sg8, acc[j][3], y[j][3]);
-                            }
-                            fresh = true;
-                        }
+                    for (int q = 0; q < NTILE; ++q) {
+                        y[q][0] = fmaf(sg, acc[q][0], y[q][0]);
+                        y[q][1] = fmaf(sg, acc[q][1], y[q][1]);
+                        y[q][2] = fmaf(sg8, acc[q][2], y[q][2]);
+                        y[q][3] = fmaf(sg8, acc[q][3], y[q][3]);
                     }
-                }
-                S += CT * U::kStepsPerTile;
-                __syncwarp();
-                if (issued < total_chunks) {
-                    if (lane == 0) issue_next();
-                    advance_issue();
+                    fresh = true;
                 }
             }
-            if (++slot == S_SLOTS) {
-                slot = 0;
-                parity ^= 1u;
-            }
         }
-        if (!fresh) {  // a block cut by the end of this warp's slice
+        if (!fresh) {  // a block cut by the end of this warp's tiles
 #pragma unroll
-            for (int j = 0; j < NTILE; ++j) {
-                y[j][0] = fmaf(sg, acc[j][0], y[j][0]);
-                y[j][1] = fmaf(sg, acc[j][1], y[j][1]);
-                y[j][2] = fmaf(sg8, acc[j][2], y[j][2]);
-                y[j][3] = fmaf(sg8, acc[j][3], y[j][3]);
+            for (int q = 0; q < NTILE; ++q) {
+                y[q][0] = fmaf(sg, acc[q][0], y[q][0]);
+                y[q][1] = fmaf(sg, acc[q][1], y[q][1]);
+                y[q][2] = fmaf(sg8, acc[q][2], y[q][2]);
+                y[q][3] = fmaf(sg8, acc[q][3], y[q][3]);
             }
+            fresh = true;
         }
-        // red[buf2][warp][row][col]
-        float* rb = red + (size_t)(i & 1) * W * 16 * MT;
-        float* mine = rb + (size_t)warp * 16 * MT;
-#pragma unroll
-        for (int j = 0; j < NTILE; ++j) {
-            const int col = j * 8 + 2 * t;
-            mine[g * MT + col] = y[j][0];
-            mine[g * MT + col + 1] = y[j][1];
-            mine[(g + 8) * MT + col] = y[j][2];
-            mine[(g + 8) * MT + col + 1] = y[j][3];
-        }
-        if (i + 1 < my_tiles) {
-            if (geo.stage_bufs == 1) __syncthreads();
-            convert(i + 1, geo.stage_bufs == 2 ? (buf ^ 1) : 0);
-        }
-        __syncthreads();
-        if (tid == 0) issue_raw(i + 1 + kRawSlots);
-        if (tid < 16 * M) {
-            const int row = tid & 15, m = tid >> 4;
-            float v = 0.f;
-            for (int w2 = 0; w2 < W; ++w2) v += rb[(size_t)w2 * 16 * MT + row * MT + m];
-            const int64_t n = rt * 16 + row;
-            if (n < L.N) {
-                if (p.bias) v += load_f32(p.bias, n, p.bias_dtype);
-                store_f32(p.y, (int64_t)m * L.N + n, v, p.out_dtype);
-            }
-        }
+        first = true;
     }
-    if (bad && lane == 0) {
-        for (int qq = q; qq < issued; ++qq) {
-            const int sl = qq % S_SLOTS;
-            const uint32_t ph = (uint32_t)((qq / S_SLOTS) & 1);
-            for (int it = 0; it < (1 << 16); ++it)
-                if (mbar_try_wait(&wbars[sl], ph)) break;
+
+    // ---- 5. reduce the warps' K-slices (fixed order), then the cluster's K-splits ----
+    float* mine = red + warp * 16 * MT;
+#pragma unroll
+    for (int q = 0; q < NTILE; ++q) {
+        const int col = q * 8 + 2 * t;
+        mine[g * MT + col] = y[q][0];
+        mine[g * MT + col + 1] = y[q][1];
+        mine[(g + 8) * MT + col] = y[q][2];
+        mine[(g + 8) * MT + col + 1] = y[q][3];
+    }
+    __syncthreads();
+    const bool owner = tid < 16 * M;
+    const int row = tid & 15, m = tid >> 4;
+    float v = 0.f;
+    if (owner) {
+#pragma unroll
+        for (int w2 = 0; w2 < kWarps; ++w2) v += red[w2 * 16 * MT + row * MT + m];
+    }
+    if (C > 1) {
+        if (owner) part[row * MT + m] = v;
+        cluster_sync();
+        if (split == 0 && owner) {
+            v = part[row * MT + m];
+            for (int c2 = 1; c2 < C; ++c2) v += ld_dsmem_f32(&part[row * MT + m], (uint32_t)c2);
+        }
+        cluster_sync();  // peers keep their shared memory until the leader has read it
+    }
+    if (split == 0 && owner) {
+        const int64_t n = rt * 16 + row;
+        if (n < L.N) {
+            if (p.bias) v += load_f32(p.bias, n, p.bias_dtype);
+            store_f32(p.y, (int64_t)m * L.N + n, v, p.out_dtype);
         }
     }
 }
 
 template <int BITS, bool BF16X, int MT, int SPB_LOG>
-cudaError_t launch_variant(const MatmulParams& p, const Geom& geo, int64_t grid, cudaStream_t s) {
+cudaError_t launch_variant(const MatmulParams& p, const Geom& geo, cudaStream_t s) {
+    const int pdl = (p.flags & kFlagPDL) ? 1 : 0;
     auto kern = gemv_mma_kernel<BITS, BF16X, MT, SPB_LOG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.total_bytes);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)grid, geo.warps * 32, geo.total_bytes, s>>>(p, geo);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.L.NT * geo.C));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = geo.total_bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)geo.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, geo, pdl);
 }
 
+// Static block structure when every warp slice starts on a block boundary and
+// blocks are at most 8 k-steps.
 template <int BITS, bool BF16X, int MT>
-cudaError_t launch_spb(const MatmulParams& p, const Geom& geo, int64_t grid, cudaStream_t s) {
-    const int steps_per_chunk = geo.chunk_tiles * (16 / BITS);
+cudaError_t launch_spb(const MatmulParams& p, const Geom& geo, cudaStream_t s) {
     const int spb = p.L.bs / 16;
-    if (steps_per_chunk % spb == 0) {
+    const int steps_per_warp = geo.tpw * (16 / BITS);
+    if (steps_per_warp % spb == 0) {
         switch (spb) {
-            case 1: return launch_variant<BITS, BF16X, MT, 0>(p, geo, grid, s);
-            case 2: return launch_variant<BITS, BF16X, MT, 1>(p, geo, grid, s);
-            case 4: return launch_variant<BITS, BF16X, MT, 2>(p, geo, grid, s);
-            case 8: return launch_variant<BITS, BF16X, MT, 3>(p, geo, grid, s);
+            case 1: return launch_variant<BITS, BF16X, MT, 0>(p, geo, s);
+            case 2: return launch_variant<BITS, BF16X, MT, 1>(p, geo, s);
+            case 4: return launch_variant<BITS, BF16X, MT, 2>(p, geo, s);
+            case 8: return launch_variant<BITS, BF16X, MT, 3>(p, geo, s);
             default: break;
         }
     }
-    return launch_variant<BITS, BF16X, MT, -1>(p, geo, grid, s);
+    return launch_variant<BITS, BF16X, MT, -1>(p, geo, s);
 }
 
 template <int BITS>
-cudaError_t launch_bits(const MatmulParams& p, const Geom& geo, int64_t grid, cudaStream_t s) {
+cudaError_t launch_bits(const MatmulParams& p, const Geom& geo, cudaStream_t s) {
     const bool bf = p.act_dtype == kBF16;
-    if (p.M <= 8) return bf ? launch_spb<BITS, true, 8>(p, geo, grid, s) : launch_spb<BITS, false, 8>(p, geo, grid, s);
-    return bf ? launch_spb<BITS, true, 16>(p, geo, grid, s) : launch_spb<BITS, false, 16>(p, geo, grid, s);
+    if (p.M <= 8) return bf ? launch_spb<BITS, true, 8>(p, geo, s) : launch_spb<BITS, false, 8>(p, geo, s);
+    return bf ? launch_spb<BITS, true, 16>(p, geo, s) : launch_spb<BITS, false, 16>(p, geo, s);
 }
 
 }  // namespace gmma

@@ -3,7 +3,7 @@
 #include "gemv_mma.cuh"
 
 namespace mnb {
-cudaError_t launch_gemv_mma_b4(const MatmulParams& p, const gmma::Geom& geo, int64_t grid, cudaStream_t s) {
-    return gmma::launch_bits<4>(p, geo, grid, s);
+cudaError_t launch_gemv_mma_b4(const MatmulParams& p, const gmma::Geom& geo, cudaStream_t s) {
+    return gmma::launch_bits<4>(p, geo, s);
 }
 }  // namespace mnb

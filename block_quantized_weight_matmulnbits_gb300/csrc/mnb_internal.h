@@ -25,7 +25,10 @@ struct MatmulParams {
     int* status;             // device status word
     void* workspace;
     size_t workspace_bytes;
+    int flags;               // MNB_FLAG_* of the call
 };
+
+constexpr int kFlagPDL = 1;  // == MNB_FLAG_PDL
 
 cudaError_t launch_pack(const uint8_t* b_ort, uint8_t* packed_hdr, const Layout& L, cudaStream_t s);
 cudaError_t launch_unpack(const uint8_t* packed, uint8_t* b_ort, const Layout& L, cudaStream_t s);

@@ -84,6 +84,16 @@ typedef enum mnb_kernel {
     MNB_KERNEL_GEMV_I8 = 5    /* int8-activation path (accuracy_level 4), integer dot products */
 } mnb_kernel;
 
+/* Flags of mnb_matmul_args.flags. */
+/* MNB_FLAG_PDL: launch with programmatic dependent launch.  The kernel starts
+ * streaming the weights, scales, zero points and bias before the preceding
+ * kernel on the stream has finished (its X and Y accesses still wait for it),
+ * and lets the next kernel start as its own blocks retire.  Use it only when
+ * the preceding kernel does not write packed_b, scales, zero_points or bias
+ * (true for constant model weights).  Honoured by MNB_KERNEL_GEMV_MMA; other
+ * kernels ignore it. */
+#define MNB_FLAG_PDL 1
+
 /* ---- weight layout (one-time re-tiling) -------------------------------- */
 
 /* Bytes of the packed weight buffer for (N, K, bits, block_size), or 0 if the
@@ -147,7 +157,8 @@ MNB_API mnb_status mnb_matmul(const void* x, const void* packed_b, const void* s
  *                  quantize_activation_signed, fn int8_row).  Needs workspace.
  *   workspace      device scratch of at least mnb_workspace_size() bytes
  *                  (256-byte aligned) or NULL when that size is 0.
- *   kernel         MNB_KERNEL_AUTO or a forced family. */
+ *   kernel         MNB_KERNEL_AUTO or a forced family.
+ *   flags          MNB_FLAG_* (0 for none). */
 typedef struct mnb_matmul_args {
     const void* x;
     const void* packed_b;
@@ -168,6 +179,7 @@ typedef struct mnb_matmul_args {
     size_t workspace_bytes;
     mnb_kernel kernel;
     mnb_stream_t stream;
+    int flags;  /* MNB_FLAG_* */
 } mnb_matmul_args;
 
 MNB_API mnb_status mnb_matmul_ex(const mnb_matmul_args* args);

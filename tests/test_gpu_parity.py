@@ -254,3 +254,24 @@ def test_full_size_workloads_sampled(G, ci):
     ref, mag = P.oracle_points(ms, ns)
     G.assert_within(y[ms, ns], ref, mag, w.out_dtype, w.name)
     assert np.all(np.isfinite(y))
+
+
+def test_pdl_chain_matches_plain_launches(G, mnb):
+    """A chain y1 = f(x), y2 = f(y1), y3 = f(y2) launched with programmatic
+    dependent launch must equal the same chain launched plainly, bit for bit:
+    each call reads its X only after the previous call has finished."""
+    N = K = 1024
+    w = _w(1, N, K, 4, 32, (BF16, F16, BF16), True, 900)
+    P = G.Problem(w)
+    outs = {}
+    for flags in (0, mnb.MNB_FLAG_PDL):
+        ys = [torch.empty((1, N), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+        src = P.x
+        for y in ys:
+            mnb.mnb_matmul_ex(src, P.packed, P.s, P.zp, y, 1, N, K, 4, 32, BF16, BF16, F16, kernel="gemv_mma",
+                              flags=flags)
+            src = y
+        torch.cuda.synchronize()
+        outs[flags] = [y.clone() for y in ys]
+    for a, b in zip(outs[0], outs[mnb.MNB_FLAG_PDL]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
