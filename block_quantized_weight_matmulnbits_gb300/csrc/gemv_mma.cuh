@@ -397,13 +397,16 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_mma_kernel(MatmulParams p, G
     __syncthreads();
 
     // ---- 4. contraction ----
-    const Entry* st_g = stage + g * kbs;
-    const Entry* st_g8 = st_g + 8 * kbs;
-    const uint2* xrow0 = reinterpret_cast<const uint2*>(xb) + (int64_t)(g % M) * geo.ks_cta * 4 + t;
-    const uint2* xrow1 = reinterpret_cast<const uint2*>(xb) + (int64_t)((g + 8) % M) * geo.ks_cta * 4 + t;
+    // Shared-memory addresses as 32-bit values so every per-k-step access is a
+    // base register plus a compile-time offset.
+    const uint32_t st_base = smem_u32(stage + g * kbs);     // row g; row g + 8 is 8 * kbs entries on
+    const uint32_t st_off8 = (uint32_t)(8 * kbs * sizeof(Entry));
+    const uint32_t xa0 = smem_u32(reinterpret_cast<const uint2*>(xb) + (int64_t)(g % M) * geo.ks_cta * 4 + t);
+    const uint32_t xa1 = smem_u32(reinterpret_cast<const uint2*>(xb) + (int64_t)((g + 8) % M) * geo.ks_cta * 4 + t);
     const int spb_log = SPB_LOG >= 0 ? SPB_LOG : __ffs(L.bs / 16) - 1;
     const int spb_mask = (1 << spb_log) - 1;
     constexpr int kStaticMask = SPB_LOG >= 0 ? (1 << (SPB_LOG >= 0 ? SPB_LOG : 0)) - 1 : 0;
+    constexpr int kStaticLog = SPB_LOG >= 0 ? SPB_LOG : 0;
     const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
     float y[NTILE][4];
     float acc[NTILE][4];
@@ -415,52 +418,63 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_mma_kernel(MatmulParams p, G
     float sg = 0.f, sg8 = 0.f;
     bool fresh = true, first = true;
 
+    auto lds2 = [](uint32_t addr) {
+        uint2 v;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+        return v;
+    };
+
     for (int round = 0; round < geo.rounds; ++round) {
         const int64_t t0 = warp_tile0(round);
         if (round > 0) load_round(round);
         const int ntile = (int)imin64(tpw, cta_t1 - t0);  // may be <= 0
         const int S0 = (int)((t0 - cta_t0) * SPT);        // local k-step of this warp's first tile
+        const uint32_t xr0 = xa0 + (uint32_t)S0 * 32u, xr1 = xa1 + (uint32_t)S0 * 32u;
+        const uint32_t er = st_base + (uint32_t)(SPB_LOG >= 0 ? (S0 >> kStaticLog) : 0) * (uint32_t)sizeof(Entry);
 #pragma unroll
         for (int j = 0; j < kMaxTPW; ++j) {
-            if (j >= ntile) break;
+            if (j < ntile) {
 #pragma unroll
-            for (int s = 0; s < SPT; ++s) {
-                const int ks = j * SPT + s;  // k-step inside this warp's slice
-                const int Sk = S0 + ks;      // k-step inside the CTA
-                const bool block_start =
-                    SPB_LOG >= 0 ? ((ks & kStaticMask) == 0) : (first || (Sk & spb_mask) == 0);
-                if (block_start) {
-                    first = false;
-                    const int kbl = Sk >> spb_log;
-                    const Entry eg = st_g[kbl], eg8 = st_g8[kbl];
-                    zg = eg.zc;
-                    sg = eg.s;
-                    zg8 = eg8.zc;
-                    sg8 = eg8.s;
-                }
-                uint32_t a[4];
-                U::kstep(wv[j], s, zg, zg8, a);
-                const bool from_zero = SPB_LOG >= 0 ? ((ks & kStaticMask) == 0) : fresh;
-                const uint2 b0 = xrow0[(int64_t)Sk * 4];
-                if (from_zero) mma16816<BF16X>(acc[0], a, b0.x, b0.y, zero4);
-                else mma16816<BF16X>(acc[0], a, b0.x, b0.y, acc[0]);
-                if constexpr (NTILE == 2) {
-                    const uint2 b1 = xrow1[(int64_t)Sk * 4];
-                    if (from_zero) mma16816<BF16X>(acc[1], a, b1.x, b1.y, zero4);
-                    else mma16816<BF16X>(acc[1], a, b1.x, b1.y, acc[1]);
-                }
-                fresh = false;
-                const bool block_end =
-                    SPB_LOG >= 0 ? (((ks + 1) & kStaticMask) == 0) : (((Sk + 1) & spb_mask) == 0);
-                if (block_end) {
-#pragma unroll
-                    for (int q = 0; q < NTILE; ++q) {
-                        y[q][0] = fmaf(sg, acc[q][0], y[q][0]);
-                        y[q][1] = fmaf(sg, acc[q][1], y[q][1]);
-                        y[q][2] = fmaf(sg8, acc[q][2], y[q][2]);
-                        y[q][3] = fmaf(sg8, acc[q][3], y[q][3]);
+                for (int s = 0; s < SPT; ++s) {
+                    const int ks = j * SPT + s;  // k-step inside this warp's slice (static)
+                    const int Sk = S0 + ks;      // k-step inside the CTA
+                    const bool block_start =
+                        SPB_LOG >= 0 ? ((ks & kStaticMask) == 0) : (first || (Sk & spb_mask) == 0);
+                    if (block_start) {
+                        first = false;
+                        const uint32_t ea = SPB_LOG >= 0
+                                                ? er + (uint32_t)(ks >> kStaticLog) * (uint32_t)sizeof(Entry)
+                                                : st_base + (uint32_t)(Sk >> spb_log) * (uint32_t)sizeof(Entry);
+                        const uint2 eg = lds2(ea), eg8 = lds2(ea + st_off8);
+                        zg = eg.x;
+                        sg = __uint_as_float(eg.y);
+                        zg8 = eg8.x;
+                        sg8 = __uint_as_float(eg8.y);
                     }
-                    fresh = true;
+                    uint32_t a[4];
+                    U::kstep(wv[j], s, zg, zg8, a);
+                    const bool from_zero = SPB_LOG >= 0 ? ((ks & kStaticMask) == 0) : fresh;
+                    const uint2 b0 = lds2(xr0 + (uint32_t)ks * 32u);
+                    if (from_zero) mma16816<BF16X>(acc[0], a, b0.x, b0.y, zero4);
+                    else mma16816<BF16X>(acc[0], a, b0.x, b0.y, acc[0]);
+                    if constexpr (NTILE == 2) {
+                        const uint2 b1 = lds2(xr1 + (uint32_t)ks * 32u);
+                        if (from_zero) mma16816<BF16X>(acc[1], a, b1.x, b1.y, zero4);
+                        else mma16816<BF16X>(acc[1], a, b1.x, b1.y, acc[1]);
+                    }
+                    fresh = false;
+                    const bool block_end =
+                        SPB_LOG >= 0 ? (((ks + 1) & kStaticMask) == 0) : (((Sk + 1) & spb_mask) == 0);
+                    if (block_end) {
+#pragma unroll
+                        for (int q = 0; q < NTILE; ++q) {
+                            y[q][0] = fmaf(sg, acc[q][0], y[q][0]);
+                            y[q][1] = fmaf(sg, acc[q][1], y[q][1]);
+                            y[q][2] = fmaf(sg8, acc[q][2], y[q][2]);
+                            y[q][3] = fmaf(sg8, acc[q][3], y[q][3]);
+                        }
+                        fresh = true;
+                    }
                 }
             }
         }

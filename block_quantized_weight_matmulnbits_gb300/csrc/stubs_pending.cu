@@ -4,9 +4,6 @@
 
 namespace mnb {
 
-bool gemm_tc_supported(const MatmulParams&) { return false; }
-cudaError_t launch_gemm_tc(const MatmulParams&, cudaStream_t) { return cudaErrorNotSupported; }
-
 size_t i8_workspace_bytes(int64_t, const Layout&) { return 0; }
 bool gemv_i8_supported(const MatmulParams&) { return false; }
 cudaError_t launch_quant_act(const void*, int, int8_t*, float*, int64_t, const Layout&, cudaStream_t) {

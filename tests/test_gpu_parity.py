@@ -120,6 +120,26 @@ def test_matmul_gemv_mma(G, M, bits, bs, dt, asym, N, K):
     G.assert_within(y, ref, mag, w.out_dtype, f"gemv_mma {w.name}")
 
 
+TC_CASES = []
+for i, (bits, bs) in enumerate(BITS_BS):
+    for M in (17, 128, 200):
+        act = BF16 if (i + M) % 2 else F16
+        TC_CASES.append((M, bits, bs, (act, [F16, F32, BF16][(i + M) % 3], [BF16, F16, F32][i % 3]),
+                         (i + M) % 3 != 0, 96 + 16 * (i % 4) + (M % 5), 64 * (2 + i % 3)))
+TC_CASES += [(64, 4, 32, (BF16, F16, BF16), False, 4096, 512), (1, 4, 32, (BF16, F16, BF16), True, 300, 256),
+             (33, 8, 128, (F16, F32, F16), True, 250, 1000), (130, 2, 64, (BF16, F16, BF16), True, 77, 1024),
+             (256, 4, 16, (BF16, BF16, F32), True, 520, 136), (300, 8, 16, (F16, F16, BF16), False, 48, 72)]
+
+
+@pytest.mark.parametrize("M,bits,bs,dt,asym,N,K", TC_CASES)
+def test_matmul_gemm_tc(G, M, bits, bs, dt, asym, N, K):
+    w = _w(M, N, K, bits, bs, dt, asym, 800 + M * 3 + bits * 7 + bs + N)
+    P = G.Problem(w)
+    y = P.y64(P.run("gemm_tc"))
+    ref, mag = P.oracle_full()
+    G.assert_within(y, ref, mag, w.out_dtype, f"gemm_tc {w.name}")
+
+
 @pytest.mark.parametrize("M", [2, 3, 8, 17, 33, 64])
 @pytest.mark.parametrize("bits,bs,dt", [(4, 32, DTYPES[0]), (8, 128, DTYPES[1]), (2, 64, DTYPES[2]),
                                         (4, 16, DTYPES[3])])
@@ -163,14 +183,14 @@ def test_bias_m1(G, mnb, kernel):
 
 # ---- degenerate cases --------------------------------------------------------
 
-@pytest.mark.parametrize("kernel", ["gemv", "gemv_mma", "generic"])
+@pytest.mark.parametrize("kernel", ["gemv", "gemv_mma", "gemm_tc", "generic"])
 @pytest.mark.parametrize("bits", [2, 4, 8])
 def test_all_codes_equal_zero_point_give_zero(G, mnb, kernel, bits):
     from tests._golden import pack_matrix_test, pack_zp_test
     N, K, bs = 48, 128, 32
     rng = np.random.default_rng(bits)
     z = rng.integers(0, 1 << bits, size=(N, K // bs))
-    w = _w(1, N, K, bits, bs, DTYPES[0], True, 400)
+    w = _w(1 if kernel != "gemm_tc" else 40, N, K, bits, bs, DTYPES[0], True, 400)
     data = wl.generate(w)
     data["b"] = pack_matrix_test(np.repeat(z, bs, axis=1), bits, bs)
     data["zp"] = pack_zp_test(z, bits)
@@ -195,10 +215,10 @@ def test_one_hot_row_selects_weight(G, mnb, oracle_mod, kernel):
         assert np.array_equal(y, wref[:, k0])
 
 
-@pytest.mark.parametrize("kernel", ["gemv", "gemv_mma", "generic"])
+@pytest.mark.parametrize("kernel", ["gemv", "gemv_mma", "gemm_tc", "generic"])
 def test_deterministic_and_n_split_bit_identical(G, mnb, kernel):
     N, K = 96, 1024
-    w = _w(1, N, K, 4, 32, DTYPES[0], True, 420)
+    w = _w(1 if kernel != "gemm_tc" else 70, N, K, 4, 32, DTYPES[0], True, 420)
     P = G.Problem(w)
     y1 = P.run(kernel).clone()
     y2 = P.run(kernel).clone()
