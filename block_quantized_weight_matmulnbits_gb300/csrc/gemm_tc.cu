@@ -35,9 +35,10 @@
 namespace mnb {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kMaxRaw = 8;   // ring of X tiles + packed W (TMA destination)
+constexpr int kWd = 4;       // ring of dequantised W tiles
 constexpr int kBM = 128;
-constexpr int kDequantWarps = 8;
+constexpr int kDequantWarps = 16;
 constexpr int kThreads = (2 + kDequantWarps) * 32;
 
 struct TcGeom {
@@ -48,7 +49,9 @@ struct TcGeom {
     int m_tiles;     // ceil(M / 128)
     int k_stages;    // ceil(Kpad / BK)
     int tiles_per_stage_row;  // packed 512-byte tiles per 16-row tile per stage
-    size_t x_stage, wp_stage, wd_stage, scale_bytes, zp_bytes, total_bytes;
+    int raw_stages;  // depth of the X + packed-W ring (<= kMaxRaw)
+    int tab_stride;  // entries per row of the converted (zero point, scale) table (odd)
+    size_t x_stage, wp_stage, wd_stage, scale_bytes, zp_bytes, tab_bytes, total_bytes;
 };
 
 // ---- PTX wrappers specific to tcgen05 / TMA tensor copies ----
@@ -58,6 +61,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
         "[%4];" ::"r"(smem_u32(dst)),
         "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -139,23 +150,27 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int k) {
 
 template <int BITS, bool BF16X>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(MatmulParams p, TcGeom geo,
-                                                               const __grid_constant__ CUtensorMap xmap) {
+                                                               const __grid_constant__ CUtensorMap xmap,
+                                                               const __grid_constant__ CUtensorMap wmap) {
     const Layout& L = p.L;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base for the swizzled tiles
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* xs = smem;                                          // [stages][128 x BK] bf16, SW128
-    uint8_t* wd = xs + kStages * geo.x_stage;                    // [stages][BN x BK] bf16, SW128
-    uint8_t* wp = wd + kStages * geo.wd_stage;                   // [stages][BN/16][tiles][512 B] packed
-    uint8_t* sraw = wp + kStages * geo.wp_stage;                 // [BN][KB] raw scales of this tile's rows
+    const int RS = geo.raw_stages;
+    uint8_t* xs = smem;                                          // [RS][128 x BK] bf16, SW128 (TMA)
+    uint8_t* wd = xs + RS * geo.x_stage;                         // [kWd][BN x BK] bf16, SW128
+    uint8_t* wp = wd + kWd * geo.wd_stage;                       // [RS][BN/16][tiles][512 B] packed
+    uint8_t* sraw = wp + RS * geo.wp_stage;                      // [BN][KB] raw scales of this tile's rows
     uint8_t* zraw = sraw + geo.scale_bytes;                      // [BN][zp_row] raw zero points
-    uint64_t* bars = reinterpret_cast<uint64_t*>(zraw + geo.zp_bytes);
-    uint64_t* full_raw = bars;                 // TMA bytes landed
-    uint64_t* full_w = bars + kStages;         // dequantised W written
-    uint64_t* empty = bars + 2 * kStages;      // MMA finished reading the stage
-    uint64_t* done = bars + 3 * kStages;       // accumulator complete
-    uint64_t* sbar = bars + 3 * kStages + 1;   // scales / zero points landed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 2);
+    uint32_t* tab = reinterpret_cast<uint32_t*>(zraw + geo.zp_bytes);  // [BN][tab_stride] converted
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(tab) + geo.tab_bytes);
+    uint64_t* raw_full = bars;                   // X tile + packed W landed
+    uint64_t* raw_empty = bars + kMaxRaw;        // MMA finished with the X tile (and so the codes)
+    uint64_t* wd_full = bars + 2 * kMaxRaw;      // dequantised W written
+    uint64_t* wd_empty = wd_full + kWd;          // MMA finished reading the dequantised W
+    uint64_t* done = wd_empty + kWd;             // accumulator complete
+    uint64_t* sbar = done + 1;                   // scales / zero points landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbar + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x;
@@ -170,10 +185,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(MatmulParams p, Tc
     const int sbytes = p.scale_dtype == kF32 ? 4 : 2;
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full_raw[s], 1);
-            mbar_init(&full_w[s], kDequantWarps);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < RS; ++s) {
+            mbar_init(&raw_full[s], 1);
+            mbar_init(&raw_empty[s], 1);
+        }
+        for (int s = 0; s < kWd; ++s) {
+            mbar_init(&wd_full[s], kDequantWarps / kWd);  // the dequant warps that own the slot
+            mbar_init(&wd_empty[s], 1);
         }
         mbar_init(done, 1);
         mbar_init(sbar, 1);
@@ -207,61 +225,55 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(MatmulParams p, Tc
                 bulk_g2s(sraw, sc_src, (uint32_t)sc_bytes, sbar);
                 if (z_bytes) bulk_g2s(zraw, z_src, (uint32_t)z_bytes, sbar);
             }
-            const int rts = (rows + 15) / 16;  // 16-row tiles with any valid row
-            const uint32_t tile_bytes = (uint32_t)geo.tiles_per_stage_row * kTileBytes;
             int issued = 0;
             for (int ks = 0; ks < KS; ++ks) {
-                const int s = ks % kStages;
-                if (ks >= kStages) {
-                    if (!mbar_wait(&empty[s], (uint32_t)(((ks / kStages) - 1) & 1), p.status)) {
+                const int s = ks % RS;
+                if (ks >= RS) {
+                    if (!mbar_wait(&raw_empty[s], (uint32_t)(((ks / RS) - 1) & 1), p.status)) {
                         *abort_flag = 1;
                         break;
                     }
                 }
                 if (*reinterpret_cast<volatile int*>(abort_flag)) break;
-                // the last stage may hold fewer packed tiles than a full one
-                const int64_t kt0 = (int64_t)ks * geo.tiles_per_stage_row;
-                const uint32_t copy_bytes =
-                    (uint32_t)imin64(geo.tiles_per_stage_row, L.KTILES - kt0) * kTileBytes;
-                const uint32_t bytes = (uint32_t)geo.x_stage + rts * copy_bytes;
-                mbar_arrive_expect_tx(&full_raw[s], bytes);
+                // one tensor copy of the stage's packed tiles for all BN / 16 row tiles
+                // ([row tile][k tile][512 B], zero fill past N and past the last k tile)
+                const int kt0 = ks * geo.tiles_per_stage_row;
+                const uint32_t bytes = (uint32_t)(geo.x_stage + geo.wp_stage);
+                mbar_arrive_expect_tx(&raw_full[s], bytes);
                 for (int half = 0; half < BK / 64; ++half)
                     tma_load_2d(xs + s * geo.x_stage + half * (kBM * 128), &xmap, ks * BK + half * 64, (int)m0,
-                                &full_raw[s]);
-                for (int r = 0; r < rts; ++r) {
-                    const int64_t nt = n0 / 16 + r;
-                    bulk_g2s(wp + s * geo.wp_stage + (size_t)r * tile_bytes,
-                             p.packed + (nt * L.KTILES + kt0) * kTileBytes, copy_bytes, &full_raw[s]);
-                }
+                                &raw_full[s]);
+                tma_load_3d(wp + s * geo.wp_stage, &wmap, 0, kt0, (int)(n0 / 16), &raw_full[s]);
                 issued = ks + 1;
             }
             if (*reinterpret_cast<volatile int*>(abort_flag)) {
                 // give copies still in flight a bounded chance to land before the CTA exits
-                for (int ks = issued - kStages < 0 ? 0 : issued - kStages; ks < issued; ++ks)
+                for (int ks = issued - RS < 0 ? 0 : issued - RS; ks < issued; ++ks)
                     for (int it = 0; it < (1 << 16); ++it)
-                        if (mbar_try_wait(&full_raw[ks % kStages], (uint32_t)((ks / kStages) & 1))) break;
+                        if (mbar_try_wait(&raw_full[ks % RS], (uint32_t)((ks / RS) & 1))) break;
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         const uint32_t idesc = idesc_f16(BF16X, BN);
         for (int ks = 0; ks < KS; ++ks) {
-            const int s = ks % kStages;
-            const uint32_t ph = (uint32_t)((ks / kStages) & 1);
-            bool ok = mbar_wait(&full_raw[s], ph, p.status) && mbar_wait(&full_w[s], ph, p.status);
+            const int s = ks % RS, w = ks % kWd;
+            bool ok = mbar_wait(&raw_full[s], (uint32_t)((ks / RS) & 1), p.status) &&
+                      mbar_wait(&wd_full[w], (uint32_t)((ks / kWd) & 1), p.status);
             if (!ok) *abort_flag = 1;
             if (*reinterpret_cast<volatile int*>(abort_flag)) break;
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t xa = smem_u32(xs + s * geo.x_stage);
-                const uint32_t wa = smem_u32(wd + s * geo.wd_stage);
+                const uint32_t wa = smem_u32(wd + w * geo.wd_stage);
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     const int half = kk >> 2, sub = kk & 3;
                     const uint64_t ad = sdesc_sw128(xa + half * (kBM * 128) + sub * 32);
                     const uint64_t bd = sdesc_sw128(wa + half * (BN * 128) + sub * 32);
                     tc_mma(tmem, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc_commit(&empty[s]);
+                tc_commit(&raw_empty[s]);
+                tc_commit(&wd_empty[w]);
                 if (ks == KS - 1) tc_commit(done);
             }
             __syncwarp();
@@ -280,63 +292,98 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(MatmulParams p, Tc
         } else if (!mbar_wait(sbar, 0, p.status)) {
             *abort_flag = 1;
         }
-        auto scale_of = [&](int r, int64_t kb) -> float {
-            const int64_t i = (int64_t)r * L.KB + kb;
-            if (sbytes == 4) return reinterpret_cast<const float*>(sraw)[i];
-            const uint16_t u = reinterpret_cast<const uint16_t*>(sraw)[i];
-            return p.scale_dtype == kF16 ? __half2float(__ushort_as_half(u)) : __uint_as_float((uint32_t)u << 16);
-        };
-        auto zp_of = [&](int r, int64_t kb) -> uint32_t {
-            if (!p.zp) return 1u << (BITS - 1);
-            const int64_t bit = kb * BITS;
-            return (zraw[(int64_t)r * L.zp_row + (bit >> 3)] >> (bit & 7)) & zmask;
-        };
-        // (zero-point constant pair, scale pair) of row r for depth k; rows past N get scale 0
-        auto consts = [&](int r, int64_t k, uint32_t& zc, uint32_t& sp) {
-            const int64_t kb = k / L.bs;
-            float sc = 0.f;
-            uint32_t z = 0;
-            if (r < rows && kb < L.KB) {
-                sc = scale_of(r, kb);
-                z = zp_of(r, kb);
+        constexpr int KT = 256 / BITS;          // depths per packed tile
+        constexpr int kSteps = 16 / BITS;       // k-steps per packed tile
+        const int bs_log = __ffs(L.bs) - 1;     // block size is a power of two
+        const int KBi = (int)L.KB;
+        const int zrow = (int)L.zp_row;
+        const int tstr = geo.tab_stride;
+        // Table of (row, block): low 16 bits the zero-point constant (magic + zp
+        // for the 16-bit paths, zp for 8-bit bf16), high 16 bits the scale
+        // rounded once to the MMA input type; rows past N and blocks past KB
+        // hold scale 0.  Built once per CTA; the odd row stride keeps the 8 row
+        // groups of a warp on different banks.
+        for (int r = dw; r < BN; r += kDequantWarps) {
+            for (int kb = lane; kb < tstr; kb += 32) {
+                float sc = 0.f;
+                uint32_t z = 0;
+                if (r < rows && kb < KBi) {
+                    const int i = r * KBi + kb;
+                    if (sbytes == 4) {
+                        sc = reinterpret_cast<const float*>(sraw)[i];
+                    } else {
+                        const uint16_t u = reinterpret_cast<const uint16_t*>(sraw)[i];
+                        sc = p.scale_dtype == kF16 ? __half2float(__ushort_as_half(u))
+                                                   : __uint_as_float((uint32_t)u << 16);
+                    }
+                    if (p.zp) {
+                        const int bit = kb * BITS;
+                        z = (zraw[r * zrow + (bit >> 3)] >> (bit & 7)) & zmask;
+                    } else {
+                        z = 1u << (BITS - 1);
+                    }
+                }
+                const uint32_t zc = (BITS == 8 && BF16X) ? z : ((kMag & 0xFFFFu) + z);
+                tab[r * tstr + kb] = zc | (to_pair(sc, bf) << 16);
             }
-            if constexpr (BITS == 8 && BF16X) {
-                zc = 0x4B000000u | z;
-            } else {
-                const uint32_t h = (kMag & 0xFFFFu) + z;
-                zc = h | (h << 16);
-            }
-            sp = to_pair(sc, bf);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kDequantWarps * 32) : "memory");
+        auto consts = [&](int r, int kb, uint32_t& zc, uint32_t& sp) {
+            const uint32_t e = tab[r * tstr + kb];
+            sp = prmt(e, e, 0x3232u);  // scale in both halves
+            if constexpr (BITS == 8 && BF16X) zc = 0x4B000000u | (e & 0xFFu);
+            else zc = prmt(e, e, 0x1010u);  // zero-point constant in both halves
         };
         const int rts = BN / 16;
         const int tiles = geo.tiles_per_stage_row;
-        for (int ks = 0; ks < KS; ++ks) {
-            const int s = ks % kStages;
-            const uint32_t ph = (uint32_t)((ks / kStages) & 1);
-            if (!mbar_wait(&full_raw[s], ph, p.status)) *abort_flag = 1;
+        const int g = lane >> 2, t = lane & 3;
+        // Stage ks belongs to the kDequantWarps / kWd warps with dw % kWd == ks % kWd;
+        // warp dw / kWd of them takes every (kDequantWarps / kWd)-th unit.  Each warp
+        // so works on every kWd-th stage, and kWd stages are dequantised at once.
+        constexpr int kOwners = kDequantWarps / kWd;
+        const int my_slot = dw % kWd, my_part = dw / kWd;
+        constexpr int kMaxUnits = 4;               // units of one warp per stage (BN <= 256)
+        const int units = rts * tiles;
+        for (int ks = my_slot; ks < KS; ks += kWd) {
+            const int s = ks % RS, w = my_slot;
+            if (ks >= kWd && !mbar_wait(&wd_empty[w], (uint32_t)(((ks / kWd) - 1) & 1), p.status)) *abort_flag = 1;
+            if (!mbar_wait(&raw_full[s], (uint32_t)((ks / RS) & 1), p.status)) *abort_flag = 1;
             if (*reinterpret_cast<volatile int*>(abort_flag)) break;
             const uint8_t* src = wp + s * geo.wp_stage;
-            uint8_t* dst = wd + s * geo.wd_stage;
-            const int g = lane >> 2, t = lane & 3;
+            uint8_t* dst = wd + w * geo.wd_stage;
             // unit = (16-row tile, packed tile of the stage); one lane's 16 bytes each
-            for (int u = dw; u < rts * tiles; u += kDequantWarps) {
+#pragma unroll
+            for (int ui = 0; ui < kMaxUnits; ++ui) {
+                const int u = kOwners * ui + my_part;
+                if (u >= units) continue;
                 const int rt = u / tiles, tl = u - rt * tiles;
                 const int r0 = rt * 16 + g, r1 = r0 + 8;
-                const uint4 wv = reinterpret_cast<const uint4*>(src + (size_t)u * kTileBytes)[lane];
-                const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-                const int64_t kbase = (int64_t)ks * BK + (int64_t)tl * L.KT;  // depth of this packed tile
-                constexpr int kSteps = 16 / BITS;  // k-steps per packed tile
-                uint32_t zc0 = 0, sp0 = 0, zc1 = 0, sp1 = 0;
-                int64_t kb_cur = -1;
+                const int kbase = ks * BK + tl * KT;
+                uint32_t zcs[2][kSteps], sps[2][kSteps];
 #pragma unroll
                 for (int st = 0; st < kSteps; ++st) {
-                    const int64_t kstep_k = kbase + 16 * st;
-                    const int64_t kb = kstep_k / L.bs;
-                    if (kb != kb_cur) {
-                        kb_cur = kb;
-                        consts(r0, kstep_k, zc0, sp0);
-                        consts(r1, kstep_k, zc1, sp1);
+                    const int kb = (kbase + 16 * st) >> bs_log;
+                    const int kb_prev = st ? (kbase + 16 * (st - 1)) >> bs_log : -1;
+                    if (kb != kb_prev) {
+                        consts(r0, kb, zcs[0][st], sps[0][st]);
+                        consts(r1, kb, zcs[1][st], sps[1][st]);
+                    } else {
+                        zcs[0][st] = zcs[0][st - 1];
+                        sps[0][st] = sps[0][st - 1];
+                        zcs[1][st] = zcs[1][st - 1];
+                        sps[1][st] = sps[1][st - 1];
                     }
+                }
+                const uint4 wv = reinterpret_cast<const uint4*>(src + (size_t)u * kTileBytes)[lane];
+                const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+                // swizzled row bases: row r at (r/8)*1024 + (r%8)*128, chunk index xor (r%8)
+                const uint32_t base0 = (uint32_t)((r0 >> 3) * 1024 + (r0 & 7) * 128 + 4 * t);
+                const uint32_t base1 = (uint32_t)((r1 >> 3) * 1024 + (r1 & 7) * 128 + 4 * t);
+                const uint32_t xr = (uint32_t)(r0 & 7);  // r1 & 7 == r0 & 7
+#pragma unroll
+                for (int st = 0; st < kSteps; ++st) {
+                    const uint32_t zc0 = zcs[0][st], zc1 = zcs[1][st];
+                    const uint32_t sp0 = sps[0][st], sp1 = sps[1][st];
                     uint32_t a[4];
                     if constexpr (BITS == 4) {
 #pragma unroll
@@ -361,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(MatmulParams p, Tc
                             if constexpr (BF16X) {
                                 const uint32_t va = prmt(word, 0x4B000000u, 0x7650u | b0);
                                 const uint32_t vb = prmt(word, 0x4B000000u, 0x7650u | b1);
-                                const uint32_t zc = (r & 1) ? zc1 : zc0;
-                                const float2 d = unpack2(fsub2(pack2u(va, vb), pack2u(zc, zc)));
+                                const uint32_t z = (r & 1) ? zc1 : zc0;
+                                const float2 d = unpack2(fsub2(pack2u(va, vb), pack2u(z, z)));
                                 asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(q) : "f"(d.y), "f"(d.x));
                             } else {
                                 q = hsub2(prmt(word, 0x64646464u, b0 | (4u << 4) | (b1 << 8) | (4u << 12)),
@@ -371,21 +418,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(MatmulParams p, Tc
                             a[r] = hmul2(q, (r & 1) ? sp1 : sp0, bf);
                         }
                     }
-                    // register r holds (row r0 or r1, depths 2t/2t+1 or 2t+8/2t+9) of this k-step
-                    const int kl = tl * L.KT + 16 * st;  // depth inside the stage
-                    const int half = kl >> 6, kin = kl & 63;
-                    uint8_t* tile = dst + (size_t)half * (BN * 128);
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int row = (r & 1) ? r1 : r0;
-                        const int k = kin + 2 * t + ((r >> 1) ? 8 : 0);
-                        *reinterpret_cast<uint32_t*>(tile + sw128_off(row, k)) = a[r];
-                    }
+                    // register r: row r0 (r even) / r1 (r odd), depths 2t(+1) (+8 for r >= 2)
+                    const int kl = tl * KT + 16 * st;   // depth inside the stage
+                    uint8_t* tile = dst + (size_t)(kl >> 6) * (BN * 128);
+                    const uint32_t c0 = (uint32_t)((((kl & 63) >> 3) ^ xr) << 4);      // depths 2t, 2t+1
+                    const uint32_t c1 = (uint32_t)(((((kl & 63) >> 3) + 1) ^ xr) << 4); // depths 2t+8, 2t+9
+                    *reinterpret_cast<uint32_t*>(tile + base0 + c0) = a[0];
+                    *reinterpret_cast<uint32_t*>(tile + base1 + c0) = a[1];
+                    *reinterpret_cast<uint32_t*>(tile + base0 + c1) = a[2];
+                    *reinterpret_cast<uint32_t*>(tile + base1 + c1) = a[3];
                 }
             }
             fence_proxy_async_smem();  // make the generic-proxy writes visible to the tensor core
             __syncwarp();
-            if (lane == 0) mbar_arrive(&full_w[s]);
+            if (lane == 0) mbar_arrive(&wd_full[w]);
         }
 
         // ---------------- epilogue: TMEM -> registers -> Y ----------------
@@ -452,7 +498,9 @@ TcGeom make_geom(const MatmulParams& p) {
     const char* env = std::getenv("MNB_TC_BN");
     const int forced = env ? std::atoi(env) : 0;
     double best = 1e30;
-    for (int bn = 32; bn <= 256; bn += 16) {
+    // the four warps that own a stage handle at most 4 (16-row tile, packed tile) units each
+    const int max_bn = 16 * 4 * (kDequantWarps / kWd) / g.tiles_per_stage_row;
+    for (int bn = 32; bn <= 256 && bn <= max_bn; bn += 16) {
         if (forced && bn != forced) continue;
         const int64_t nt = (L.N + bn - 1) / bn;
         const int64_t tiles = nt * g.m_tiles;
@@ -472,17 +520,25 @@ TcGeom make_geom(const MatmulParams& p) {
     g.wp_stage = (size_t)(g.BN / 16) * g.tiles_per_stage_row * kTileBytes;
     g.scale_bytes = round16((size_t)g.BN * L.KB * (p.scale_dtype == kF32 ? 4 : 2));
     g.zp_bytes = round16(p.zp ? (size_t)g.BN * L.zp_row : 0);
-    g.total_bytes = 1024 + kStages * (g.x_stage + g.wd_stage + g.wp_stage) + g.scale_bytes + g.zp_bytes +
-                    (3 * kStages + 4) * 8 + 16;
+    // blocks reachable by the staged depths (the packed rows run to KTILES * KT)
+    g.tab_stride = (int)(((L.KTILES * L.KT + L.bs - 1) / L.bs) | 1);
+    g.tab_bytes = round16((size_t)g.BN * g.tab_stride * 4);
+    const size_t fixed = 1024 + kWd * g.wd_stage + g.scale_bytes + g.zp_bytes + g.tab_bytes +
+                         (2 * kMaxRaw + 2 * kWd + 4) * 8 + 16;
+    const size_t limit = device_info().smem_optin ? device_info().smem_optin : 232448;
+    g.raw_stages = kMaxRaw;
+    while (g.raw_stages > 2 && fixed + g.raw_stages * (g.x_stage + g.wp_stage) > limit) --g.raw_stages;
+    g.total_bytes = fixed + g.raw_stages * (g.x_stage + g.wp_stage);
     return g;
 }
 
 template <int BITS, bool BF16X>
-cudaError_t launch(const MatmulParams& p, const TcGeom& geo, const CUtensorMap& map, cudaStream_t s) {
+cudaError_t launch(const MatmulParams& p, const TcGeom& geo, const CUtensorMap& map, const CUtensorMap& wmap,
+                   cudaStream_t s) {
     auto kern = gemm_tc_kernel<BITS, BF16X>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.total_bytes);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(geo.n_tiles * geo.m_tiles), kThreads, geo.total_bytes, s>>>(p, geo, map);
+    kern<<<(unsigned)(geo.n_tiles * geo.m_tiles), kThreads, geo.total_bytes, s>>>(p, geo, map, wmap);
     return cudaGetLastError();
 }
 
@@ -515,11 +571,21 @@ cudaError_t launch_gemm_tc(const MatmulParams& p, cudaStream_t s) {
     CUresult r = enc(&map, dt, 2, const_cast<void*>(p.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    // Packed codes as a 3-D tensor of 16-bit elements: [row tile][k tile][256 x u16].
+    CUtensorMap wmap;
+    const cuuint64_t wdims[3] = {256, (cuuint64_t)p.L.KTILES, (cuuint64_t)p.L.NT};
+    const cuuint64_t wstrides[2] = {(cuuint64_t)kTileBytes, (cuuint64_t)p.L.KTILES * kTileBytes};
+    const cuuint32_t wbox[3] = {256, (cuuint32_t)geo.tiles_per_stage_row, (cuuint32_t)(geo.BN / 16)};
+    const cuuint32_t westr[3] = {1, 1, 1};
+    r = enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint8_t*>(p.packed), wdims, wstrides, wbox, westr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     const bool bf = p.act_dtype == kBF16;
     switch (p.L.bits) {
-        case 2: return bf ? launch<2, true>(p, geo, map, s) : launch<2, false>(p, geo, map, s);
-        case 4: return bf ? launch<4, true>(p, geo, map, s) : launch<4, false>(p, geo, map, s);
-        case 8: return bf ? launch<8, true>(p, geo, map, s) : launch<8, false>(p, geo, map, s);
+        case 2: return bf ? launch<2, true>(p, geo, map, wmap, s) : launch<2, false>(p, geo, map, wmap, s);
+        case 4: return bf ? launch<4, true>(p, geo, map, wmap, s) : launch<4, false>(p, geo, map, wmap, s);
+        case 8: return bf ? launch<8, true>(p, geo, map, wmap, s) : launch<8, false>(p, geo, map, wmap, s);
         default: return cudaErrorInvalidValue;
     }
 }

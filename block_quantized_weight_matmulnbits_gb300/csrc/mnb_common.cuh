@@ -208,14 +208,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait on a phase of an mbarrier.  Each try_wait already suspends the
-// thread for a hardware-chosen interval, so the limit is a count of retries.
-// Returns false (and records MNB_ERR_TIMEOUT) when the limit runs out.
-constexpr uint32_t kWaitLimit = 1u << 22;
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or the hint (nanoseconds) elapses, instead of polling the barrier.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on a phase of an mbarrier: retries of a suspending try_wait
+// (up to kWaitHintNs each), about two seconds in all.  Returns false (and
+// records MNB_ERR_TIMEOUT) when the limit runs out.
+constexpr uint32_t kWaitHintNs = 100000;
+constexpr uint32_t kWaitLimit = 20000;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
     for (uint32_t i = 0; i < kWaitLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kWaitHintNs)) return true;
     }
     set_status(status, 5 /* MNB_ERR_TIMEOUT */);
     return false;
