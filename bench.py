@@ -4,7 +4,9 @@
 Default workload: the int4 decode GEMV, M=1, K=4096, N=11008, bf16 X/Y, f16
 scales, uint8 zero points (block 32), metric GB/s (algorithmic bytes / time).
 ``--config 4`` selects the M=512 prefill GEMM (metric TFLOP/s).  The default
-run also reports the M=512 GEMM as a secondary object.
+run also reports the M=512 GEMM and the int8-activation path (accuracy level
+4: activation quantisation + integer GEMV) on the decode workload as
+secondary objects.
 
 A step is one mnb_matmul call over one batch (the decode step of one
 projection).  Weights are rotated over enough distinct copies that every
@@ -49,6 +51,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--accuracy-level", type=int, default=0, choices=[0, 4],
+                    help="4: int8-activation path for the main workload")
     return ap.parse_args()
 
 
@@ -138,7 +142,7 @@ def cpu_oracle_rate(w: wl.Workload, data, seconds: float):
     n_cols = max(1, min(w.N, 64))
     done_cols, t_total = 0, 0.0
     rng = np.random.default_rng(1)
-    while t_total < seconds and done_cols < 50 * w.N:
+    while t_total < seconds and done_cols < 1000 * w.N:
         cols = rng.integers(0, w.N, n_cols)
         ms = np.repeat(np.arange(w.M), n_cols)
         ns = np.tile(cols, w.M)
@@ -154,6 +158,23 @@ def cpu_oracle_rate(w: wl.Workload, data, seconds: float):
     sample = (f"{done_cols} output columns x all {w.M} rows (={frac:.3g} of the workload) in {t_total:.2f} s, "
               f"fp64 oracle, OpenMP over outputs")
     return value, cores, sample
+
+
+# ---- rank logic (replicas: no data-path collective) ------------------------
+
+def max_over_ranks(t: float, dist=None, device="cuda") -> float:
+    """The slowest rank's time (the job ends when the last replica does)."""
+    if dist is None:
+        return t
+    import torch
+    tt = torch.tensor([t], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_value(world: int, steps: int, per_step: float, t: float) -> float:
+    """Units all ranks processed / the max-over-ranks time (weak scaling)."""
+    return world * steps * per_step / t
 
 
 # ---- GPU arm ---------------------------------------------------------------
@@ -214,7 +235,7 @@ def run_ours(args):
 
     flags = 0 if args.no_pdl else mnb.MNB_FLAG_PDL
 
-    def measure(w: wl.Workload, steps: int, warmup: int, kernel: str, want_e2e: bool):
+    def measure(w: wl.Workload, steps: int, warmup: int, kernel: str, want_e2e: bool, acc: int = 0):
         data = wl.generate(w)
         x = to_dev(data["x"], w.act_dtype)
         b = torch.from_numpy(np.ascontiguousarray(data["b"])).cuda()
@@ -224,7 +245,9 @@ def run_ours(args):
         mnb.mnb_pack_weights(b, packed, w.N, w.K, w.bits, w.bs)
         del b
         chosen = kernel if kernel != "auto" else mnb.mnb_select_kernel(w.M, w.N, w.K, w.bits, w.bs,
-                                                                       w.act_dtype)
+                                                                       w.act_dtype, acc)
+        ws_bytes = mnb.mnb_workspace_size(w.M, w.N, w.K, w.bits, w.bs, acc)
+        ws = aligned_empty(ws_bytes) if ws_bytes else None
         # weight copies so that each step streams from HBM
         l2 = torch.cuda.get_device_properties(local).L2_cache_size
         wbytes = packed.numel() + s0.numel() * s0.element_size() + (zp0.numel() if zp0 is not None else 0)
@@ -241,7 +264,7 @@ def run_ours(args):
             pb, s, zp = copies[i % R]
             mnb.mnb_matmul_ex(x if xin is None else xin, pb, s, zp, yb if yout is None else yout, w.M, w.N,
                               w.K, w.bits, w.bs, w.act_dtype, w.out_dtype, w.scale_dtype, kernel=kernel,
-                              stream=stream, flags=flags)
+                              stream=stream, flags=flags, accuracy_level=acc, workspace=ws)
 
         with torch.cuda.stream(stream):
             for i in range(R):
@@ -278,16 +301,13 @@ def run_ours(args):
             ev1.record(stream)
         barrier()
         ck = clocks.stop()
-        t = ev0.elapsed_time(ev1) / 1e3
-        if dist is not None:
-            tt = torch.tensor([t], device="cuda")
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            t = float(tt.item())
+        t = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, dist)
         unit, per_step = metric_of(w)
-        value = world * steps_eff * per_step / t
+        value = whole_job_value(world, steps_eff, per_step, t)
         per_launch_s = t / steps_eff
+        kernels_per_step = 2 if acc == 4 else 1  # accuracy level 4: activation quantisation + GEMV
         out = {"value": value, "unit": unit, "steps": steps_eff, "ms_per_step": per_launch_s * 1e3,
-               "kernel": chosen, "clocks": ck, "weight_copies": R, "launches": steps_eff}
+               "kernel": chosen, "clocks": ck, "weight_copies": R, "launches": steps_eff * kernels_per_step}
         if unit == "GB/s":
             peak = pk["hbm_gbs"]
             out["roofline"] = {"bound": "hbm", "achieved": per_step / per_launch_s, "peak": peak, "unit": "GB/s",
@@ -327,19 +347,15 @@ def run_ours(args):
                     ge.replay()
                 e1.record(stream)
             barrier()
-            te = e0.elapsed_time(e1) / 1e3
-            if dist is not None:
-                tt = torch.tensor([te], device="cuda")
-                dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-                te = float(tt.item())
-            out["e2e"] = {"value": world * reps * R * per_step / te, "unit": unit,
+            te = max_over_ranks(e0.elapsed_time(e1) / 1e3, dist)
+            out["e2e"] = {"value": whole_job_value(world, max(1, reps) * R, per_step, te), "unit": unit,
                           "h2d_bytes_per_step": x.numel() * x.element_size(),
                           "d2h_bytes_per_step": yb.numel() * yb.element_size(),
                           "mode": "CUDA graph of (H2D X from pinned host, mnb_matmul, D2H Y to pinned host) per step"}
         return out, data
 
     w = wl.config(args.config)
-    main, data = measure(w, args.steps, args.warmup, args.kernel, True)
+    main, data = measure(w, args.steps, args.warmup, args.kernel, True, args.accuracy_level)
     res = {
         "metric": "int4 MatMulNBits GB/s at M=1, TFLOP/s at M=512; % of roofline",
         "value": main["value"], "unit": main["unit"], "n_gpus": world, "steps": main["steps"],
@@ -349,6 +365,7 @@ def run_ours(args):
         "data": "synthetic (seeded, LLM-projection shaped; no trained weights)",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "bits": w.bits, "block_size": w.bs,
                    "zero_points": w.zp is not None, "kernel": main["kernel"],
+                   "accuracy_level": args.accuracy_level,
                    "l2": f"inputs larger than L2: {main['weight_copies']} rotating weight copies (>= 3 x L2)",
                    "launch": "CUDA graph replay, one kernel per step"},
         "roofline": main["roofline"], "clocks": main["clocks"], "e2e": main["e2e"],
@@ -360,6 +377,12 @@ def run_ours(args):
         res["m512"] = {"workload": w2.name, "value": sec["value"], "unit": sec["unit"], "kernel": sec["kernel"],
                        "ms_per_step": sec["ms_per_step"], "roofline": sec["roofline"], "clocks": sec["clocks"]}
         res["gpu_launches"] += sec["launches"]
+    if args.config == 1 and args.accuracy_level == 0 and not args.no_secondary:
+        sec, _ = measure(w, max(20, args.steps // 4), max(3, args.warmup // 4), "auto", False, 4)
+        res["a8"] = {"workload": w.name, "accuracy_level": 4, "value": sec["value"], "unit": sec["unit"],
+                     "kernel": sec["kernel"], "ms_per_step": sec["ms_per_step"], "roofline": sec["roofline"],
+                     "clocks": sec["clocks"], "launches_per_step": 2}
+        res["gpu_launches"] += sec["launches"]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = cpu_oracle_rate(w, data, args.cpu_seconds)
         res["cpu_baseline"] = {"value": v, "unit": main["unit"], "cores": cores, "kind": "oracle", "sample": sample}
@@ -370,9 +393,10 @@ def run_ours(args):
 
 
 def run_reference(args):
+    """The CPU oracle as it stands, on rank 0 only (other ranks exit without work)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
-        return
+        return None
     w = wl.config(args.config)
     data = wl.generate(w)
     unit, _ = metric_of(w)
@@ -396,6 +420,7 @@ def run_reference(args):
                             "sample": f"per step: {sample}"},
            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
+    return res
 
 
 if __name__ == "__main__":
