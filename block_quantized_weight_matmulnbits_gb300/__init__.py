@@ -25,8 +25,9 @@ KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 EXPORTS = [
     "mnb_packed_size", "mnb_pack_weights", "mnb_unpack_codes", "mnb_dequantize", "mnb_matmul",
     "mnb_matmul_ex", "mnb_workspace_size", "mnb_quantize_activations", "mnb_select_kernel",
-    "mnb_get_device_error", "mnb_status_string", "mnb_kernel_name", "mnb_abi_version",
+    "mnb_get_device_error", "mnb_status_string", "mnb_kernel_name", "mnb_abi_version", "mnb_matmul_a8_static",
 ]
+MNB_A8_STATIC_SCRATCH_BYTES = 1 << 20
 
 
 class MnbError(RuntimeError):
@@ -78,6 +79,7 @@ def load(build: bool = True):
             "mnb_status_string": (ctypes.c_char_p, [ci]),
             "mnb_kernel_name": (ctypes.c_char_p, [ci]),
             "mnb_abi_version": (ci, []),
+            "mnb_matmul_a8_static": (ci, [vp, vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, ci, ci, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -160,6 +162,13 @@ def mnb_matmul_ex(x, packed_b, scales, zero_points, y, M, N, K, bits, block_size
     a.stream = _stream(stream)
     a.flags = flags
     _check(load().mnb_matmul_ex(ctypes.byref(a)), f"mnb_matmul_ex[{kernel}]")
+
+
+def mnb_matmul_a8_static(x, packed_b, scales, zero_points, y, M, N, K, bits, block_size, act_dtype, out_dtype,
+                         scale_dtype, stream=None):
+    _check(load().mnb_matmul_a8_static(_ptr(x), _ptr(packed_b), _ptr(scales), _ptr(zero_points), _ptr(y), M, N, K,
+                                       bits, block_size, act_dtype, out_dtype, scale_dtype, _stream(stream)),
+           "mnb_matmul_a8_static")
 
 
 def mnb_workspace_size(M, N, K, bits, block_size, accuracy_level) -> int:

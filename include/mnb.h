@@ -194,6 +194,28 @@ MNB_API size_t mnb_workspace_size(int64_t M, int64_t N, int64_t K, int bits, int
 MNB_API mnb_status mnb_quantize_activations(const void* x, int8_t* qa, float* sa, int64_t M, int64_t K,
                                     int block_size, mnb_dtype act_dtype, mnb_stream_t stream);
 
+/* int8-activation matmul (accuracy level 4) that allocates nothing and takes
+ * no workspace: for callers that cannot call cudaMalloc.  No counterpart on
+ * the pages; an addition to the boundary.  Arguments as mnb_matmul (device
+ * pointers, ORT layouts); zero_points may be NULL.
+ *   Scratch: a file-scope device array of MNB_A8_STATIC_SCRATCH_BYTES (1 MiB)
+ *   per device holds the quantised activations and their block scales
+ *   (mnb_workspace_size(M, N, K, bits, block_size, 4) bytes).  Calls that
+ *   need more return MNB_ERR_NO_MEM without launching.  Nothing in it needs
+ *   to start at zero: the quantisation kernel writes every byte the GEMV
+ *   reads.
+ *   Set-up: the first call on a device looks the array up
+ *   (cudaGetSymbolAddress); make that first call outside stream capture.
+ *   Concurrency: calls that overlap on the same device (different streams,
+ *   threads or graphs in flight together) share the array and race; calls
+ *   ordered on one stream are safe.
+ * Returns the statuses of mnb_matmul_ex with accuracy_level 4. */
+#define MNB_A8_STATIC_SCRATCH_BYTES (1u << 20)
+MNB_API mnb_status mnb_matmul_a8_static(const void* x, const void* packed_b, const void* scales,
+                                        const uint8_t* zero_points, void* y, int64_t M, int64_t N, int64_t K,
+                                        int bits, int block_size, mnb_dtype act_dtype, mnb_dtype out_dtype,
+                                        mnb_dtype scale_dtype, mnb_stream_t stream);
+
 /* ---- diagnostics ------------------------------------------------------- */
 
 /* The family mnb_matmul_ex would run with kernel == MNB_KERNEL_AUTO (host
