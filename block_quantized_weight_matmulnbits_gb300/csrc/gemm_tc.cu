@@ -19,15 +19,16 @@
 //                 descriptors advanced by addition): it shares an SM
 //                 sub-partition with dequantising warps, and its per-stage
 //                 latency paces the whole pipeline.
-//   warps 2-3   : idle (they keep the dequantising warps' sub-partition
-//                 placement even).
+//   warps 2-3   : per stage, convert the BN rows' block scales and zero
+//                 points into 32-bit entries (zero-point constant | scale in
+//                 the MMA's input type) in a small shared-memory ring; the two
+//                 warps take alternate stages and keep the next stage's
+//                 global loads in flight while they store the current one.
 //   warps 4-19  : dequantise.  The stage's (16-row tile, packed tile) units
 //                 are dealt round-robin over the 16 warps (unit U of the
 //                 kernel to warp U % 16); every warp still visits every stage
-//                 in order, so each barrier is only ever waited on for its
-//                 current or next phase.  A unit's block scales and zero
-//                 points are loaded from global memory one unit ahead.  A
-//                 code pair is masked into the mantissa of 128.0 / 1024.0,
+//                 only at most R - 1 stages apart, so each barrier is only
+//                 ever waited on for its current or next phase.  A code pair is masked into the mantissa of 128.0 / 1024.0,
 //                 (q - zp) is one exact packed subtract and one packed
 //                 multiply by the block scale rounds w once to the MMA's input
 //                 type, written straight into the canonical K-major
@@ -39,6 +40,7 @@
 // returns.  The reduction order over K is fixed, so results are deterministic.
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <cuda.h>
 
 #include "mnb_internal.h"
@@ -60,8 +62,11 @@ struct TcGeom {
     int m_tiles;     // ceil(M / 128)
     int k_stages;    // ceil(KTILES * KT / BK)
     int units;       // (16-row tile, packed tile) units per stage
+    int nbs;         // quantisation blocks per stage (max(1, BK / bs)); BN * nbs <= 256
     int R;           // ring depth
-    size_t x_stage, wp_stage, wd_stage, total_bytes;
+    int scale_tma;   // raw scales / zero points arrive by TMA, SB blocks at a time
+    int sb;          // blocks per raw scale buffer (TMA path)
+    size_t x_stage, wp_stage, wd_stage, ent_stage, sraw_bytes, zraw_bytes, total_bytes;
 };
 
 // ---- PTX wrappers specific to tcgen05 / TMA tensor copies ----
@@ -157,7 +162,9 @@ __device__ __forceinline__ uint32_t to_pair(float v, bool bf16) {
 template <int BITS, bool BF16X, int NBU>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(MatmulParams p, TcGeom geo,
                                                                const __grid_constant__ CUtensorMap xmap,
-                                                               const __grid_constant__ CUtensorMap wmap) {
+                                                               const __grid_constant__ CUtensorMap wmap,
+                                                               const __grid_constant__ CUtensorMap smap,
+                                                               const __grid_constant__ CUtensorMap zmap) {
     constexpr int KT = 256 / BITS;              // depths per packed tile
     constexpr int kSteps = 16 / BITS;           // 16-deep k-steps per packed tile
     constexpr int SPB = kSteps / NBU;           // k-steps per quantisation block inside a unit
@@ -165,16 +172,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(MatmulParams p, Tc
     constexpr uint32_t kMag = BF16X ? 0x43004300u : 0x64006400u;
     const Layout& L = p.L;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived by pointer arithmetic so the compiler keeps
+    // the shared address space (plain loads / stores compile to LDS / STS)
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int R = geo.R;
     uint8_t* xs = smem;                                   // [R][BK/64][128 x 64] bf16, SW128 (TMA)
     uint8_t* wd = xs + R * geo.x_stage;                   // [R][BK/64][BN x 64] bf16, SW128
     uint8_t* wp = wd + R * geo.wd_stage;                  // [R][BN/16][TILES][512 B] packed codes (TMA)
-    uint64_t* bars = reinterpret_cast<uint64_t*>(wp + R * geo.wp_stage);
+    uint8_t* ent = wp + R * geo.wp_stage;                 // [R][BN][nbs] u32 (zero-point constant | scale << 16)
+    uint8_t* sraw = ent + R * geo.ent_stage;              // [2][BN][sb] raw scales (TMA path)
+    uint8_t* zraw = sraw + 2 * geo.sraw_bytes;            // [2][BN][sb * bits / 8] raw zero points (TMA path)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(zraw + 2 * geo.zraw_bytes);
     uint64_t* tma_full = bars;                            // X tile + packed codes landed
     uint64_t* wd_full = bars + kMaxR;                     // all units of the stage dequantised
     uint64_t* mma_done = bars + 2 * kMaxR;                // MMAs of the stage finished: slot free
-    uint64_t* done = bars + 3 * kMaxR;                    // accumulator complete
+    uint64_t* ent_full = bars + 3 * kMaxR;                // scale / zero-point entries of the stage written
+    uint64_t* raw_full = bars + 4 * kMaxR;                // raw scale buffer b landed (TMA path)
+    uint64_t* done = raw_full + 2;                        // accumulator complete
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -192,7 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(MatmulParams p, Tc
             mbar_init(&tma_full[s], 1);
             mbar_init(&wd_full[s], geo.units);
             mbar_init(&mma_done[s], 1);
+            mbar_init(&ent_full[s], 1);
         }
+        mbar_init(&raw_full[0], 1);
+        mbar_init(&raw_full[1], 1);
         mbar_init(done, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -278,81 +295,213 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(MatmulParams p, Tc
         }
         if (lane == 0) tc_commit(done);
         __syncwarp();
-    } else if (warp >= kCtlWarps) {
+    } else if (warp < kCtlWarps) {
+        // ---------------- scale / zero-point entries ----------------
+        const int nsw = geo.scale_tma ? 1 : (R >= 3 ? 2 : 1);  // consecutive stages of a warp stay within R - 1
+        const int sw = warp - 2;
+        if (geo.scale_tma && sw == 0) {
+            // Raw scales (and zero points) of SB blocks of the BN rows arrive by TMA
+            // into a double buffer; this warp converts each stage's blocks from
+            // shared memory.
+            const int SB = geo.sb, sb_log = __ffs(SB) - 1;
+            const int nbs = geo.nbs, nbs_log = __ffs(nbs) - 1;
+            const int per_stage = BN * nbs;
+            const int bs_log = __ffs(L.bs) - 1;
+            const int sdt = p.scale_dtype;
+            const int zmask = code_mask(BITS);
+            const uint32_t zrow = (uint32_t)(SB * BITS / 8);
+            const int nq = (int)((L.KB + SB - 1) >> sb_log);
+            const uint32_t rbytes = (uint32_t)(geo.sraw_bytes + (p.zp ? geo.zraw_bytes : 0));
+            auto issue = [&](int q) {
+                const int b = q & 1;
+                mbar_arrive_expect_tx(&raw_full[b], rbytes);
+                tma_load_2d(sraw + b * geo.sraw_bytes, &smap, q * SB, (int)n0, &raw_full[b]);
+                if (p.zp) tma_load_2d(zraw + b * geo.zraw_bytes, &zmap, q * SB * BITS / 8, (int)n0, &raw_full[b]);
+            };
+            if (lane == 0) {
+                issue(0);
+                if (nq > 1) issue(1);
+            }
+            int q_cur = -1, waited = 0, issued = nq > 1 ? 2 : 1;
+            int s = 0;
+            uint32_t ph = 0;
+            for (int ks = 0; ks < KS; ++ks) {
+                const int64_t kb0 = ((int64_t)ks * BK) >> bs_log;
+                const int q = (int)(kb0 >> sb_log);
+                if (q != q_cur) {
+                    if (q_cur >= 0 && q_cur + 2 < nq) {
+                        if (lane == 0) issue(q_cur + 2);  // buffer of q_cur is free again
+                        issued = q_cur + 3;
+                    }
+                    if (!mbar_wait(&raw_full[q & 1], (uint32_t)((q >> 1) & 1), p.status)) {
+                        *abort_v = 1;
+                        break;
+                    }
+                    waited = q + 1;
+                    q_cur = q;
+                }
+                if (ks >= R && !mbar_wait(&mma_done[s], ph ^ 1u, p.status)) {
+                    *abort_v = 1;
+                    break;
+                }
+                const uint8_t* sb_base = sraw + (q & 1) * geo.sraw_bytes;
+                const uint8_t* zb_base = zraw + (q & 1) * geo.zraw_bytes;
+                uint32_t* dst = reinterpret_cast<uint32_t*>(ent + s * geo.ent_stage);
+                const int kl0 = (int)(kb0 - ((int64_t)q << sb_log));
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int e = lane + 32 * i;
+                    if (e < per_stage) {
+                        const int r = e >> nbs_log, kl = kl0 + (e & (nbs - 1));
+                        float sc;
+                        if (sdt == kF32) {
+                            sc = reinterpret_cast<const float*>(sb_base)[r * SB + kl];
+                        } else {
+                            const unsigned short v = reinterpret_cast<const unsigned short*>(sb_base)[r * SB + kl];
+                            sc = sdt == kF16 ? __half2float(__ushort_as_half(v)) : __uint_as_float((uint32_t)v << 16);
+                        }
+                        uint32_t z = 1u << (BITS - 1);
+                        if (p.zp) {
+                            const uint32_t bit = (uint32_t)kl * BITS;
+                            z = ((uint32_t)zb_base[r * zrow + (bit >> 3)] >> (bit & 7)) & zmask;
+                        }
+                        uint32_t lo;
+                        if constexpr (BITS == 8 && BF16X) lo = z;
+                        else lo = (kMag & 0xFFFFu) + z;
+                        dst[e] = lo | (to_pair(sc, BF16X) << 16);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ent_full[s]);
+                if (++s == R) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (*abort_v && lane == 0) {
+                // let raw copies still in flight land (bounded)
+                for (int q = waited; q < issued; ++q)
+                    for (int it = 0; it < (1 << 16); ++it)
+                        if (mbar_try_wait(&raw_full[q & 1], (uint32_t)((q >> 1) & 1))) break;
+            }
+        } else if (!geo.scale_tma && sw < nsw) {
+            const int nbs = geo.nbs;
+            const int nbs_log = __ffs(nbs) - 1;
+            const int per_stage = BN * nbs;  // <= 256: at most 8 entries per lane
+            const int bs_log = __ffs(L.bs) - 1;
+            const int sdt = p.scale_dtype;
+            const int zmask = code_mask(BITS);
+            float sa[8], sb[8];
+            uint32_t za[8], zb[8];
+            auto load = [&](int ks, float (&sc)[8], uint32_t (&zz)[8]) {
+                const int64_t kbs = ((int64_t)ks * BK) >> bs_log;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int e = lane + 32 * i;
+                    const int64_t n = n0 + (e >> nbs_log), kb = kbs + (e & (nbs - 1));
+                    const bool ok = e < per_stage && n < L.N && kb < L.KB;
+                    sc[i] = ok ? load_f32(p.scales, n * L.KB + kb, sdt) : 0.f;
+                    uint32_t z = 1u << (BITS - 1);
+                    if (p.zp != nullptr) {
+                        const int64_t bit = kb * BITS;
+                        z = ok ? ((uint32_t)__ldg(p.zp + n * L.zp_row + (bit >> 3)) >> (bit & 7)) & zmask : 0u;
+                    }
+                    zz[i] = z;
+                }
+            };
+            if (sw < KS) load(sw, sa, za);
+            for (int ks = sw; ks < KS; ks += nsw) {
+                if (ks + nsw < KS) load(ks + nsw, sb, zb);
+                const int s = ks % R;
+                const uint32_t ph = (uint32_t)((ks / R) & 1);
+                if (ks >= R && !mbar_wait(&mma_done[s], ph ^ 1u, p.status)) {
+                    *abort_v = 1;
+                    break;
+                }
+                uint32_t* dst = reinterpret_cast<uint32_t*>(ent + s * geo.ent_stage);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int e = lane + 32 * i;
+                    if (e < per_stage) {
+                        uint32_t lo;
+                        if constexpr (BITS == 8 && BF16X) lo = za[i];
+                        else lo = (kMag & 0xFFFFu) + za[i];
+                        dst[e] = lo | (to_pair(sa[i], BF16X) << 16);
+                    }
+                    sa[i] = sb[i];
+                    za[i] = zb[i];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ent_full[s]);
+            }
+        }
+    } else {
         // ---------------- dequantiser, then epilogue ----------------
         const int dw = warp - kCtlWarps;
         const int units = geo.units;
         const int total_units = KS * units;
         const int g = lane >> 2, t = lane & 3;
         const int bs_log = __ffs(L.bs) - 1;
-        const int zmask = code_mask(BITS);
-        const int sdt = p.scale_dtype;
-
-        // raw block scales (f32 bits) and zero points of rows g and g+8 of a unit
-        float sc_n[2][NBU];
-        uint32_t z_n[2][NBU];
-        auto prefetch = [&](int U) {
-            const int ks = U / units, u = U - ks * units;
-            const int rt = u / TILES, tl = u - rt * TILES;
-            const int64_t kb0 = ((int64_t)ks * BK + tl * KT) >> bs_log;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int64_t n = n0 + rt * 16 + g + 8 * h;
-#pragma unroll
-                for (int j = 0; j < NBU; ++j) {
-                    const int64_t kb = kb0 + j;
-                    const bool ok = n < L.N && kb < L.KB;
-                    sc_n[h][j] = ok ? load_f32(p.scales, n * L.KB + kb, sdt) : 0.f;
-                    uint32_t z = 1u << (BITS - 1);
-                    if (p.zp != nullptr) {
-                        const int64_t bit = kb * BITS;
-                        z = ok ? ((uint32_t)__ldg(p.zp + n * L.zp_row + (bit >> 3)) >> (bit & 7)) & zmask : 0u;
-                    }
-                    z_n[h][j] = z;
-                }
-            }
-        };
+        const int nbs = geo.nbs;
         // Active warps: at most units * (R - 1), so consecutive stages a warp works
         // on are at most R - 1 apart and every barrier it waits on is at its
         // current or next phase.
         const int A = units * (R - 1) < kDqWarps ? units * (R - 1) : kDqWarps;
         bool ok = true;
         if (dw < A) {
-            if (dw < total_units) prefetch(dw);
             int ks = dw / units, u = dw - ks * units;
             int s = ks % R;
             uint32_t ph = (uint32_t)((ks / R) & 1);
+            const int dks = A / units, du = A - dks * units;  // advance per unit of this warp
             for (int U = dw; U < total_units; U += A) {
                 if (ks >= R && !mbar_wait(&mma_done[s], ph ^ 1u, p.status)) {
                     ok = false;
                     break;
                 }
-                if (!mbar_wait(&tma_full[s], ph, p.status)) {
+                if (!mbar_wait(&tma_full[s], ph, p.status) || !mbar_wait(&ent_full[s], ph, p.status)) {
                     ok = false;
                     break;
                 }
-                // this unit's constants, then start the loads of the warp's next unit
+                const int rt = u / TILES, tl = u - rt * TILES;
+                // this unit's constants: entries of rows g, g + 8 for its NBU blocks
                 uint32_t zc[2][NBU], sp[2][NBU];
+                {
+                    const int j0 = (L.bs <= KT) ? ((tl * KT) >> bs_log) : 0;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t* ea = reinterpret_cast<const uint32_t*>(ent + s * geo.ent_stage) +
+                                             (rt * 16 + g + 8 * h) * nbs + j0;
+                        uint32_t e[NBU];
+                        if constexpr (NBU == 1) {
+                            e[0] = ea[0];
+                        } else if constexpr (NBU == 2) {
+                            const uint2 v = *reinterpret_cast<const uint2*>(ea);
+                            e[0] = v.x;
+                            e[1] = v.y;
+                        } else {
 #pragma unroll
-                    for (int j = 0; j < NBU; ++j) {
-                        sp[h][j] = to_pair(sc_n[h][j], BF16X);
-                        const uint32_t z = z_n[h][j];
-                        if constexpr (BITS == 8 && BF16X) zc[h][j] = 0x4B000000u | z;
-                        else zc[h][j] = ((kMag & 0xFFFFu) + z) * 0x10001u;
+                            for (int q = 0; q < NBU; q += 4) {
+                                const uint4 v = *reinterpret_cast<const uint4*>(ea + q);
+                                e[q] = v.x;
+                                e[q + 1] = v.y;
+                                e[q + 2] = v.z;
+                                e[q + 3] = v.w;
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < NBU; ++j) {
+                            sp[h][j] = prmt(e[j], e[j], 0x3232u);  // scale in both halves
+                            if constexpr (BITS == 8 && BF16X) zc[h][j] = 0x4B000000u | (e[j] & 0xFFu);
+                            else zc[h][j] = prmt(e[j], e[j], 0x1010u);  // zero-point constant in both halves
+                        }
                     }
                 }
-                if (U + A < total_units) prefetch(U + A);
 
-                const int rt = u / TILES, tl = u - rt * TILES;
-                const uint4 wv = reinterpret_cast<const uint4*>(wp + s * geo.wp_stage + u * kTileBytes)[lane];
+                const uint4 wv = *reinterpret_cast<const uint4*>(wp + s * geo.wp_stage + u * kTileBytes + lane * 16);
                 const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-                uint8_t* dst = wd + s * geo.wd_stage;
-                const int r0 = rt * 16 + g;
                 // swizzled row bases: row r at (r/8)*1024 + (r%8)*128, 16-byte chunk index xor (r%8)
-                const uint32_t base0 = (uint32_t)((r0 >> 3) * 1024 + g * 128 + 4 * t);
-                const uint32_t base1 = base0 + 1024;  // row r0 + 8
+                uint8_t* base0 = wd + s * geo.wd_stage + (rt * 2048 + g * 128 + 4 * t);
+                uint8_t* base1 = base0 + 1024;  // row r0 + 8
 #pragma unroll
                 for (int st = 0; st < kSteps; ++st) {
                     const int j = st / SPB;
@@ -394,26 +543,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(MatmulParams p, Tc
                     }
                     // register r: row r0 (r even) / r0 + 8 (r odd), depths 2t(+1) (+8 for r >= 2)
                     const int kl = tl * KT + 16 * st;  // depth inside the stage
-                    uint8_t* tile = dst + (size_t)(kl >> 6) * (BN * 128);
-                    const uint32_t c0 = (uint32_t)((((kl & 63) >> 3) ^ g) << 4);        // depths 2t, 2t+1
-                    const uint32_t c1 = (uint32_t)(((((kl & 63) >> 3) + 1) ^ g) << 4);  // depths 2t+8, 2t+9
-                    *reinterpret_cast<uint32_t*>(tile + base0 + c0) = a[0];
-                    *reinterpret_cast<uint32_t*>(tile + base1 + c0) = a[1];
-                    *reinterpret_cast<uint32_t*>(tile + base0 + c1) = a[2];
-                    *reinterpret_cast<uint32_t*>(tile + base1 + c1) = a[3];
+                    const uint32_t tile = (uint32_t)(kl >> 6) * (uint32_t)(BN * 128);
+                    const uint32_t c0 = tile + (uint32_t)((((kl & 63) >> 3) ^ g) << 4);        // depths 2t, 2t+1
+                    const uint32_t c1 = tile + (uint32_t)(((((kl & 63) >> 3) + 1) ^ g) << 4);  // depths 2t+8, 2t+9
+                    *reinterpret_cast<uint32_t*>(base0 + c0) = a[0];
+                    *reinterpret_cast<uint32_t*>(base1 + c0) = a[1];
+                    *reinterpret_cast<uint32_t*>(base0 + c1) = a[2];
+                    *reinterpret_cast<uint32_t*>(base1 + c1) = a[3];
                 }
                 fence_proxy_async_smem();  // generic-proxy writes -> tensor core
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&wd_full[s]);
                 // advance (stage, unit) by A units
-                u += A;
-                while (u >= units) {
+                u += du;
+                int adv = dks;
+                if (u >= units) {
                     u -= units;
-                    ++ks;
-                    if (++s == R) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+                    ++adv;
+                }
+                ks += adv;
+                s += adv;
+                while (s >= R) {
+                    s -= R;
+                    ph ^= 1u;
                 }
             }
         }
@@ -504,18 +656,22 @@ TcGeom make_geom(const MatmulParams& p) {
     const char* env = std::getenv("MNB_TC_BN");
     const int forced = env ? std::atoi(env) : 0;
     double best = 1e30;
-    for (int bn = 32; bn <= 256; bn += 16) {
+    g.nbs = L.bs >= g.BK ? 1 : (int)(g.BK / L.bs);
+    const int max_bn = 256 / g.nbs < 256 ? 256 / g.nbs : 256;  // entries per stage <= 256
+    for (int bn = 16; bn <= max_bn; bn += 16) {
         if (forced && bn != forced) continue;
         const int64_t nt = (L.N + bn - 1) / bn;
         const int64_t ntiles = nt * g.m_tiles;
         const int64_t waves = (ntiles + sms - 1) / sms;
-        const double cost = (double)waves * bn + 1e-3 * (double)(nt * bn - L.N);
+        // per-SM work of a wave ~ BN columns plus a fixed per-tile cost (pipeline fill,
+        // epilogue, the X stream) worth about 32 columns
+        const double cost = (double)waves * (bn + 32) + 1e-3 * (double)(nt * bn - L.N);
         if (cost < best) {
             best = cost;
             g.BN = bn;
         }
     }
-    if (g.BN == 0) g.BN = 128;
+    if (g.BN == 0) g.BN = max_bn;
     g.n_tiles = (int)((L.N + g.BN - 1) / g.BN);
     g.tmem_cols = 32;
     while (g.tmem_cols < g.BN) g.tmem_cols <<= 1;
@@ -524,8 +680,21 @@ TcGeom make_geom(const MatmulParams& p) {
     g.x_stage = (size_t)kBM * g.BK * 2;
     g.wd_stage = (size_t)g.BN * g.BK * 2;
     g.wp_stage = (size_t)(g.BN / 16) * tiles * kTileBytes;
-    const size_t fixed = 1024 + (3 * kMaxR + 1) * 8 + 16;
-    const size_t per_stage = g.x_stage + g.wd_stage + g.wp_stage;
+    g.ent_stage = round16((size_t)g.BN * g.nbs * 4);
+    // raw scales by TMA: rows of scales / zero points must be 16-byte strided and aligned
+    const int sbytes = p.scale_dtype == kF32 ? 4 : 2;
+    g.sb = 16 / sbytes;
+    if (g.sb < 128 / L.bits) g.sb = 128 / L.bits;  // zero-point box at least 16 bytes
+    if (g.sb < g.nbs) g.sb = g.nbs;
+    g.scale_tma = ((L.KB * sbytes) % 16 == 0) && ((reinterpret_cast<uintptr_t>(p.scales) & 15) == 0) &&
+                  (p.zp == nullptr || ((L.zp_row % 16 == 0) && ((reinterpret_cast<uintptr_t>(p.zp) & 15) == 0)));
+    // boxes no wider than the tensors they read
+    if (g.sb > L.KB || (p.zp != nullptr && (int64_t)g.sb * L.bits / 8 > L.zp_row)) g.scale_tma = 0;
+    if (std::getenv("MNB_TC_NO_SCALE_TMA")) g.scale_tma = 0;
+    g.sraw_bytes = g.scale_tma ? round16((size_t)g.BN * g.sb * sbytes) : 0;
+    g.zraw_bytes = (g.scale_tma && p.zp) ? round16((size_t)g.BN * g.sb * L.bits / 8) : 0;
+    const size_t fixed = 1024 + 2 * (g.sraw_bytes + g.zraw_bytes) + (4 * kMaxR + 3) * 8 + 16;
+    const size_t per_stage = g.x_stage + g.wd_stage + g.wp_stage + g.ent_stage;
     const size_t limit = device_info().smem_optin ? device_info().smem_optin : 232448;
     g.R = kMaxR;
     const char* renv = std::getenv("MNB_TC_STAGES");
@@ -535,30 +704,32 @@ TcGeom make_geom(const MatmulParams& p) {
     return g;
 }
 
+struct Maps {
+    CUtensorMap x, w, s, z;
+};
+
 template <int BITS, bool BF16X, int NBU>
-cudaError_t launch_nbu(const MatmulParams& p, const TcGeom& geo, const CUtensorMap& map, const CUtensorMap& wmap,
-                       cudaStream_t s) {
+cudaError_t launch_nbu(const MatmulParams& p, const TcGeom& geo, const Maps& m, cudaStream_t s) {
     auto kern = gemm_tc_kernel<BITS, BF16X, NBU>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.total_bytes);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)(geo.n_tiles * geo.m_tiles), kThreads, geo.total_bytes, s>>>(p, geo, map, wmap);
+    kern<<<(unsigned)(geo.n_tiles * geo.m_tiles), kThreads, geo.total_bytes, s>>>(p, geo, m.x, m.w, m.s, m.z);
     return cudaGetLastError();
 }
 
 // NBU = quantisation blocks per packed tile (1 when a block covers the tile).
 template <int BITS, bool BF16X>
-cudaError_t launch(const MatmulParams& p, const TcGeom& geo, const CUtensorMap& map, const CUtensorMap& wmap,
-                   cudaStream_t s) {
+cudaError_t launch(const MatmulParams& p, const TcGeom& geo, const Maps& m, cudaStream_t s) {
     constexpr int KT = 256 / BITS;
     const int nbu = p.L.bs >= KT ? 1 : (int)(KT / p.L.bs);
     switch (nbu) {
-        case 1: return launch_nbu<BITS, BF16X, 1>(p, geo, map, wmap, s);
-        case 2: return launch_nbu<BITS, BF16X, 2>(p, geo, map, wmap, s);
+        case 1: return launch_nbu<BITS, BF16X, 1>(p, geo, m, s);
+        case 2: return launch_nbu<BITS, BF16X, 2>(p, geo, m, s);
         case 4:
-            if constexpr (BITS != 8) return launch_nbu<BITS, BF16X, 4>(p, geo, map, wmap, s);
+            if constexpr (BITS != 8) return launch_nbu<BITS, BF16X, 4>(p, geo, m, s);
             break;
         case 8:
-            if constexpr (BITS == 2) return launch_nbu<BITS, BF16X, 8>(p, geo, map, wmap, s);
+            if constexpr (BITS == 2) return launch_nbu<BITS, BF16X, 8>(p, geo, m, s);
             break;
         default: break;
     }
@@ -584,31 +755,53 @@ cudaError_t launch_gemm_tc(const MatmulParams& p, cudaStream_t s) {
     const TcGeom geo = make_geom(p);
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    CUtensorMap map;
+    Maps m;
+    std::memset(&m, 0, sizeof(m));
+    const cuuint32_t estr[3] = {1, 1, 1};
+    // X: [M][K] bf16/f16, 128-row x 64-deep boxes, 128-byte swizzle, zero fill past M and K
     const cuuint64_t dims[2] = {(cuuint64_t)p.L.K, (cuuint64_t)p.M};
     const cuuint64_t strides[1] = {(cuuint64_t)p.L.K * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)kBM};
-    const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType dt =
         p.act_dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUresult r = enc(&map, dt, 2, const_cast<void*>(p.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    CUresult r = enc(&m.x, dt, 2, const_cast<void*>(p.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     // Packed codes as a 3-D tensor of 16-bit elements: [row tile][k tile][256 x u16].
-    CUtensorMap wmap;
     const cuuint64_t wdims[3] = {256, (cuuint64_t)p.L.KTILES, (cuuint64_t)p.L.NT};
     const cuuint64_t wstrides[2] = {(cuuint64_t)kTileBytes, (cuuint64_t)p.L.KTILES * kTileBytes};
     const cuuint32_t wbox[3] = {256, (cuuint32_t)(geo.BK / p.L.KT), (cuuint32_t)(geo.BN / 16)};
-    const cuuint32_t westr[3] = {1, 1, 1};
-    r = enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint8_t*>(p.packed), wdims, wstrides, wbox, westr,
+    r = enc(&m.w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint8_t*>(p.packed), wdims, wstrides, wbox, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (geo.scale_tma) {
+        // scales [N][KB] and zero points [N][zp_row] in the ORT layout, SB blocks x BN rows per box
+        const int sbytes = p.scale_dtype == kF32 ? 4 : 2;
+        const CUtensorMapDataType sdt = p.scale_dtype == kF32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                        : p.scale_dtype == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const cuuint64_t sdims[2] = {(cuuint64_t)p.L.KB, (cuuint64_t)p.L.N};
+        const cuuint64_t sstr[1] = {(cuuint64_t)p.L.KB * sbytes};
+        const cuuint32_t sbox[2] = {(cuuint32_t)geo.sb, (cuuint32_t)geo.BN};
+        r = enc(&m.s, sdt, 2, const_cast<void*>(p.scales), sdims, sstr, sbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        if (p.zp) {
+            const cuuint64_t zdims[2] = {(cuuint64_t)p.L.zp_row, (cuuint64_t)p.L.N};
+            const cuuint64_t zstr[1] = {(cuuint64_t)p.L.zp_row};
+            const cuuint32_t zbox[2] = {(cuuint32_t)(geo.sb * p.L.bits / 8), (cuuint32_t)geo.BN};
+            r = enc(&m.z, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.zp), zdims, zstr, zbox, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        }
+    }
     const bool bf = p.act_dtype == kBF16;
     switch (p.L.bits) {
-        case 2: return bf ? launch<2, true>(p, geo, map, wmap, s) : launch<2, false>(p, geo, map, wmap, s);
-        case 4: return bf ? launch<4, true>(p, geo, map, wmap, s) : launch<4, false>(p, geo, map, wmap, s);
-        case 8: return bf ? launch<8, true>(p, geo, map, wmap, s) : launch<8, false>(p, geo, map, wmap, s);
+        case 2: return bf ? launch<2, true>(p, geo, m, s) : launch<2, false>(p, geo, m, s);
+        case 4: return bf ? launch<4, true>(p, geo, m, s) : launch<4, false>(p, geo, m, s);
+        case 8: return bf ? launch<8, true>(p, geo, m, s) : launch<8, false>(p, geo, m, s);
         default: return cudaErrorInvalidValue;
     }
 }
