@@ -1,11 +1,50 @@
 // Host side of the small-batch tensor-core GEMV (kernel in gemv_mma.cuh).
-#include "gemv_mma.cuh"
+#include <cstdlib>
+
+#include "gemv_pers.cuh"
 
 namespace mnb {
 
 cudaError_t launch_gemv_mma_b2(const MatmulParams& p, const gmma::Geom& geo, cudaStream_t s);
 cudaError_t launch_gemv_mma_b4(const MatmulParams& p, const gmma::Geom& geo, cudaStream_t s);
 cudaError_t launch_gemv_mma_b8(const MatmulParams& p, const gmma::Geom& geo, cudaStream_t s);
+cudaError_t launch_gemv_pers_b2(const MatmulParams& p, const gpers::PGeom& geo, int grid, cudaStream_t s);
+cudaError_t launch_gemv_pers_b4(const MatmulParams& p, const gpers::PGeom& geo, int grid, cudaStream_t s);
+cudaError_t launch_gemv_pers_b8(const MatmulParams& p, const gpers::PGeom& geo, int grid, cudaStream_t s);
+
+// The persistent schedule (gemv_pers.cuh) takes the shapes it was built for:
+// a row tile's K in one pass of 16 warps, enough row tiles to fill every SM at
+// least twice, block boundaries on warp slices.  Measured on GB300: for
+// M = 1 the per-tile grid is faster (10.5 vs 12.3 us on the int4 4096 x 11008
+// decode), for M = 8 the persistent one (16.0 vs 21.6 us on the int2
+// 4096 x 14336 batch), so it is the default for M >= 2.  MNB_GEMV_PERS=0 / 1
+// forces either schedule.
+static bool pers_ok(const MatmulParams& p, gpers::PGeom* out, int* grid) {
+    const char* env = std::getenv("MNB_GEMV_PERS");
+    if (env && env[0] == '0') return false;
+    if (!(env && env[0] == '1') && p.M < 2) return false;
+    const Layout& L = p.L;
+    if (L.KTILES > gpers::kWarps * gpers::kMaxTPW) return false;
+    const int spb = L.bs / 16;
+    if (spb != 1 && spb != 2 && spb != 4 && spb != 8) return false;
+    gpers::PGeom g = gpers::make_pgeom(L, p.M, p.M <= 8 ? 8 : 16);
+    // raw scales / zero points by bulk copy: 16-byte rows and bases
+    const int sbytes = p.scale_dtype == kF32 ? 4 : 2;
+    if ((L.KB * sbytes) % 16 != 0 || (reinterpret_cast<uintptr_t>(p.scales) & 15) != 0) return false;
+    if (p.zp && (L.zp_row % 16 != 0 || (reinterpret_cast<uintptr_t>(p.zp) & 15) != 0)) return false;
+    g.raw_row = (size_t)L.KB * sbytes;
+    g.raw_zoff = 16 * g.raw_row;
+    g.raw_slot = round16(g.raw_zoff + (p.zp ? 16 * (size_t)L.zp_row : 0));
+    g.total_bytes += gpers::kDepth * g.raw_slot;
+    if ((g.tpw * (16 / L.bits)) % spb != 0) return false;
+    if (16 * g.runs > 2 * gpers::kThreads) return false;
+    const int sms = device_info().sm_count > 0 ? device_info().sm_count : 148;
+    if (L.NT < 2 * (int64_t)sms) return false;
+    if (g.total_bytes > device_info().smem_optin) return false;
+    *out = g;
+    *grid = sms;
+    return true;
+}
 
 static gmma::Geom geom_for(const MatmulParams& p) {
     return gmma::make_geom(p.L, p.M, p.M <= 8 ? 8 : 16);
@@ -21,6 +60,16 @@ bool gemv_mma_supported(const MatmulParams& p) {
 }
 
 cudaError_t launch_gemv_mma(const MatmulParams& p, cudaStream_t s) {
+    gpers::PGeom pg;
+    int grid = 0;
+    if (pers_ok(p, &pg, &grid)) {
+        switch (p.L.bits) {
+            case 2: return launch_gemv_pers_b2(p, pg, grid, s);
+            case 4: return launch_gemv_pers_b4(p, pg, grid, s);
+            case 8: return launch_gemv_pers_b8(p, pg, grid, s);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     const gmma::Geom geo = geom_for(p);
     if (geo.total_bytes > device_info().smem_optin) return cudaErrorNotSupported;
     switch (p.L.bits) {

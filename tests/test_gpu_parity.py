@@ -120,6 +120,31 @@ def test_matmul_gemv_mma(G, M, bits, bs, dt, asym, N, K):
     G.assert_within(y, ref, mag, w.out_dtype, f"gemv_mma {w.name}")
 
 
+# Enough row tiles (N >= 2 x 16 x SMs) and a short enough K for the persistent
+# decode schedule; ragged N and K, every code width, 1 <= M <= 16.
+PERS_CASES = [
+    (1, 4, 32, (BF16, F16, BF16), True, 4801, 4096),
+    (1, 4, 16, (F16, F32, F16), False, 4800, 1000),
+    (8, 2, 64, (BF16, F16, BF16), True, 4900, 4096),
+    (3, 8, 32, (BF16, BF16, F32), True, 4850, 2048),
+    (16, 4, 128, (F16, F16, BF16), True, 4864, 1024),
+    (5, 2, 16, (BF16, F32, BF16), False, 4800, 640),
+    (1, 8, 128, (F16, F32, F16), True, 4800, 2048),
+    (12, 4, 64, (BF16, F16, F32), True, 4817, 3000),
+]
+
+
+@pytest.mark.parametrize("M,bits,bs,dt,asym,N,K", PERS_CASES)
+@pytest.mark.parametrize("pers", ["1", "0"])  # persistent schedule opt-in, per-tile default
+def test_matmul_gemv_persistent(G, monkeypatch, M, bits, bs, dt, asym, N, K, pers):
+    monkeypatch.setenv("MNB_GEMV_PERS", pers)
+    w = _w(M, N, K, bits, bs, dt, asym, 900 + M * 13 + bits * 7 + bs + N)
+    P = G.Problem(w)
+    y = P.y64(P.run("gemv_mma"))
+    ref, mag = P.oracle_full()
+    G.assert_within(y, ref, mag, w.out_dtype, f"gemv_mma pers={pers} {w.name}")
+
+
 TC_CASES = []
 for i, (bits, bs) in enumerate(BITS_BS):
     for M in (17, 128, 200):
