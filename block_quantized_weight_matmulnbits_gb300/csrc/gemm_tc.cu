@@ -1,11 +1,14 @@
 // Host side of the tcgen05 prefill GEMM (kernel in gemm_tc.cuh): tile
 // geometry, tensor maps and dispatch to the per-code-width instantiations.
-#include "gemm_tc.cuh"
+#include "gemm_ta.cuh"
 
 namespace mnb {
 cudaError_t launch_gemm_tc_b2(const MatmulParams& p, const gtc::TcGeom& geo, const gtc::Maps& m, cudaStream_t s);
 cudaError_t launch_gemm_tc_b4(const MatmulParams& p, const gtc::TcGeom& geo, const gtc::Maps& m, cudaStream_t s);
 cudaError_t launch_gemm_tc_b8(const MatmulParams& p, const gtc::TcGeom& geo, const gtc::Maps& m, cudaStream_t s);
+cudaError_t launch_gemm_ta_b2(const MatmulParams& p, const gtc::TcGeom& geo, const gtc::Maps& m, cudaStream_t s);
+cudaError_t launch_gemm_ta_b4(const MatmulParams& p, const gtc::TcGeom& geo, const gtc::Maps& m, cudaStream_t s);
+cudaError_t launch_gemm_ta_b8(const MatmulParams& p, const gtc::TcGeom& geo, const gtc::Maps& m, cudaStream_t s);
 
 namespace {
 using gtc::TcGeom;
@@ -93,6 +96,62 @@ TcGeom make_geom(const MatmulParams& p) {
     return g;
 }
 
+// Geometry of the W-in-TMEM kernel (gemm_ta.cuh): 128 W rows x BT tokens per
+// tile; needs the TMA raw-scale path, a ring of at least 5 stages (the
+// dequantising warps take every 4th stage) and the A ring in tensor memory.
+// Returns false when the shape is not for it.
+bool make_geom_ta(const MatmulParams& p, TcGeom* out) {
+    const char* env = std::getenv("MNB_TC_TA");
+    if (env && env[0] == '0') return false;
+    const Layout& L = p.L;
+    TcGeom g = make_geom(p);
+    if (!g.scale_tma) return false;
+    g.ta = 1;
+    // 128-deep stages; the raw-scale buffer must still span >= kMaxR stages
+    g.BK = 128;
+    g.k_stages = (int)((L.KTILES * L.KT + g.BK - 1) / g.BK);
+    while ((int64_t)g.sb * L.bs < (int64_t)kMaxR * g.BK) g.sb <<= 1;
+    g.sb_stages = (int)((int64_t)g.sb * L.bs / g.BK);
+    if (g.sb > L.KB || (p.zp != nullptr && (int64_t)g.sb * L.bits / 8 > L.zp_row)) return false;
+    const int sms = device_info().sm_count > 0 ? device_info().sm_count : 148;
+    const int64_t nt = (L.N + gtc::kTaRows - 1) / gtc::kTaRows;
+    double best = 1e30;
+    int bt_best = 0;
+    for (int bt = 16; bt <= 256; bt += 16) {
+        const int64_t mt = (p.M + bt - 1) / bt;
+        const int64_t waves = (nt * mt + sms - 1) / sms;
+        const double cost = (double)waves * (bt + 32) + 1e-3 * (double)(mt * bt - p.M);
+        if (cost < best) {
+            best = cost;
+            bt_best = bt;
+        }
+    }
+    g.BN = bt_best;  // tokens per tile
+    g.n_tiles = (int)nt;
+    g.m_tiles = (int)((p.M + g.BN - 1) / g.BN);
+    const int tiles = (int)(g.BK / L.KT);
+    const int a_cols = (g.BK / 16) * 8;
+    g.a_col0 = (g.BN + 31) & ~31;
+    g.x_stage = (size_t)g.BN * g.BK * 2;
+    g.wp_stage = (size_t)(gtc::kTaRows / 16) * tiles * kTileBytes;
+    g.wd_stage = 0;
+    g.ent_stage = 0;
+    const int sbytes = p.scale_dtype == kF32 ? 4 : 2;
+    g.sraw_bytes = round16((size_t)gtc::kTaRows * g.sb * sbytes);
+    g.zraw_bytes = p.zp ? round16((size_t)gtc::kTaRows * g.sb * L.bits / 8) : 0;
+    const size_t fixed = 1024 + 2 * (g.sraw_bytes + g.zraw_bytes) + (4 * kMaxR + 3) * 8 + 16;
+    const size_t per_stage = g.x_stage + g.wp_stage;
+    const size_t limit = device_info().smem_optin ? device_info().smem_optin : 232448;
+    g.R = kMaxR;
+    while (g.R > 2 && (fixed + g.R * per_stage > limit || g.a_col0 + g.R * a_cols > 512)) --g.R;
+    if (g.R < 2 || g.sb_stages < g.R) return false;
+    g.tmem_cols = 32;
+    while (g.tmem_cols < g.a_col0 + g.R * a_cols) g.tmem_cols <<= 1;
+    g.total_bytes = fixed + g.R * per_stage;
+    *out = g;
+    return true;
+}
+
 }  // namespace
 
 bool gemm_tc_supported(const MatmulParams& p) {
@@ -109,7 +168,9 @@ bool gemm_tc_supported(const MatmulParams& p) {
 }
 
 cudaError_t launch_gemm_tc(const MatmulParams& p, cudaStream_t s) {
-    const TcGeom geo = make_geom(p);
+    TcGeom geo;
+    if (!make_geom_ta(p, &geo)) geo = make_geom(p);
+    const int rows = geo.ta ? gtc::kTaRows : geo.BN;  // W rows per tile
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     Maps m;
@@ -118,7 +179,7 @@ cudaError_t launch_gemm_tc(const MatmulParams& p, cudaStream_t s) {
     // X: [M][K] bf16/f16, 128-row x 64-deep boxes, 128-byte swizzle, zero fill past M and K
     const cuuint64_t dims[2] = {(cuuint64_t)p.L.K, (cuuint64_t)p.M};
     const cuuint64_t strides[1] = {(cuuint64_t)p.L.K * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)kBM};
+    const cuuint32_t box[2] = {64, (cuuint32_t)(geo.ta ? geo.BN : kBM)};
     const CUtensorMapDataType dt =
         p.act_dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUresult r = enc(&m.x, dt, 2, const_cast<void*>(p.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -127,11 +188,26 @@ cudaError_t launch_gemm_tc(const MatmulParams& p, cudaStream_t s) {
     // Packed codes as a 3-D tensor of 16-bit elements: [row tile][k tile][256 x u16].
     const cuuint64_t wdims[3] = {256, (cuuint64_t)p.L.KTILES, (cuuint64_t)p.L.NT};
     const cuuint64_t wstrides[2] = {(cuuint64_t)kTileBytes, (cuuint64_t)p.L.KTILES * kTileBytes};
-    const cuuint32_t wbox[3] = {256, (cuuint32_t)(geo.BK / p.L.KT), (cuuint32_t)(geo.BN / 16)};
+    const cuuint32_t wbox[3] = {256, (cuuint32_t)(geo.BK / p.L.KT), (cuuint32_t)(rows / 16)};
     r = enc(&m.w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint8_t*>(p.packed), wdims, wstrides, wbox, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (geo.ta) {
+        // the W-in-TMEM kernel reads codes row by row: load each 512-byte tile as
+        // [t][g][16 B] (dims: 8 x u16, g (stride 64), t (stride 16), k tile, row tile)
+        const cuuint64_t tdims[5] = {8, 8, 4, (cuuint64_t)p.L.KTILES, (cuuint64_t)p.L.NT};
+        const cuuint64_t tstrides[4] = {64, 16, (cuuint64_t)kTileBytes, (cuuint64_t)p.L.KTILES * kTileBytes};
+        const cuuint32_t tbox[5] = {8, 8, 4, (cuuint32_t)(geo.BK / p.L.KT), (cuuint32_t)(rows / 16)};
+        const cuuint32_t testr[5] = {1, 1, 1, 1, 1};
+        r = enc(&m.w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<uint8_t*>(p.packed), tdims, tstrides, tbox, testr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            if (std::getenv("MNB_LOG")) std::fprintf(stderr, "[mnb] 5-D code map rejected (%d)\n", (int)r);
+            return cudaErrorInvalidValue;
+        }
+    }
     if (geo.scale_tma) {
         // scales [N][KB] and zero points [N][zp_row] in the ORT layout, SB blocks x BN rows per box
         const int sbytes = p.scale_dtype == kF32 ? 4 : 2;
@@ -140,18 +216,26 @@ cudaError_t launch_gemm_tc(const MatmulParams& p, cudaStream_t s) {
                                                                 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         const cuuint64_t sdims[2] = {(cuuint64_t)p.L.KB, (cuuint64_t)p.L.N};
         const cuuint64_t sstr[1] = {(cuuint64_t)p.L.KB * sbytes};
-        const cuuint32_t sbox[2] = {(cuuint32_t)geo.sb, (cuuint32_t)geo.BN};
+        const cuuint32_t sbox[2] = {(cuuint32_t)geo.sb, (cuuint32_t)rows};
         r = enc(&m.s, sdt, 2, const_cast<void*>(p.scales), sdims, sstr, sbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
         if (p.zp) {
             const cuuint64_t zdims[2] = {(cuuint64_t)p.L.zp_row, (cuuint64_t)p.L.N};
             const cuuint64_t zstr[1] = {(cuuint64_t)p.L.zp_row};
-            const cuuint32_t zbox[2] = {(cuuint32_t)(geo.sb * p.L.bits / 8), (cuuint32_t)geo.BN};
+            const cuuint32_t zbox[2] = {(cuuint32_t)(geo.sb * p.L.bits / 8), (cuuint32_t)rows};
             r = enc(&m.z, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.zp), zdims, zstr, zbox, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
             if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        }
+    }
+    if (geo.ta) {
+        switch (p.L.bits) {
+            case 2: return launch_gemm_ta_b2(p, geo, m, s);
+            case 4: return launch_gemm_ta_b4(p, geo, m, s);
+            case 8: return launch_gemm_ta_b8(p, geo, m, s);
+            default: return cudaErrorInvalidValue;
         }
     }
     switch (p.L.bits) {

@@ -69,6 +69,8 @@ struct TcGeom {
     int scale_tma;   // raw scales / zero points arrive by TMA, SB blocks at a time
     int sb;          // blocks per raw scale buffer (TMA path)
     int sb_stages;   // stages per raw scale buffer (sb * bs / BK, >= R)
+    int ta;          // W in tensor memory (gemm_ta.cuh): BN = tokens per tile, 128 W rows per tile
+    int a_col0;      // (ta) first TMEM column of the A ring
     size_t x_stage, wp_stage, wd_stage, ent_stage, sraw_bytes, zraw_bytes, total_bytes;
 };
 

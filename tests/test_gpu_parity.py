@@ -156,6 +156,33 @@ TC_CASES += [(64, 4, 32, (BF16, F16, BF16), False, 4096, 512), (1, 4, 32, (BF16,
              (256, 4, 16, (BF16, BF16, F32), True, 520, 136), (300, 8, 16, (F16, F16, BF16), False, 48, 72)]
 
 
+# Shapes for the W-in-tensor-memory GEMM (scales / zero points 16-byte aligned
+# per row, enough blocks for one raw-scale box): every code width, ragged M
+# and N, both activation dtypes, with and without zero points.
+TA_CASES = [
+    (128, 4, 32, (BF16, F16, BF16), True, 256, 1024),
+    (200, 4, 32, (F16, F32, F16), False, 300, 2048),
+    (64, 2, 64, (BF16, F16, BF16), True, 130, 4096),
+    (40, 8, 128, (F16, F32, F16), True, 200, 2048),
+    (33, 8, 128, (BF16, F16, BF16), True, 77, 2048),
+    (256, 4, 16, (BF16, BF16, F32), True, 520, 1024),
+    (300, 4, 64, (F16, F16, BF16), True, 64, 2048),
+    (17, 4, 32, (BF16, F16, BF16), True, 1000, 1024),
+    (512, 4, 128, (BF16, F16, BF16), False, 384, 4096),
+]
+
+
+@pytest.mark.parametrize("M,bits,bs,dt,asym,N,K", TA_CASES)
+@pytest.mark.parametrize("ta", ["1", "0"])
+def test_matmul_gemm_tmem_weights(G, monkeypatch, M, bits, bs, dt, asym, N, K, ta):
+    monkeypatch.setenv("MNB_TC_TA", ta)
+    w = _w(M, N, K, bits, bs, dt, asym, 1100 + M * 3 + bits * 7 + bs + N)
+    P = G.Problem(w)
+    y = P.y64(P.run("gemm_tc"))
+    ref, mag = P.oracle_full()
+    G.assert_within(y, ref, mag, w.out_dtype, f"gemm_tc ta={ta} {w.name}")
+
+
 @pytest.mark.parametrize("M,bits,bs,dt,asym,N,K", TC_CASES)
 def test_matmul_gemm_tc(G, M, bits, bs, dt, asym, N, K):
     w = _w(M, N, K, bits, bs, dt, asym, 800 + M * 3 + bits * 7 + bs + N)
