@@ -188,8 +188,11 @@ inline Geom make_geom(const Layout& L, int64_t M, int MT) {
 
 // SPB_LOG >= 0: blocks of 2^SPB_LOG k-steps start at every warp slice (static
 // block structure); -1: any block size, run-time checks.
+// Occupancy by code width (measured on GB300): 8-bit codes are the longest K
+// (K-split clusters) and gain from 4 CTAs per SM; 2- and 4-bit codes are
+// faster with 3 CTAs per SM and spill-free registers.
 template <int BITS, bool BF16X, int MT, int SPB_LOG>
-__global__ void __launch_bounds__(kThreads, 3) gemv_mma_kernel(MatmulParams p, Geom geo, int pdl) {
+__global__ void __launch_bounds__(kThreads, BITS == 8 ? 4 : 3) gemv_mma_kernel(MatmulParams p, Geom geo, int pdl) {
     using U = Unpack<BITS, BF16X>;
     constexpr int NTILE = MT / 8;  // MMA n8 tiles (activation rows 0-7, 8-15)
     constexpr int SPT = U::kStepsPerTile;
