@@ -93,7 +93,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_ta_kernel(MatmulParams p, Tc
     constexpr int KT = 256 / BITS;
     constexpr int BKC = 128;                         // depths per stage
     constexpr int TILES = BKC / KT;                  // packed tiles per 16-row tile per stage
-    constexpr int SPT = 16 / BITS;                   // k-steps per packed tile
     constexpr int SSTAGE = BKC / 16;                 // 16-deep k-steps per stage
     constexpr uint32_t kMag = BF16X ? 0x43004300u : 0x64006400u;
     constexpr int NB = (SSTAGE >> SPB_LOG) > 0 ? (SSTAGE >> SPB_LOG) : 1;  // blocks per stage
@@ -299,25 +298,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_ta_kernel(MatmulParams p, Tc
             const uint8_t* cb = wp + s * geo.wp_stage + rt * TILES * kTileBytes + g * 16;
             uint32_t v[16];
 #pragma unroll
-            for (int ss = 0; ss < 2; ++ss) {
-                const int st = 2 * jw + ss;           // k-step inside the stage
-                const int tl = st / SPT, si = st % SPT;  // packed tile, k-step inside it
-                const int j = (ss >> SPB_LOG) < NBW ? (ss >> SPB_LOG) : 0;
+            for (int t = 0; t < 4; ++t) {
+                // this thread's code words of k-steps 2 jw, 2 jw + 1 in chunk t, in one load:
+                //   4-bit: packed tile jw / 2, words 2 (jw % 2) + ss
+                //   2-bit: packed tile 0, word jw (both k-steps)
+                //   8-bit: packed tile jw, words 2 ss + half
+                uint32_t wd[4];
+                if constexpr (BITS == 4) {
+                    const uint2 w2 = *reinterpret_cast<const uint2*>(cb + (jw >> 1) * kTileBytes + t * 128 + 8 * (jw & 1));
+                    wd[0] = w2.x;
+                    wd[1] = w2.y;
+                } else if constexpr (BITS == 2) {
+                    wd[0] = *reinterpret_cast<const uint32_t*>(cb + t * 128 + 4 * jw);
+                } else {
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(cb + jw * kTileBytes + t * 128);
+                    wd[0] = w4.x;
+                    wd[1] = w4.y;
+                    wd[2] = w4.z;
+                    wd[3] = w4.w;
+                }
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const uint32_t* cw = reinterpret_cast<const uint32_t*>(cb + tl * kTileBytes + t * 128);
+                for (int ss = 0; ss < 2; ++ss) {
+                    const int j = (ss >> SPB_LOG) < NBW ? (ss >> SPB_LOG) : 0;
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         uint32_t pr;
                         if constexpr (BITS == 4) {
-                            const uint32_t x = lop3_and_or(cw[si] >> (4 * (hi + 2 * half)), 0x000F000Fu, kMag);
+                            const uint32_t x = lop3_and_or(wd[ss] >> (4 * (hi + 2 * half)), 0x000F000Fu, kMag);
                             pr = hmul2(hsub2(x, zc[j], BF16X), sp[j], BF16X);
                         } else if constexpr (BITS == 2) {
-                            const int f = 4 * (si & 1) + hi + 2 * half;
-                            const uint32_t x = lop3_and_or(cw[si >> 1] >> (2 * f), 0x00030003u, kMag);
+                            const int f = 4 * ss + hi + 2 * half;
+                            const uint32_t x = lop3_and_or(wd[0] >> (2 * f), 0x00030003u, kMag);
                             pr = hmul2(hsub2(x, zc[j], BF16X), sp[j], BF16X);
                         } else {
-                            const uint32_t word = cw[2 * si + half];
+                            const uint32_t word = wd[2 * ss + half];
                             const uint32_t b0 = 2 * hi, b1 = b0 + 1;
                             uint32_t qv;
                             if constexpr (BF16X) {
@@ -331,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_ta_kernel(MatmulParams p, Tc
                             }
                             pr = hmul2(qv, sp[j], BF16X);
                         }
-                        v[ss * 8 + 4 * half + t] = pr;  // depths 16 st + 2t + 8 half (+1)
+                        v[ss * 8 + 4 * half + t] = pr;  // depths 16 st + 2t + 8 half (+1), st = 2 jw + ss
                     }
                 }
             }
