@@ -218,6 +218,21 @@ MNB_API mnb_status mnb_matmul_a8_static(const void* x, const void* packed_b, con
 
 /* ---- diagnostics ------------------------------------------------------- */
 
+/* Environment overrides, read at each call (none changes a result beyond
+ * rounding order; none is needed for normal use):
+ *   MNB_LOG=1              print the kernel family chosen for each call
+ *   MNB_GEMV_MAX_M         largest M routed to the decode GEMV (default 16)
+ *   MNB_GEMV_PERS=0|1      force the per-tile or the persistent decode GEMV
+ *   MNB_MMA_TPW, MNB_I8_TPW  k-tiles per warp of the decode / int8 GEMV (1..8)
+ *   MNB_TC_TA=0            prefill GEMM dequantises into shared memory
+ *                          instead of tensor memory
+ *   MNB_TC_BN, MNB_TC_STAGES, MNB_TC_NO_SCALE_TMA=1
+ *                          tile width, ring depth and scale path of the
+ *                          shared-memory prefill GEMM
+ *   MNB_GEMV_STAGE_BUFS, MNB_GEMV_MAX_SLOTS  ring shape of the f32 GEMV
+ *   MNB_FAIL_LAUNCH=1      test hook: every launch reports MNB_ERR_CUDA
+ *                          without launching */
+
 /* The family mnb_matmul_ex would run with kernel == MNB_KERNEL_AUTO (host
  * only, no GPU needed).  Thresholds: MNB_GEMV_MAX_M (default 16) and the
  * environment override of the same name. */
