@@ -26,8 +26,10 @@ EXPORTS = [
     "mnb_packed_size", "mnb_pack_weights", "mnb_unpack_codes", "mnb_dequantize", "mnb_matmul",
     "mnb_matmul_ex", "mnb_workspace_size", "mnb_quantize_activations", "mnb_select_kernel",
     "mnb_get_device_error", "mnb_status_string", "mnb_kernel_name", "mnb_abi_version", "mnb_matmul_a8_static",
+    "mnb_matmul_host_io",
 ]
 MNB_A8_STATIC_SCRATCH_BYTES = 1 << 20
+MNB_HOST_IO_X_BYTES = 8 << 20
 
 
 class MnbError(RuntimeError):
@@ -80,6 +82,7 @@ def load(build: bool = True):
             "mnb_kernel_name": (ctypes.c_char_p, [ci]),
             "mnb_abi_version": (ci, []),
             "mnb_matmul_a8_static": (ci, [vp, vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, ci, ci, vp]),
+            "mnb_matmul_host_io": (ci, [ctypes.POINTER(MatmulArgs)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -147,9 +150,8 @@ def mnb_matmul(x, packed_b, scales, zero_points, y, M, N, K, bits, block_size, a
                              block_size, act_dtype, out_dtype, scale_dtype, _stream(stream)), "mnb_matmul")
 
 
-def mnb_matmul_ex(x, packed_b, scales, zero_points, y, M, N, K, bits, block_size, act_dtype, out_dtype,
-                  scale_dtype, g_idx=None, bias=None, bias_dtype=MNB_F32, accuracy_level=0, workspace=None,
-                  kernel="auto", stream=None, flags=0):
+def _matmul_args(x, packed_b, scales, zero_points, y, M, N, K, bits, block_size, act_dtype, out_dtype,
+                 scale_dtype, g_idx, bias, bias_dtype, accuracy_level, workspace, kernel, stream, flags):
     a = MatmulArgs()
     a.x, a.packed_b, a.scales, a.zero_points = _ptr(x), _ptr(packed_b), _ptr(scales), _ptr(zero_points)
     a.g_idx, a.bias, a.y = _ptr(g_idx), _ptr(bias), _ptr(y)
@@ -161,7 +163,24 @@ def mnb_matmul_ex(x, packed_b, scales, zero_points, y, M, N, K, bits, block_size
     a.kernel = KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
     a.stream = _stream(stream)
     a.flags = flags
+    return a
+
+
+def mnb_matmul_ex(x, packed_b, scales, zero_points, y, M, N, K, bits, block_size, act_dtype, out_dtype,
+                  scale_dtype, g_idx=None, bias=None, bias_dtype=MNB_F32, accuracy_level=0, workspace=None,
+                  kernel="auto", stream=None, flags=0):
+    a = _matmul_args(x, packed_b, scales, zero_points, y, M, N, K, bits, block_size, act_dtype, out_dtype,
+                     scale_dtype, g_idx, bias, bias_dtype, accuracy_level, workspace, kernel, stream, flags)
     _check(load().mnb_matmul_ex(ctypes.byref(a)), f"mnb_matmul_ex[{kernel}]")
+
+
+def mnb_matmul_host_io(x, packed_b, scales, zero_points, y, M, N, K, bits, block_size, act_dtype, out_dtype,
+                       scale_dtype, g_idx=None, bias=None, bias_dtype=MNB_F32, accuracy_level=0, workspace=None,
+                       kernel="auto", stream=None, flags=0):
+    """As mnb_matmul_ex, with x and y page-locked host tensors (e.g. .pin_memory())."""
+    a = _matmul_args(x, packed_b, scales, zero_points, y, M, N, K, bits, block_size, act_dtype, out_dtype,
+                     scale_dtype, g_idx, bias, bias_dtype, accuracy_level, workspace, kernel, stream, flags)
+    _check(load().mnb_matmul_host_io(ctypes.byref(a)), f"mnb_matmul_host_io[{kernel}]")
 
 
 def mnb_matmul_a8_static(x, packed_b, scales, zero_points, y, M, N, K, bits, block_size, act_dtype, out_dtype,

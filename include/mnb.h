@@ -216,6 +216,33 @@ MNB_API mnb_status mnb_matmul_a8_static(const void* x, const void* packed_b, con
                                         int bits, int block_size, mnb_dtype act_dtype, mnb_dtype out_dtype,
                                         mnb_dtype scale_dtype, mnb_stream_t stream);
 
+/* mnb_matmul_ex with X and Y in page-locked HOST memory: the call moves the
+ * activations in and the result out itself, with no copy-engine transfers.
+ * No counterpart on the pages; an addition to the boundary.
+ *   args->x  host [M, K] of act_dtype, 16-byte aligned, page-locked
+ *            (cudaHostAlloc / cudaMallocHost, or cudaHostRegister'ed).
+ *   args->y  host [M, N] of out_dtype, 16-byte aligned, page-locked.
+ *   Everything else is as mnb_matmul_ex (device weights, scales, workspace).
+ * Steps, all on args->stream: one small kernel reads X over the host link
+ * into a file-scope device array of MNB_HOST_IO_X_BYTES (8 MiB) per device;
+ * the matmul runs as its programmatic dependent (its weight stream starts
+ * while X is in flight) and stores Y straight into the host buffer.  Y is
+ * complete when the stream's work is (synchronise before reading it).
+ *   Pointer check: outside stream capture every call checks with
+ *   cudaPointerGetAttributes that x and y are page-locked host memory (or
+ *   device memory) and uses the device address that reports; pageable
+ *   memory is MNB_ERR_INVALID_ARG and nothing is launched.  During capture
+ *   the addresses are used as given: under unified addressing the device
+ *   address of page-locked memory is its host address.
+ *   Limits: M*K*sizeof(act) > MNB_HOST_IO_X_BYTES returns MNB_ERR_NO_MEM
+ *   without launching.  The first call on a device looks the array up
+ *   (cudaGetSymbolAddress); make it outside stream capture.  Calls that
+ *   overlap on one device (different streams, graphs in flight together)
+ *   share the array and race; calls ordered on one stream are safe.
+ * Returns the statuses of mnb_matmul_ex. */
+#define MNB_HOST_IO_X_BYTES (8u << 20)
+MNB_API mnb_status mnb_matmul_host_io(const mnb_matmul_args* args);
+
 /* ---- diagnostics ------------------------------------------------------- */
 
 /* Environment overrides, read at each call (none changes a result beyond
