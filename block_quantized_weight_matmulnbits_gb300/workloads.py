@@ -160,3 +160,96 @@ def generate(w: Workload, rng: Optional[np.random.Generator] = None) -> dict:
         "scales": to_storage(s64, w.scale_dtype),
         "zp": zp,
     }
+
+
+@dataclasses.dataclass(frozen=True)
+class MoeWorkload:
+    """A grouped (mixture-of-experts) instance: T tokens, S expert slots per
+    token, E experts that share one [N, K] weight shape.
+
+    ids: "distinct" draws S different experts per token (top-S routing);
+    "repeat" draws every slot independently (an expert may repeat within a
+    token).  x_per_slot: X is [T, S, K] (one row per slot) instead of [T, K].
+    """
+    name: str
+    T: int
+    S: int
+    E: int
+    N: int
+    K: int
+    bits: int
+    bs: int
+    act_dtype: int
+    out_dtype: int
+    scale_dtype: int
+    x_per_slot: bool = False
+    ids: str = "distinct"
+    scale_lo: float = 0.001
+    scale_hi: float = 0.01
+    zp: Optional[tuple] = None
+    seed: int = SEED_BASE
+
+    def expert(self) -> Workload:
+        """One expert's dense shape (M = the most rows it can own)."""
+        return Workload(self.name + "_expert", self.T * self.S, self.N, self.K, self.bits, self.bs,
+                        self.act_dtype, self.out_dtype, self.scale_dtype, "normal", self.scale_lo,
+                        self.scale_hi, self.zp, self.seed)
+
+    def bytes(self, ids: np.ndarray) -> int:
+        """Algorithmic bytes: the selected experts' codes, scales and zero points once each, X and Y."""
+        w = self.expert()
+        active = len(np.unique(ids))
+        per_expert = (w.N * w.kblocks * w.blob + w.N * w.kblocks * DTYPE_BYTES[self.scale_dtype] +
+                      (w.N * w.zp_row_bytes if self.zp is not None else 0))
+        xrows = self.T * (self.S if self.x_per_slot else 1)
+        return (active * per_expert + xrows * self.K * DTYPE_BYTES[self.act_dtype] +
+                self.T * self.S * self.N * DTYPE_BYTES[self.out_dtype])
+
+
+MOE_CONFIGS = [
+    MoeWorkload("moe_t4_top2_e8_k4096_n14336_int4_bs32_asym_bf16", 4, 2, 8, 14336, 4096, 4, 32, BF16, BF16, F16,
+                scale_lo=0.001, scale_hi=0.01, zp=(0, 15), seed=SEED_BASE + 10),
+]
+
+
+def generate_moe(w: MoeWorkload, rng: Optional[np.random.Generator] = None) -> dict:
+    """Draw one grouped workload's inputs.
+
+    Returns a dict with
+      x      : [T, K] or [T, S, K] storage
+      ids    : [T, S] int32 expert indices
+      b      : [E, N, KB, blob] uint8 packed codes (ORT layout per expert)
+      scales : [E, N, KB] storage
+      zp     : [E, N, ceil(KB*bits/8)] uint8 or None
+    Draw order is fixed (x, ids, scales, b, zp).
+    """
+    if rng is None:
+        rng = np.random.default_rng(w.seed)
+    ew = w.expert()
+    x64 = rng.standard_normal((w.T, w.S, w.K) if w.x_per_slot else (w.T, w.K))
+    if w.ids == "distinct":
+        if w.S > w.E:
+            raise ValueError("distinct routing needs S <= E")
+        ids = np.stack([rng.permutation(w.E)[:w.S] for _ in range(w.T)]) if w.T else np.zeros((0, w.S))
+    elif w.ids == "repeat":
+        ids = rng.integers(0, w.E, size=(w.T, w.S))
+    else:
+        raise ValueError(w.ids)
+    s64 = rng.uniform(w.scale_lo, w.scale_hi, (w.E, w.N, ew.kblocks))
+    b = rng.integers(0, 256, size=(w.E, w.N, ew.kblocks, ew.blob), dtype=np.uint8)
+    zp = None
+    if w.zp is not None:
+        lo, hi = w.zp
+        if lo == 0 and hi == (1 << w.bits) - 1:
+            zp = rng.integers(0, 256, size=(w.E, w.N, ew.zp_row_bytes), dtype=np.uint8)
+        elif w.bits == 8:
+            zp = rng.integers(lo, hi + 1, size=(w.E, w.N, ew.zp_row_bytes), dtype=np.uint8)
+        else:
+            raise ValueError("a partial zero-point range needs packing; draw it in the caller")
+    return {
+        "x": to_storage(x64, w.act_dtype),
+        "ids": np.ascontiguousarray(ids, dtype=np.int32).reshape(w.T, w.S),
+        "b": b,
+        "scales": to_storage(s64, w.scale_dtype),
+        "zp": zp,
+    }

@@ -14,7 +14,8 @@ f64 and scales as f32 (every storage dtype of the operator widens exactly to
 these).
 
 Parity status of each function is recorded in its docstring; all are pinned
-by ``tests/test_oracle_pins.py``.
+by ``tests/test_oracle_pins.py`` (``matmul_grouped`` by
+``tests/test_oracle_grouped_pins.py``).
 """
 from __future__ import annotations
 
@@ -176,4 +177,41 @@ def matmul_a8(qa, sa, b, scales_f32, zp, N, K, bits, bs, bias_f64=None):
     mag = np.empty((M, N), dtype=np.float64)
     _load().oracle_matmul_a8(_ptr(qa), _ptr(sa), _ptr(b), _ptr(s), _ptr(zp), _ptr(bias), M, N, K, bits, bs,
                              _ptr(y), _ptr(mag))
+    return y, mag
+
+
+def matmul_grouped(x_f64, ids, b, scales_f32, zp, E, N, K, bits, bs, x_per_slot=False):
+    """Grouped (mixture-of-experts) product: (y[T, S, N] f64, absdot[T, S, N]).
+
+    y[t, s, :] = x_row(t, s) . dequant(B_e)^T with e = ids[t, s], where x_row is
+    x[t] (x: [T, K], one activation row shared by a token's slots) or x[t, s]
+    (x: [T, S, K]).  The steps are those of ggml's MUL_MAT_ID as the SpacemiT
+    backend computes it (toy 0.8.0, data/vendor/ggml/src/ggml-cpu/spacemit/
+    ime.cpp, forward_mul_mat_id): group the (token, slot) rows by the expert
+    they select, in ascending token-then-slot order, then multiply each group
+    by its expert's matrix (here ``matmul``, the pinned plain product) and
+    write each row back to its (token, slot).  With S = 1 it is rlx's grouped
+    dequant matmul (rlx-cpu 0.2.13, src/thunk/ops/quant.rs,
+    exec_dequant_grouped_mat_mul_gguf).  An expert id outside [0, E) is an
+    error, as the page's assertion makes it.
+    b: [E, N, KB, blob] uint8, scales_f32: [E, N, KB], zp: [E, N, zp_row] or None.
+    Pinned by a one-hot expert-sum restatement, relabelling invariance and
+    the E = 1 and equal-slot-rows reductions.
+    """
+    ids = np.asarray(ids)
+    T, S = ids.shape
+    x = np.asarray(x_f64, dtype=np.float64)
+    if np.any(ids < 0) or np.any(ids >= E):
+        raise ValueError("expert id out of range")
+    y = np.zeros((T, S, N), dtype=np.float64)
+    mag = np.zeros((T, S, N), dtype=np.float64)
+    for e in range(E):
+        rows = [(t, s) for t in range(T) for s in range(S) if ids[t, s] == e]
+        if not rows:
+            continue
+        xe = np.stack([x[t, s] if x_per_slot else x[t] for (t, s) in rows])
+        ye, me = matmul(xe, b[e], scales_f32[e], None if zp is None else zp[e], N, K, bits, bs)
+        for r, (t, s) in enumerate(rows):
+            y[t, s] = ye[r]
+            mag[t, s] = me[r]
     return y, mag
