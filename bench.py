@@ -5,8 +5,8 @@ Default workload: the int4 decode GEMV, M=1, K=4096, N=11008, bf16 X/Y, f16
 scales, uint8 zero points (block 32), metric GB/s (algorithmic bytes / time).
 ``--config 4`` selects the M=512 prefill GEMM (metric TFLOP/s).  The default
 run also reports the M=512 GEMM and the int8-activation path (accuracy level
-4: activation quantisation + integer GEMV) on the decode workload as
-secondary objects.
+4: activation quantisation + integer GEMV) on the decode workload and the
+grouped mixture-of-experts decode GEMV (``moe``) as secondary objects.
 
 A step is one mnb_matmul call over one batch (the decode step of one
 projection).  Weights are rotated over enough distinct copies that every
@@ -239,6 +239,47 @@ def run_ours(args):
 
     flags = 0 if args.no_pdl else mnb.MNB_FLAG_PDL
 
+    def replay_timed(call, R, steps, warmup, stream):
+        """Warm up, capture R calls (call(i) for i < R) in a CUDA graph, replay it
+        `warmup` steps untimed and `steps` steps timed with CUDA events on
+        `stream`, barrier + synchronise on both sides.  Returns (seconds, clocks,
+        full replays)."""
+        with torch.cuda.stream(stream):
+            for i in range(R):
+                call(i)
+        torch.cuda.synchronize()
+
+        def capture(n):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                for i in range(n):
+                    call(i)
+            return gr
+
+        g = capture(R)
+        rem = steps % R
+        g_rem = capture(rem) if rem else None
+        reps = steps // R
+        clocks = ClockSampler(local)
+        clocks.start()
+        with torch.cuda.stream(stream):
+            for _ in range(warmup // R):
+                g.replay()
+            for i in range(warmup % R):
+                call(i)
+        barrier()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            ev1.record(stream)
+        barrier()
+        ck = clocks.stop()
+        return max_over_ranks(ev0.elapsed_time(ev1) / 1e3, dist), ck, reps
+
     def measure(w: wl.Workload, steps: int, warmup: int, kernel: str, want_e2e: bool, acc: int = 0):
         data = wl.generate(w)
         x = to_dev(data["x"], w.act_dtype)
@@ -270,42 +311,8 @@ def run_ours(args):
                               w.K, w.bits, w.bs, w.act_dtype, w.out_dtype, w.scale_dtype, kernel=kernel,
                               stream=stream, flags=flags, accuracy_level=acc, workspace=ws)
 
-        with torch.cuda.stream(stream):
-            for i in range(R):
-                call(i)
-        torch.cuda.synchronize()
-
-        def capture(n):
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=stream):
-                for i in range(n):
-                    call(i)
-            return gr
-
-        g = capture(R)
-        rem = steps % R
-        g_rem = capture(rem) if rem else None
-        reps = steps // R
+        t, ck, reps = replay_timed(call, R, steps, warmup, stream)
         steps_eff = steps
-        clocks = ClockSampler(local)
-        clocks.start()
-        with torch.cuda.stream(stream):
-            for _ in range(warmup // R):
-                g.replay()
-            for i in range(warmup % R):
-                call(i)
-        barrier()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(reps):
-                g.replay()
-            if g_rem is not None:
-                g_rem.replay()
-            ev1.record(stream)
-        barrier()
-        ck = clocks.stop()
-        t = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, dist)
         unit, per_step = metric_of(w)
         value = whole_job_value(world, steps_eff, per_step, t)
         per_launch_s = t / steps_eff
@@ -363,6 +370,47 @@ def run_ours(args):
             out["e2e_launches"] = max(1, reps) * R * (kernels_per_step + 1)  # + the X fetch kernel
         return out, data
 
+    def measure_moe(w: wl.MoeWorkload, steps: int, warmup: int):
+        """The grouped (mixture-of-experts) decode GEMV: one launch over all experts per step."""
+        d = wl.generate_moe(w)
+        x = to_dev(d["x"], w.act_dtype)
+        ids = torch.from_numpy(d["ids"]).cuda()
+        ps = mnb.mnb_packed_size(w.N, w.K, w.bits, w.bs)
+        packed = aligned_empty(w.E * ps)
+        for e in range(w.E):
+            be = torch.from_numpy(np.ascontiguousarray(d["b"][e])).cuda()
+            mnb.mnb_pack_weights(be, packed[e * ps:(e + 1) * ps], w.N, w.K, w.bits, w.bs)
+            del be
+        s0 = to_dev(d["scales"], w.scale_dtype)
+        zp0 = None if d["zp"] is None else torch.from_numpy(np.ascontiguousarray(d["zp"])).cuda()
+        step_bytes = w.bytes(d["ids"])
+        l2 = torch.cuda.get_device_properties(local).L2_cache_size
+        R = max(2, math.ceil(3 * l2 / step_bytes))
+        copies = [(packed, s0, zp0)]
+        for _ in range(R - 1):
+            pb = aligned_empty(packed.numel())
+            pb.copy_(packed)
+            copies.append((pb, s0.clone(), None if zp0 is None else zp0.clone()))
+        y = torch.empty((w.T, w.S, w.N), dtype=TORCH_DT[w.out_dtype], device="cuda")
+        stream = torch.cuda.Stream()
+
+        def call(i):
+            pb, s, zp = copies[i % R]
+            mnb.mnb_matmul_grouped(x, ids, pb, s, zp, y, w.T, w.S, w.E, w.N, w.K, w.bits, w.bs, w.act_dtype,
+                                   w.out_dtype, w.scale_dtype, x_per_slot=w.x_per_slot, stream=stream)
+
+        t, ck, _ = replay_timed(call, R, steps, warmup, stream)
+        per_step = step_bytes / 1e9
+        per_launch_s = t / steps
+        achieved = per_step / per_launch_s
+        return {"workload": w.name, "value": whole_job_value(world, steps, per_step, t), "unit": "GB/s",
+                "kernel": "gemv_moe", "ms_per_step": per_launch_s * 1e3,
+                "experts_active": int(len(np.unique(d["ids"]))), "experts": w.E, "tokens": w.T, "top_k": w.S,
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                             "frac": achieved / pk["hbm_gbs"], "traffic": traffic_for(f"gemv_moe:{w.name}"),
+                             "peak_source": f"{pk_src} hbm_gbs"},
+                "clocks": ck, "weight_copies": R}, steps
+
     w = wl.config(args.config)
     main, data = measure(w, args.steps, args.warmup, args.kernel, True, args.accuracy_level)
     res = {
@@ -392,6 +440,10 @@ def run_ours(args):
                      "kernel": sec["kernel"], "ms_per_step": sec["ms_per_step"], "roofline": sec["roofline"],
                      "clocks": sec["clocks"], "launches_per_step": 2}
         res["gpu_launches"] += sec["launches"]
+    if args.config == 1 and args.accuracy_level == 0 and not args.no_secondary:
+        moe, n = measure_moe(wl.MOE_CONFIGS[0], max(20, args.steps // 10), max(3, args.warmup // 10))
+        res["moe"] = moe
+        res["gpu_launches"] += n
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = cpu_oracle_rate(w, data, args.cpu_seconds)
         res["cpu_baseline"] = {"value": v, "unit": main["unit"], "cores": cores, "kind": "oracle", "sample": sample}

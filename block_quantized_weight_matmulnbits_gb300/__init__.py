@@ -26,7 +26,7 @@ EXPORTS = [
     "mnb_packed_size", "mnb_pack_weights", "mnb_unpack_codes", "mnb_dequantize", "mnb_matmul",
     "mnb_matmul_ex", "mnb_workspace_size", "mnb_quantize_activations", "mnb_select_kernel",
     "mnb_get_device_error", "mnb_status_string", "mnb_kernel_name", "mnb_abi_version", "mnb_matmul_a8_static",
-    "mnb_matmul_host_io",
+    "mnb_matmul_host_io", "mnb_matmul_grouped",
 ]
 MNB_A8_STATIC_SCRATCH_BYTES = 1 << 20
 MNB_HOST_IO_X_BYTES = 8 << 20
@@ -83,6 +83,8 @@ def load(build: bool = True):
             "mnb_abi_version": (ci, []),
             "mnb_matmul_a8_static": (ci, [vp, vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, ci, ci, vp]),
             "mnb_matmul_host_io": (ci, [ctypes.POINTER(MatmulArgs)]),
+            "mnb_matmul_grouped": (ci, [vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, i64, i64, ci, ci, ci, ci, ci,
+                                        vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -188,6 +190,14 @@ def mnb_matmul_a8_static(x, packed_b, scales, zero_points, y, M, N, K, bits, blo
     _check(load().mnb_matmul_a8_static(_ptr(x), _ptr(packed_b), _ptr(scales), _ptr(zero_points), _ptr(y), M, N, K,
                                        bits, block_size, act_dtype, out_dtype, scale_dtype, _stream(stream)),
            "mnb_matmul_a8_static")
+
+
+def mnb_matmul_grouped(x, ids, packed_b, scales, zero_points, y, T, S, E, N, K, bits, block_size, act_dtype,
+                       out_dtype, scale_dtype, x_per_slot=False, stream=None):
+    """Grouped (mixture-of-experts) product: y[t, s] = x_row(t, s) . dequant(B[ids[t, s]])^T."""
+    _check(load().mnb_matmul_grouped(_ptr(x), _ptr(ids), _ptr(packed_b), _ptr(scales), _ptr(zero_points), _ptr(y),
+                                     T, S, E, 1 if x_per_slot else 0, N, K, bits, block_size, act_dtype, out_dtype,
+                                     scale_dtype, _stream(stream)), "mnb_matmul_grouped")
 
 
 def mnb_workspace_size(M, N, K, bits, block_size, accuracy_level) -> int:

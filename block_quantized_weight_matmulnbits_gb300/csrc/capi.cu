@@ -92,16 +92,21 @@ mnb_status from_cuda(cudaError_t e) {
     return MNB_ERR_CUDA;
 }
 
+}  // namespace
+
 // Test hook: MNB_FAIL_LAUNCH=1 makes every launch report a CUDA error without
 // launching anything (exercises the error path on the host, no GPU fault).
 bool inject_launch_failure() { return env_int("MNB_FAIL_LAUNCH", 0) == 1; }
-
-}  // namespace
 
 const DeviceInfo& device_info() {
     static DeviceInfo empty{};
     PerDevice* pd = per_device();
     return pd ? pd->info : empty;
+}
+
+int* device_status_word() {
+    PerDevice* pd = per_device();
+    return pd ? pd->status : nullptr;
 }
 
 }  // namespace mnb

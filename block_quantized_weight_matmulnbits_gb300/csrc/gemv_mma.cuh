@@ -186,18 +186,29 @@ inline Geom make_geom(const Layout& L, int64_t M, int MT) {
     return g;
 }
 
-// SPB_LOG >= 0: blocks of 2^SPB_LOG k-steps start at every warp slice (static
-// block structure); -1: any block size, run-time checks.
-// Occupancy by code width (measured on GB300): 8-bit codes are the longest K
-// (K-split clusters) and gain from 4 CTAs per SM; 2- and 4-bit codes are
-// faster with 3 CTAs per SM and spill-free registers.
-template <int BITS, bool BF16X, int MT, int SPB_LOG>
-__global__ void __launch_bounds__(kThreads, BITS == 8 ? 4 : 3) gemv_mma_kernel(MatmulParams p, Geom geo, int pdl) {
+// Activation and output rows of one CTA: local row m (0 <= m < M <= MT)
+// reads X row x_row(m) and writes Y row y_row(m).  prepare() runs once the
+// weight loads are in flight and before X is staged (every thread calls it;
+// it may synchronise the CTA) and fixes M.  The plain product uses rows
+// 0 .. M-1 of both; the grouped product gathers and scatters.
+struct DenseRows {
+    int M;
+    __device__ __forceinline__ void prepare() {}
+    __device__ __forceinline__ int64_t x_row(int m) const { return m; }
+    __device__ __forceinline__ int64_t y_row(int m) const { return m; }
+};
+
+// One CTA's share of the product: row tile rt, K-split `split` of its
+// cluster, rows given by `rows`.  SPB_LOG >= 0: blocks of 2^SPB_LOG k-steps
+// start at every warp slice (static block structure); -1: any block size,
+// run-time checks.
+template <int BITS, bool BF16X, int MT, int SPB_LOG, class Rows>
+__device__ __forceinline__ void gemv_tile(const MatmulParams& p, const Geom& geo, int pdl, int64_t rt, int split,
+                                          Rows& rows, uint8_t* smem) {
     using U = Unpack<BITS, BF16X>;
     constexpr int NTILE = MT / 8;  // MMA n8 tiles (activation rows 0-7, 8-15)
     constexpr int SPT = U::kStepsPerTile;
     const Layout& L = p.L;
-    extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* xb = smem;
     Entry* stage = reinterpret_cast<Entry*>(smem + geo.xb_bytes);
     float* red = reinterpret_cast<float*>(smem + geo.xb_bytes + geo.stage_bytes);
@@ -206,10 +217,7 @@ __global__ void __launch_bounds__(kThreads, BITS == 8 ? 4 : 3) gemv_mma_kernel(M
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int M = (int)p.M;
     const int C = geo.C;
-    const int64_t rt = blockIdx.x / C;
-    const int split = (int)(blockIdx.x - rt * C);
     const int64_t cta_t0 = (int64_t)split * geo.tiles_cta;  // first k-tile of this CTA
     const int64_t cta_t1 = imin64(cta_t0 + geo.tiles_cta, L.KTILES);
     const int tpw = geo.tpw;
@@ -332,6 +340,8 @@ __global__ void __launch_bounds__(kThreads, BITS == 8 ? 4 : 3) gemv_mma_kernel(M
         }
     }
     if (pdl) griddep_wait();  // X (and Y) may belong to the previous kernel on the stream
+    rows.prepare();
+    const int M = rows.M;
 
     // ---- 3. activations (B fragments) of this CTA's k-steps:
     //         row m, local k-step S, lane class t -> (X[m][k+2t..], X[m][k+2t+8..]);
@@ -344,9 +354,10 @@ __global__ void __launch_bounds__(kThreads, BITS == 8 ? 4 : 3) gemv_mma_kernel(M
         for (int it = tid; it < items; it += kThreads) {
             const int m = it / KS, S = it - m * KS;
             const int64_t k0 = k_cta0 + 16 * (int64_t)S;
+            const int64_t xr = rows.x_row(m);
             uint4 v0, v1;
             if (vec && k0 + 16 <= L.K) {
-                const uint4* src = reinterpret_cast<const uint4*>(x16 + m * L.K + k0);
+                const uint4* src = reinterpret_cast<const uint4*>(x16 + xr * L.K + k0);
                 v0 = __ldg(src);
                 v1 = __ldg(src + 1);
             } else {
@@ -354,8 +365,8 @@ __global__ void __launch_bounds__(kThreads, BITS == 8 ? 4 : 3) gemv_mma_kernel(M
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int64_t ka = k0 + 2 * j, kb2 = ka + 1;
-                    const uint32_t lo = ka < L.K ? x16[m * L.K + ka] : 0u;
-                    const uint32_t hi = kb2 < L.K ? x16[m * L.K + kb2] : 0u;
+                    const uint32_t lo = ka < L.K ? x16[xr * L.K + ka] : 0u;
+                    const uint32_t hi = kb2 < L.K ? x16[xr * L.K + kb2] : 0u;
                     h[j] = lo | (hi << 16);
                 }
                 v0 = make_uint4(h[0], h[1], h[2], h[3]);
@@ -494,9 +505,21 @@ __global__ void __launch_bounds__(kThreads, BITS == 8 ? 4 : 3) gemv_mma_kernel(M
         const int64_t n = rt * 16 + row;
         if (n < L.N) {
             if (p.bias) v += load_f32(p.bias, n, p.bias_dtype);
-            store_f32(p.y, (int64_t)m * L.N + n, v, p.out_dtype);
+            store_f32(p.y, rows.y_row(m) * L.N + n, v, p.out_dtype);
         }
     }
+}
+
+// The plain product: one CTA per (row tile, K-split), rows 0 .. M-1.
+// Occupancy by code width (measured on GB300): 8-bit codes are the longest K
+// (K-split clusters) and gain from 4 CTAs per SM; 2- and 4-bit codes are
+// faster with 3 CTAs per SM and spill-free registers.
+template <int BITS, bool BF16X, int MT, int SPB_LOG>
+__global__ void __launch_bounds__(kThreads, BITS == 8 ? 4 : 3) gemv_mma_kernel(MatmulParams p, Geom geo, int pdl) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int64_t rt = blockIdx.x / geo.C;
+    DenseRows rows{(int)p.M};
+    gemv_tile<BITS, BF16X, MT, SPB_LOG>(p, geo, pdl, rt, (int)(blockIdx.x - rt * geo.C), rows, smem);
 }
 
 template <int BITS, bool BF16X, int MT, int SPB_LOG>

@@ -9,7 +9,6 @@
 //      while X is in flight, waits for the fetch before it reads X, and
 //      stores Y straight into the host buffer.
 // The library allocates nothing.
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -76,11 +75,6 @@ const void* device_alias(const void* p) {
     }
 }
 
-bool fail_launch_hook() {
-    const char* v = std::getenv("MNB_FAIL_LAUNCH");
-    return v && v[0] == '1' && v[1] == 0;
-}
-
 }  // namespace
 
 extern "C" {
@@ -117,7 +111,7 @@ mnb_status mnb_matmul_host_io(const mnb_matmul_args* args) {
         cudaGetLastError();
         return MNB_ERR_CUDA;
     }
-    if (fail_launch_hook()) return MNB_ERR_CUDA;
+    if (mnb::inject_launch_failure()) return MNB_ERR_CUDA;
 
     const int64_t n16 = (int64_t)(x_bytes / 16);
     const int tail = (int)(x_bytes % 16);

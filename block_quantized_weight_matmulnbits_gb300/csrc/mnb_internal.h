@@ -63,4 +63,10 @@ struct DeviceInfo {
 };
 const DeviceInfo& device_info();
 
+// Device address of the current device's status word (see mnb_get_device_error).
+int* device_status_word();
+
+// MNB_FAIL_LAUNCH=1: entry points report MNB_ERR_CUDA instead of launching.
+bool inject_launch_failure();
+
 }  // namespace mnb

@@ -25,7 +25,9 @@
  *   - Pointers documented as "device" must point to memory the current CUDA
  *     device can access (cudaMalloc, or a torch CUDA tensor's data_ptr()).
  *     The caller owns every buffer; the library allocates no device memory
- *     and keeps no state between calls other than a per-device status word.
+ *     and keeps no state between calls other than a per-device status word
+ *     and the file-scope device arrays of mnb_matmul_a8_static and
+ *     mnb_matmul_host_io.
  *   - All work is enqueued on `stream` (NULL = the legacy default stream) and
  *     is asynchronous.  A returned MNB_OK means the arguments were valid and
  *     the launch was accepted; faults during execution surface at the
@@ -90,8 +92,8 @@ typedef enum mnb_kernel {
  * kernel on the stream has finished (its X and Y accesses still wait for it),
  * and lets the next kernel start as its own blocks retire.  Use it only when
  * the preceding kernel does not write packed_b, scales, zero_points or bias
- * (true for constant model weights).  Honoured by MNB_KERNEL_GEMV_MMA; other
- * kernels ignore it. */
+ * (true for constant model weights).  Honoured by MNB_KERNEL_GEMV_MMA and
+ * MNB_KERNEL_GEMV_I8; other kernels ignore it. */
 #define MNB_FLAG_PDL 1
 
 /* ---- weight layout (one-time re-tiling) -------------------------------- */
@@ -216,6 +218,36 @@ MNB_API mnb_status mnb_matmul_a8_static(const void* x, const void* packed_b, con
                                         int bits, int block_size, mnb_dtype act_dtype, mnb_dtype out_dtype,
                                         mnb_dtype scale_dtype, mnb_stream_t stream);
 
+/* Grouped (mixture-of-experts) MatMulNBits, one launch over all experts:
+ *   Y[t, s, :] = X_row(t, s) . dequant(B_{ids[t, s]})^T   (0 <= t < T, 0 <= s < S)
+ * This is ggml's MUL_MAT_ID as the SpacemiT backend computes it (toy 0.8.0,
+ * data/vendor/ggml/src/ggml-cpu/spacemit/ime.cpp, forward_mul_mat_id:
+ * (slot, token) rows grouped by the expert they select, in ascending
+ * token-then-slot order, each group one product with that expert's matrix)
+ * and rlx's grouped dequant matmul (rlx-cpu 0.2.13, src/thunk/ops/quant.rs,
+ * exec_dequant_grouped_mat_mul_gguf: one expert per row, S = 1).
+ *   x           device [T, K] (x_per_slot = 0: one activation row per token,
+ *               shared by its S slots) or [T, S, K] (x_per_slot = 1), bf16
+ *               or f16 (f32 is MNB_ERR_UNSUPPORTED), 16-byte aligned.
+ *   ids         device int32 [T, S]: the expert of each (token, slot).
+ *   packed_b    device, 256-byte aligned: E packed weights back to back, each
+ *               mnb_packed_size(N, K, bits, block_size) bytes as written by
+ *               mnb_pack_weights from that expert's ORT bytes.
+ *   scales      device [E, N, KB] of scale_dtype.
+ *   zero_points device uint8 [E, N, ceil(KB*bits/8)] or NULL (default
+ *               2^(bits-1) for every expert).
+ *   y           device [T, S, N] of out_dtype, 16-byte aligned.
+ * The weights of experts that no pair selects are not read.  Limits:
+ * E <= 1024 and T*S <= 4096 (MNB_ERR_UNSUPPORTED beyond).  An id outside
+ * [0, E) is not checked on the host (ids live on the device): its Y row is
+ * left unwritten and the device status word becomes MNB_ERR_INVALID_ARG
+ * (read it with mnb_get_device_error).  T == 0 returns MNB_OK. */
+MNB_API mnb_status mnb_matmul_grouped(const void* x, const int32_t* ids, const void* packed_b, const void* scales,
+                                      const uint8_t* zero_points, void* y, int64_t T, int64_t S, int64_t E,
+                                      int x_per_slot, int64_t N, int64_t K, int bits, int block_size,
+                                      mnb_dtype act_dtype, mnb_dtype out_dtype, mnb_dtype scale_dtype,
+                                      mnb_stream_t stream);
+
 /* mnb_matmul_ex with X and Y in page-locked HOST memory: the call moves the
  * activations in and the result out itself, with no copy-engine transfers.
  * No counterpart on the pages; an addition to the boundary.
@@ -257,6 +289,7 @@ MNB_API mnb_status mnb_matmul_host_io(const mnb_matmul_args* args);
  *                          tile width, ring depth and scale path of the
  *                          shared-memory prefill GEMM
  *   MNB_GEMV_STAGE_BUFS, MNB_GEMV_MAX_SLOTS  ring shape of the f32 GEMV
+ *   MNB_MOE_SETS           expert sets per row tile of mnb_matmul_grouped
  *   MNB_FAIL_LAUNCH=1      test hook: every launch reports MNB_ERR_CUDA
  *                          without launching */
 
