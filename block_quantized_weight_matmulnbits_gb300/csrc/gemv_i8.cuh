@@ -134,6 +134,46 @@ __device__ __forceinline__ void act_words(const uint32_t (&v)[8], int t, uint32_
     }
 }
 
+// Zero points and weight scales of a CTA's 16 rows x kb_cta blocks into the
+// entry table (entry (r, j) at r * kbs + j).  Each thread issues the loads of
+// all its entries (up to kPer per pass, consecutive threads on consecutive
+// blocks) before it decodes any, so a pass costs one memory latency rather
+// than one per entry.  SC is the stored scale type (float, or the 16-bit
+// pattern of f16 / bf16).
+template <typename SC>
+__device__ __forceinline__ void stage_entries(const MatmulParams& p, const Layout& L, int64_t rt, int64_t kb0,
+                                              int kb_cta, int kbs, Entry* stage) {
+    constexpr int kPer = 4;
+    const int tid = threadIdx.x;
+    const int total = 16 * kb_cta;
+    const SC* sc = static_cast<const SC*>(p.scales);
+    for (int base = 0; base < total; base += kPer * kThreads) {
+        SC raw[kPer];
+        int zq[kPer];
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int it = base + q * kThreads + tid;
+            const int r = it / kb_cta, j = it - r * kb_cta;
+            const int64_t n = rt * 16 + r, kb = kb0 + j;
+            const bool ok = it < total && n < L.N && kb < L.KB;
+            raw[q] = ok ? __ldg(sc + n * L.KB + kb) : SC(0);
+            zq[q] = ok ? load_zp(p.zp, L, n, kb) : 0;
+        }
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int it = base + q * kThreads + tid;
+            if (it < total) {
+                const int r = it / kb_cta, j = it - r * kb_cta;
+                float sv;
+                if constexpr (sizeof(SC) == 4) sv = raw[q];
+                else if (p.scale_dtype == kF16) sv = __half2float(__ushort_as_half(raw[q]));
+                else sv = __uint_as_float(static_cast<uint32_t>(raw[q]) << 16);
+                stage[r * kbs + j] = Entry{zq[q], sv};
+            }
+        }
+    }
+}
+
 // ---- 2. the GEMV ----
 // SPB_LOG >= 0: blocks of 2^SPB_LOG k-steps and every warp slice starts on a
 // block boundary (static block ends); -1: run-time block ends.
@@ -184,16 +224,8 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : 1)
     if (pdl) griddep_launch_dependents();
 
     // ---- zero points and weight scales of the CTA's (row, block)s ----
-    for (int it = tid; it < 16 * kb_cta; it += kThreads) {
-        const int r = it / kb_cta, j = it - r * kb_cta;
-        const int64_t n = rt * 16 + r, kb = kb0 + j;
-        Entry e{0, 0.f};
-        if (n < L.N && kb < L.KB) {
-            e.z = load_zp(p.zp, L, n, kb);
-            e.s = load_f32(p.scales, n * L.KB + kb, p.scale_dtype);
-        }
-        stage[r * kbs + j] = e;
-    }
+    if (p.scale_dtype == kF32) stage_entries<float>(p, L, rt, kb0, kb_cta, kbs, stage);
+    else stage_entries<uint16_t>(p, L, rt, kb0, kb_cta, kbs, stage);
 
     griddep_wait();  // the workspace is written by the quantisation kernel
 
