@@ -3,8 +3,10 @@
 // directly over NVLink-C2C, so the transfers are done by kernels rather than
 // by copy-engine operations (each of which costs a few microseconds of
 // dependency latency per call):
-//   1. fetch_kernel reads X from the host into a file-scope device array and
-//      immediately allows its programmatic dependent to launch;
+//   1. fetch_kernel reads X from the host into one of two file-scope device
+//      arrays (alternate calls use alternate arrays) and immediately allows
+//      its programmatic dependent to launch; with MNB_FLAG_PDL it is itself a
+//      programmatic dependent of the preceding kernel;
 //   2. the matmul (mnb_matmul_ex with MNB_FLAG_PDL) starts its weight stream
 //      while X is in flight, waits for the fetch before it reads X, and
 //      stores Y straight into the host buffer.
@@ -21,12 +23,16 @@ constexpr size_t kXBytes = MNB_HOST_IO_X_BYTES;
 constexpr int kMaxDevices = 64;
 constexpr int kFetchThreads = 256;
 
-// One per device (a __device__ variable exists once in every context).
-static __device__ __align__(256) uint8_t g_host_x[kXBytes];
+// Two staging buffers per device (a __device__ variable exists once in every
+// context), used by alternate calls: the fetch of call i+1 may run while the
+// matmul of call i still reads its X.
+static __device__ __align__(256) uint8_t g_host_x[2][kXBytes];
 
 std::mutex g_mu;
 void* g_x_dev[kMaxDevices] = {};
+unsigned g_calls[kMaxDevices] = {};
 
+// The staging buffer of this call: the two alternate call by call.
 cudaError_t x_buffer_for_current_device(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -39,13 +45,16 @@ cudaError_t x_buffer_for_current_device(void** out) {
         if (e != cudaSuccess) return e;
         g_x_dev[dev] = p;
     }
-    *out = g_x_dev[dev];
+    *out = static_cast<uint8_t*>(g_x_dev[dev]) + (size_t)(g_calls[dev]++ & 1u) * kXBytes;
     return cudaSuccess;
 }
 
 // Copy n16 16-byte words, then `tail` trailing bytes, from host-resident src
 // to device dst.  Loads use the "fetch again" cache operator: host memory
-// is written by the CPU between calls.
+// is written by the CPU between calls.  Launched as a programmatic dependent
+// (MNB_FLAG_PDL) it copies while the preceding kernel still runs and
+// finishes only after that kernel has: the matmul that waits on this fetch
+// is then ordered after the preceding call's matmul as well.
 __global__ void __launch_bounds__(kFetchThreads) fetch_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                                              int64_t n16, int tail) {
     mnb::griddep_launch_dependents();  // the matmul may start streaming its weights now
@@ -56,6 +65,7 @@ __global__ void __launch_bounds__(kFetchThreads) fetch_kernel(const uint4* __res
         uint8_t* d8 = reinterpret_cast<uint8_t*>(dst + n16);
         d8[threadIdx.x] = __ldcv(s8 + threadIdx.x);
     }
+    mnb::griddep_wait();  // no-op unless launched as a programmatic dependent
 }
 
 // Device address of a caller pointer that must be page-locked host memory
@@ -120,10 +130,21 @@ mnb_status mnb_matmul_host_io(const mnb_matmul_args* args) {
     int64_t grid = (n16 + kFetchThreads - 1) / kFetchThreads;
     if (grid > 2 * (int64_t)sms) grid = 2 * (int64_t)sms;
     if (grid < 1) grid = 1;
-    fetch_kernel<<<(unsigned)grid, kFetchThreads, 0, s>>>(static_cast<const uint4*>(x_dev),
-                                                            static_cast<uint4*>(xbuf), n16, tail);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return MNB_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kFetchThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (a.flags & MNB_FLAG_PDL) ? 1 : 0;
+    const uint4* src = static_cast<const uint4*>(x_dev);
+    uint4* dst = static_cast<uint4*>(xbuf);
+    if (cudaLaunchKernelEx(&cfg, fetch_kernel, src, dst, n16, tail) != cudaSuccess) {
+        cudaGetLastError();
+        return MNB_ERR_CUDA;
+    }
 
     mnb_matmul_args b = a;
     b.x = xbuf;

@@ -256,10 +256,14 @@ MNB_API mnb_status mnb_matmul_grouped(const void* x, const int32_t* ids, const v
  *   args->y  host [M, N] of out_dtype, 16-byte aligned, page-locked.
  *   Everything else is as mnb_matmul_ex (device weights, scales, workspace).
  * Steps, all on args->stream: one small kernel reads X over the host link
- * into a file-scope device array of MNB_HOST_IO_X_BYTES (8 MiB) per device;
- * the matmul runs as its programmatic dependent (its weight stream starts
- * while X is in flight) and stores Y straight into the host buffer.  Y is
- * complete when the stream's work is (synchronise before reading it).
+ * into one of two file-scope device arrays of MNB_HOST_IO_X_BYTES (8 MiB)
+ * per device (alternate calls use alternate arrays); the matmul runs as its
+ * programmatic dependent (its weight stream starts while X is in flight) and
+ * stores Y straight into the host buffer.  With MNB_FLAG_PDL the X read also
+ * starts before the preceding kernel on the stream has finished (the
+ * preceding kernel must then not write x either); every call's Y stores stay
+ * ordered after the preceding kernel's completion.  Y is complete when the
+ * stream's work is (synchronise before reading it).
  *   Pointer check: outside stream capture every call checks with
  *   cudaPointerGetAttributes that x and y are page-locked host memory (or
  *   device memory) and uses the device address that reports; pageable
@@ -267,10 +271,10 @@ MNB_API mnb_status mnb_matmul_grouped(const void* x, const int32_t* ids, const v
  *   the addresses are used as given: under unified addressing the device
  *   address of page-locked memory is its host address.
  *   Limits: M*K*sizeof(act) > MNB_HOST_IO_X_BYTES returns MNB_ERR_NO_MEM
- *   without launching.  The first call on a device looks the array up
+ *   without launching.  The first call on a device looks the arrays up
  *   (cudaGetSymbolAddress); make it outside stream capture.  Calls that
  *   overlap on one device (different streams, graphs in flight together)
- *   share the array and race; calls ordered on one stream are safe.
+ *   share the arrays and race; calls ordered on one stream are safe.
  * Returns the statuses of mnb_matmul_ex. */
 #define MNB_HOST_IO_X_BYTES (8u << 20)
 MNB_API mnb_status mnb_matmul_host_io(const mnb_matmul_args* args);

@@ -126,3 +126,58 @@ def test_host_io_rejects_x_beyond_the_staging_array(mnb):
     with pytest.raises(mnb.MnbError) as e:
         mnb.mnb_matmul_host_io(xh, packed, s, None, yh, M + 1, N, K, 4, 32, BF16, BF16, F16)
     assert e.value.status == mnb.MNB_ERR_NO_MEM
+
+
+@pytest.mark.parametrize("case", [0, 5], ids=["gemv_mma", "int8_path"])
+def test_host_io_pdl_back_to_back_calls_without_syncs(mnb, case):
+    """MNB_FLAG_PDL: each call's X fetch may start before the previous call's
+    matmul has finished.  Six calls issued back to back (eager, then twice in
+    one captured graph), each with its own host X and Y, must each give the
+    device-buffer call's result."""
+    from tests import _gpu as G
+    w, acc = CASES[case]
+    P = G.Problem(w)
+    ws_bytes = mnb.mnb_workspace_size(w.M, w.N, w.K, w.bits, w.bs, acc)
+    ws = G.aligned_empty(ws_bytes) if ws_bytes else None
+    rng = np.random.default_rng(88)
+    n = 6
+    xs = [P.x] + [P.x[:, torch.from_numpy(rng.permutation(w.K)).cuda()].contiguous() for _ in range(n - 1)]
+    refs = []
+    for x in xs:
+        y = torch.empty((w.M, w.N), dtype=G.TORCH_DT[w.out_dtype], device="cuda")
+        mnb.mnb_matmul_ex(x, P.packed, P.s, P.zp, y, w.M, w.N, w.K, w.bits, w.bs, w.act_dtype, w.out_dtype,
+                          w.scale_dtype, accuracy_level=acc, workspace=ws)
+        refs.append(y.cpu())
+    torch.cuda.synchronize()
+    xhs = [_pinned_like(P.x) for _ in range(n)]
+    for xh, x in zip(xhs, xs):
+        xh.copy_(x.cpu())
+    yhs = [torch.empty((w.M, w.N), dtype=G.TORCH_DT[w.out_dtype]).pin_memory() for _ in range(n)]
+    stream = torch.cuda.Stream()
+
+    def calls():
+        for xh, yh in zip(xhs, yhs):
+            mnb.mnb_matmul_host_io(xh, P.packed, P.s, P.zp, yh, w.M, w.N, w.K, w.bits, w.bs, w.act_dtype,
+                                   w.out_dtype, w.scale_dtype, accuracy_level=acc, workspace=ws, stream=stream,
+                                   flags=mnb.MNB_FLAG_PDL)
+
+    def check():
+        for i, (yh, ref) in enumerate(zip(yhs, refs)):
+            assert torch.equal(_bits(yh), _bits(ref)), f"call {i}"
+
+    for yh in yhs:
+        yh.fill_(float("nan"))
+    with torch.cuda.stream(stream):
+        calls()
+    stream.synchronize()
+    check()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        calls()
+    for _ in range(2):
+        for yh in yhs:
+            yh.fill_(float("nan"))
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+        check()
