@@ -15,7 +15,8 @@ these).
 
 Parity status of each function is recorded in its docstring; all are pinned
 by ``tests/test_oracle_pins.py`` (``matmul_grouped`` by
-``tests/test_oracle_grouped_pins.py``).
+``tests/test_oracle_grouped_pins.py``, the FP8 / NVFP4 functions by
+``tests/test_oracle_fp_formats_pins.py``).
 """
 from __future__ import annotations
 
@@ -73,6 +74,15 @@ def _load():
         lib.oracle_quantize_act.restype = None
         lib.oracle_matmul_a8.argtypes = [p, p, p, p, p, p, i64, i64, i64, ci, ci, p, p]
         lib.oracle_matmul_a8.restype = None
+        for name in ("oracle_fp8_e4m3", "oracle_fp8_e5m2", "oracle_e4m3fn_scale", "oracle_e2m1"):
+            getattr(lib, name).argtypes = [ci]
+            getattr(lib, name).restype = ctypes.c_float
+        lib.oracle_matmul_fp8.argtypes = [p, p, p, i64, i64, i64, ci, p, p]
+        lib.oracle_matmul_fp8.restype = None
+        lib.oracle_nvfp4_weight.argtypes = [p, p, ctypes.c_float, i64, i64, i64]
+        lib.oracle_nvfp4_weight.restype = ctypes.c_float
+        lib.oracle_matmul_nvfp4.argtypes = [p, p, p, ctypes.c_float, i64, i64, i64, p, p]
+        lib.oracle_matmul_nvfp4.restype = None
         lib.oracle_threads.argtypes = []
         lib.oracle_threads.restype = ci
         lib.oracle_set_threads.argtypes = [ci]
@@ -214,4 +224,64 @@ def matmul_grouped(x_f64, ids, b, scales_f32, zp, E, N, K, bits, bs, x_per_slot=
         for r, (t, s) in enumerate(rows):
             y[t, s] = ye[r]
             mag[t, s] = me[r]
+    return y, mag
+
+
+# ---- other weight formats: FP8 and NVFP4 (rlx-cpu 0.2.13, src/thunk/ops/quant.rs) ----
+
+def _decode_each(fn, codes):
+    codes = np.asarray(codes)
+    return np.array([fn(int(c)) for c in codes.ravel()], dtype=np.float32).reshape(codes.shape)
+
+
+def fp8_decode(codes, e5m2=False) -> np.ndarray:
+    """FP8 codes to f32 as the page's fp8_e4m3_to_f32 / fp8_e5m2_to_f32 define them
+    (exponent all ones: infinity or NaN).  Pinned."""
+    lib = _load()
+    return _decode_each(lib.oracle_fp8_e5m2 if e5m2 else lib.oracle_fp8_e4m3, codes)
+
+
+def e4m3fn_scale(codes) -> np.ndarray:
+    """NVFP4 block-scale codes to f32 (OCP E4M3, no infinity; the page's
+    fp8_e4m3_scale_to_f32 is not printed).  Pinned."""
+    return _decode_each(_load().oracle_e4m3fn_scale, codes)
+
+
+def e2m1(nibbles) -> np.ndarray:
+    """FP4 E2M1 codes to f32 (OCP E2M1; the page's fp4_e2m1_to_f32 is not printed).  Pinned."""
+    return _decode_each(_load().oracle_e2m1, nibbles)
+
+
+def matmul_fp8(x_f64, w8, scales_f32, K, N, e5m2=False):
+    """dequant_matmul_fp8: (y[M, N] f64, absdot) with y[i, j] = sum_p x[i, p] * fp8(w8[p, j]) * s[j];
+    w8 is [K, N] uint8, scales [N] f32 or None (1.0).  Pinned."""
+    x = _f64(x_f64).reshape(-1, K)
+    M = x.shape[0]
+    w8, s = _u8(w8), _f32(scales_f32)
+    y = np.empty((M, N), dtype=np.float64)
+    mag = np.empty((M, N), dtype=np.float64)
+    _load().oracle_matmul_fp8(_ptr(x), _ptr(w8), _ptr(s), M, K, N, 1 if e5m2 else 0, _ptr(y), _ptr(mag))
+    return y, mag
+
+
+def nvfp4_weights(w4, scale8, global_scale, K, N) -> np.ndarray:
+    """The dequantised NVFP4 weights [K, N] f32, each formed as the page forms it.  Pinned."""
+    lib = _load()
+    w4, s8 = _u8(w4), _u8(scale8)
+    out = np.empty((K, N), dtype=np.float32)
+    for p in range(K):
+        for j in range(N):
+            out[p, j] = lib.oracle_nvfp4_weight(_ptr(w4), _ptr(s8), float(global_scale), N, p, j)
+    return out
+
+
+def matmul_nvfp4(x_f64, w4, scale8, global_scale, K, N):
+    """dequant_matmul_nvfp4: (y[M, N] f64, absdot); w4 holds K*N nibbles (flat index p*N + j, low nibble
+    first), scale8 the [ceil(K/16), N] e4m3 block scales.  Pinned."""
+    x = _f64(x_f64).reshape(-1, K)
+    M = x.shape[0]
+    w4, s8 = _u8(w4), _u8(scale8)
+    y = np.empty((M, N), dtype=np.float64)
+    mag = np.empty((M, N), dtype=np.float64)
+    _load().oracle_matmul_nvfp4(_ptr(x), _ptr(w4), _ptr(s8), float(global_scale), M, K, N, _ptr(y), _ptr(mag))
     return y, mag

@@ -26,7 +26,9 @@
  *  - rlx-cpu 0.2.13, src/thunk/ops/quant.rs: `dequant_matmul_int4`
  *      ((nibble - z) * s, low nibble first) corroborates the dequant form;
  *      the per-channel quantize thunk rounds with Rust's f32::round (half
- *      away from zero), which is the rounding used for int8 activations.
+ *      away from zero), which is the rounding used for int8 activations;
+ *      `fp8_e4m3_to_f32`, `fp8_e5m2_to_f32`, `dequant_matmul_fp8` and
+ *      `dequant_matmul_nvfp4` define the FP8 and NVFP4 weight formats.
  */
 #include <math.h>
 #include <stddef.h>
@@ -214,6 +216,118 @@ void oracle_matmul_a8(const int8_t* qa, const float* sa, const uint8_t* b, const
             }
             y[m * N + n] = acc;
             if (absdot) absdot[m * N + n] = mag;
+        }
+    }
+}
+
+/* ---- other weight formats: FP8 and NVFP4 ---------------------------------
+ * rlx-cpu 0.2.13, src/thunk/ops/quant.rs: fp8_e4m3_to_f32, fp8_e5m2_to_f32,
+ * dequant_matmul_fp8, dequant_matmul_nvfp4.  Weights are stored [K, N]
+ * (element (p, j) at flat index p * N + j). */
+
+/* A minifloat with `ebits` exponent bits (bias 2^(ebits-1) - 1) and `mbits`
+ * mantissa bits, as the page decodes FP8: exponent 0 is subnormal
+ * (mant * 2^(1 - bias - mbits)); the all-ones exponent is infinity for a zero
+ * mantissa and NaN otherwise (IEEE style). */
+static float ieee_minifloat(unsigned code, int ebits, int mbits) {
+    unsigned sign = (code >> (ebits + mbits)) & 1u;
+    unsigned e = (code >> mbits) & ((1u << ebits) - 1u);
+    unsigned m = code & ((1u << mbits) - 1u);
+    int bias = (1 << (ebits - 1)) - 1;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, 1 - bias - mbits);
+    } else if (e == (1u << ebits) - 1u) {
+        if (m != 0) return NAN;
+        v = INFINITY;
+    } else {
+        v = ldexp(1.0 + ldexp((double)m, -mbits), (int)e - bias);
+    }
+    return (float)(sign ? -v : v);
+}
+
+/* fp8_e4m3_to_f32 as the page defines it (exponent 15 is inf / NaN). */
+float oracle_fp8_e4m3(int code) { return ieee_minifloat((unsigned)code & 0xFFu, 4, 3); }
+
+/* fp8_e5m2_to_f32 as the page defines it. */
+float oracle_fp8_e5m2(int code) { return ieee_minifloat((unsigned)code & 0xFFu, 5, 2); }
+
+/* NVFP4 block scale.  The page calls fp8_e4m3_scale_to_f32 without printing
+ * it; read as the OCP E4M3 format NVFP4 scales are stored in ("fn": no
+ * infinity, exponent 15 is a normal binade except mantissa 7, which is NaN;
+ * largest value 448). */
+float oracle_e4m3fn_scale(int code) {
+    unsigned c = (unsigned)code & 0xFFu;
+    unsigned e = (c >> 3) & 0xFu, m = c & 7u;
+    if (e == 15u && m == 7u) return NAN;
+    double v = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, (int)e - 7);
+    return (float)((c & 0x80u) ? -v : v);
+}
+
+/* FP4 E2M1 weight code.  The page calls fp4_e2m1_to_f32 without printing it;
+ * read as OCP E2M1: sign, 2 exponent bits (bias 1), 1 mantissa bit, no
+ * infinity or NaN: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+float oracle_e2m1(int nibble) {
+    unsigned c = (unsigned)nibble & 0xFu;
+    unsigned e = (c >> 1) & 3u, m = c & 1u;
+    double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, (int)e - 1);
+    return (float)((c & 8u) ? -v : v);
+}
+
+/* dequant_matmul_fp8: y[i, j] = sum_p x[i, p] * w(p, j) * s[j], w the FP8 code
+ * at w8[p * N + j] decoded as e4m3 (e5m2 = 0) or e5m2, s[j] = scales[j] or 1
+ * when scales is NULL (the page's missing-scale default).  f64 accumulation;
+ * absdot = sum_p |x * w * s|. */
+void oracle_matmul_fp8(const double* x, const uint8_t* w8, const float* scales, int64_t M, int64_t K, int64_t N,
+                       int e5m2, double* y, double* absdot) {
+    int64_t j;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (j = 0; j < N; ++j) {
+        double s = scales ? (double)scales[j] : 1.0;
+        for (int64_t i = 0; i < M; ++i) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t p = 0; p < K; ++p) {
+                int code = w8[p * N + j];
+                double w = e5m2 ? oracle_fp8_e5m2(code) : oracle_fp8_e4m3(code);
+                double t = x[i * K + p] * w * s;
+                acc += t;
+                mag += fabs(t);
+            }
+            y[i * N + j] = acc;
+            if (absdot) absdot[i * N + j] = mag;
+        }
+    }
+}
+
+/* The NVFP4 weight (p, j), formed in f32 as the page forms it:
+ * e2m1(nibble) * e4m3(block scale) * global_scale, with the nibble at flat
+ * index f = p * N + j (byte f / 2, low nibble when f is even) and the block
+ * scale at scale8[(p / 16) * N + j]. */
+float oracle_nvfp4_weight(const uint8_t* w4, const uint8_t* scale8, float global_scale, int64_t N, int64_t p,
+                          int64_t j) {
+    int64_t f = p * N + j;
+    int nibble = (f & 1) ? (w4[f / 2] >> 4) : (w4[f / 2] & 0x0F);
+    volatile float a = oracle_e2m1(nibble) * oracle_e4m3fn_scale(scale8[(p / 16) * N + j]);
+    volatile float w = a * global_scale;
+    return w;
+}
+
+/* dequant_matmul_nvfp4: y[i, j] = sum_p x[i, p] * w(p, j), f64 accumulation;
+ * absdot = sum_p |x * w|. */
+void oracle_matmul_nvfp4(const double* x, const uint8_t* w4, const uint8_t* scale8, float global_scale, int64_t M,
+                         int64_t K, int64_t N, double* y, double* absdot) {
+    int64_t j;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (j = 0; j < N; ++j) {
+        for (int64_t i = 0; i < M; ++i) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t p = 0; p < K; ++p) {
+                double t = x[i * K + p] * (double)oracle_nvfp4_weight(w4, scale8, global_scale, N, p, j);
+                acc += t;
+                mag += fabs(t);
+            }
+            y[i * N + j] = acc;
+            if (absdot) absdot[i * N + j] = mag;
         }
     }
 }
