@@ -46,7 +46,8 @@ mnb_status mnb_matmul_grouped(const void* x, const int32_t* ids, const void* pac
         !aligned_to(scales, dt_bytes(scale_dtype)))
         return MNB_ERR_INVALID_ARG;
     if (act_dtype == MNB_F32) return MNB_ERR_UNSUPPORTED;
-    if (E > gmoe::kMaxExperts || S > gmoe::kMaxPairs || T * S > gmoe::kMaxPairs) return MNB_ERR_UNSUPPORTED;
+    if (E > gmoe::kMaxExperts || T > gmoe::kMaxPairs || S > gmoe::kMaxPairs || T * S > gmoe::kMaxPairs)
+        return MNB_ERR_UNSUPPORTED;  // (T and S bounded first: T * S cannot overflow)
     const int pairs = (int)(T * S);
     const int MT = pairs <= 8 ? 8 : 16;
 

@@ -110,3 +110,49 @@ def test_status_strings(lib):
     for s in range(7):
         assert mnb.mnb_status_string(s)
     assert mnb.mnb_kernel_name(3) == "gemm_tc"
+
+
+def _grouped(lib, **kw):
+    d = dict(x=FAKE, ids=FAKE, packed_b=FAKE, scales=FAKE, zp=None, y=FAKE, T=4, S=2, E=8, x_per_slot=0, N=64,
+             K=64, bits=4, block_size=32, act=2, out=2, sc=1)
+    d.update(kw)
+    return lib.mnb_matmul_grouped(d["x"], d["ids"], d["packed_b"], d["scales"], d["zp"], d["y"], d["T"], d["S"],
+                                  d["E"], d["x_per_slot"], d["N"], d["K"], d["bits"], d["block_size"], d["act"],
+                                  d["out"], d["sc"], None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(S=0), mnb.MNB_ERR_INVALID_ARG), (dict(E=0), mnb.MNB_ERR_INVALID_ARG), (dict(T=-1), mnb.MNB_ERR_INVALID_ARG),
+    (dict(x_per_slot=2), mnb.MNB_ERR_INVALID_ARG), (dict(bits=3), mnb.MNB_ERR_INVALID_ARG),
+    (dict(act=5), mnb.MNB_ERR_INVALID_ARG), (dict(ids=0), mnb.MNB_ERR_INVALID_ARG),
+    (dict(ids=FAKE + 2), mnb.MNB_ERR_INVALID_ARG), (dict(x=FAKE + 8), mnb.MNB_ERR_INVALID_ARG),
+    (dict(packed_b=FAKE + 16), mnb.MNB_ERR_INVALID_ARG), (dict(act=0), mnb.MNB_ERR_UNSUPPORTED),
+    (dict(E=1025), mnb.MNB_ERR_UNSUPPORTED), (dict(T=4097, S=1), mnb.MNB_ERR_UNSUPPORTED),
+    (dict(T=1 << 40, S=1 << 30), mnb.MNB_ERR_UNSUPPORTED), (dict(T=2048, S=3), mnb.MNB_ERR_UNSUPPORTED),
+    (dict(T=0, x=0, y=0), mnb.MNB_OK),
+])
+def test_grouped_rejects_invalid_arguments_on_the_host(lib, kw, want):
+    assert _grouped(lib, **kw) == want
+
+
+def _host_io(lib, **kw):
+    a = mnb.MatmulArgs()
+    d = dict(x=FAKE, packed_b=FAKE, scales=FAKE, y=FAKE, M=1, N=64, K=64, bits=4, block_size=32,
+             act_dtype=2, out_dtype=2, scale_dtype=1, bias_dtype=0, accuracy_level=0, kernel=0)
+    d.update(kw)
+    for k, v in d.items():
+        setattr(a, k, v)
+    return lib.mnb_matmul_host_io(ctypes.byref(a))
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(bits=3), mnb.MNB_ERR_INVALID_ARG), (dict(act_dtype=9), mnb.MNB_ERR_INVALID_ARG),
+    (dict(M=-1), mnb.MNB_ERR_INVALID_ARG), (dict(x=0), mnb.MNB_ERR_INVALID_ARG), (dict(y=0), mnb.MNB_ERR_INVALID_ARG),
+    (dict(x=FAKE + 4), mnb.MNB_ERR_INVALID_ARG), (dict(y=FAKE + 8), mnb.MNB_ERR_INVALID_ARG),
+    (dict(M=17, K=1 << 18), mnb.MNB_ERR_NO_MEM),                   # 17 x 256 Ki bf16 > 8 MiB
+    (dict(M=9, K=1 << 18, act_dtype=0), mnb.MNB_ERR_NO_MEM),       # f32 X counts 4 bytes per element
+    (dict(M=0, x=0, y=0), mnb.MNB_OK),
+])
+def test_host_io_rejects_invalid_arguments_on_the_host(lib, kw, want):
+    assert _host_io(lib, **kw) == want
+    assert lib.mnb_matmul_host_io(None) == mnb.MNB_ERR_INVALID_ARG
