@@ -11,17 +11,18 @@
 // src/thunk/ops/quant.rs, exec_dequant_grouped_mat_mul_gguf).
 //
 // One launch covers every expert with no host round trip.  CTA (x, y) owns
-// row tile x / C (K-split x % C) of a set of experts: it finds the experts
-// present in ids once, then for the y-th, (y + G)-th, ... of them in
+// row tile x / C (K-split x % C) of a set of experts.  It finds the experts
+// present in ids once; then, for the y-th, (y + G)-th, ... of them in
 // ascending order (G = gridDim.y, chosen on the host so the grid fills the
-// GPU about twice) gathers that expert's (t, s) pairs in order in shared
-// memory and runs the decode GEMV tile of gemv_mma.cuh on them, a chunk of
-// pairs at a time (the pairs are gathered inside the first pass, after its
-// weight loads are issued, so the gathering hides under the load latency) (at most the MMA's 8 or 16 rows; fewer when the staged
-// activation rows would not fit three CTAs per SM).  Doing several experts per CTA amortises the routing and
-// keeps every CTA streaming weights.  Only active experts' weights are read.
-// Pairs whose expert id is out of range belong to no group: their Y rows are
-// not written and the device status word reports MNB_ERR_INVALID_ARG.
+// GPU about twice), it runs the decode GEMV tile of gemv_mma.cuh on that
+// expert's (t, s) pairs, a chunk of pairs per pass.  A chunk is at most the
+// MMA's 8 or 16 rows, fewer when the staged activation rows would not fit
+// three CTAs per SM.  The pairs are gathered, in order, into shared memory
+// inside the first pass, after its weight loads are issued, so the
+// gathering hides under the load latency.  Only active experts' weights are
+// read.  Pairs whose expert id is out of range belong to no group: their Y
+// rows are not written and the device status word reports
+// MNB_ERR_INVALID_ARG.
 #pragma once
 
 #include "gemv_mma.cuh"
