@@ -10,11 +10,20 @@ grouped mixture-of-experts decode GEMV (``moe``) as secondary objects.
 
 A step is one mnb_matmul call over one batch (the decode step of one
 projection).  Weights are rotated over enough distinct copies that every
-step streams them from HBM (copies x bytes >= 3 x L2).  Steps are replayed
-from a CUDA graph (one graph node per call, as a serving loop would) and
-timed with CUDA events on the launching stream, with a barrier and a device
-synchronise on both sides.  Under torchrun each rank runs its own replica
+step streams them from HBM (copies x bytes >= 3 x L2).  The timed steps are
+captured into CUDA graphs (all of them in one graph up to 2048 steps; graphs
+of 1024 beyond), one kernel node per call as a serving loop would launch
+them.  A GPU spin kernel is queued just before the start event, so the host
+has submitted every graph before the device reaches the timed region, which
+then holds device time only, at any step count.  Timing uses CUDA events on
+the launching stream with a barrier and a device synchronise on both sides.
+Clocks and throttle reasons are sampled read-only through NVML in-process
+around the timed region.  Under torchrun each rank runs its own replica
 (weak scaling, no data-path collective); the time is the max over ranks.
+
+The default run also reports, as secondary objects with their own roofline,
+the 8-bit K=11008 decode (``int8_k11008``) and the 2-bit M=8 batch
+(``int2_m8``).
 
 The ``e2e`` object times the same steps through mnb_matmul_host_io: X starts
 in pinned host memory and Y ends there, moved by the library's kernels
@@ -31,7 +40,6 @@ import json
 import math
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -78,56 +86,93 @@ def metric_of(w: wl.Workload):
 # ---- clocks ----------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Read-only NVML sampling of the SM clock and the clock-event (throttle)
+    reasons in a background thread, through the driver's libnvidia-ml (ctypes,
+    no Python NVML package needed).  Nothing is ever set."""
 
-    def __init__(self, device_index: int):
-        self.dev = str(device_index)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int, period_s: float = 0.0005):
+        import ctypes
+        import threading
+        self.period = period_s
+        self.samples = []
+        self.err = None
+        self._stop = threading.Event()
+        self._thread = None
+        self.lib = None
+        self.handle = None
         try:
-            import torch
-            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
-            self.dev = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
-        except Exception:
-            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
-            if vis:
-                self.dev = vis.split(",")[device_index]
-        self.proc = None
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            handle = ctypes.c_void_p()
+            uuid = None
+            try:
+                import torch
+                u = str(torch.cuda.get_device_properties(device_index).uuid)
+                uuid = u if u.startswith("GPU-") else "GPU-" + u
+            except Exception:
+                uuid = None
+            if uuid is None or lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(handle)) != 0:
+                if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device_index), ctypes.byref(handle)) != 0:
+                    raise OSError("no NVML handle")
+            self.lib, self.handle = lib, handle
+            self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint()
+            self.sm_max = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0 \
+                else None
+        except (OSError, AttributeError) as e:
+            self.err = str(e) or type(e).__name__
+
+    def _read(self):
+        import ctypes
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) != 0:
+            return None
+        if self._reasons_fn(self.handle, ctypes.byref(rs)) != 0:
+            rs.value = 0
+        return (time.perf_counter(), float(clk.value), int(rs.value))
+
+    def _loop(self):
+        while not self._stop.is_set():
+            s = self._read()
+            if s is not None:
+                self.samples.append(s)
+            time.sleep(self.period)
 
     def start(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except (OSError, ValueError):
-            self.proc = None
+        import threading
+        if self.lib is None:
+            return
+        s = self._read()
+        if s is not None:
+            self.samples.append(s)
+        self._thread = threading.Thread(target=self._loop, daemon=True)
+        self._thread.start()
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, smax, reasons, n = [], None, set(), 0
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax = float(parts[2])
-            except ValueError:
-                continue
-            n += 1
-            for name, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
+        if self.lib is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [f"NVML unavailable: {self.err}"],
+                    "samples": 0, "source": "nvml"}
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join()
+        s = self._read()
+        if s is not None:
+            self.samples.append(s)
+        sm = [c for _, c, _ in self.samples]
+        reasons = set()
+        for _, _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": n}
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.sm_max,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "sm_mhz_min": min(sm) if sm else None,
+                "source": "nvml, in-process, from before the pre-spin to after the timed region"}
 
 
 # ---- CPU oracle timing -----------------------------------------------------
@@ -239,37 +284,43 @@ def run_ours(args):
 
     flags = 0 if args.no_pdl else mnb.MNB_FLAG_PDL
 
-    def replay_timed(call, R, steps, warmup, stream):
-        """Warm up, capture R calls (call(i) for i < R) in a CUDA graph, replay it
-        `warmup` steps untimed and `steps` steps timed with CUDA events on
-        `stream`, barrier + synchronise on both sides.  Returns (seconds, clocks,
-        full replays)."""
+    def replay_timed(call, steps, warmup, stream, per_graph=None):
+        """Run `warmup` untimed steps, then time exactly `steps` steps with CUDA
+        events on `stream`, barrier + synchronise on both sides.  Steps are
+        captured into CUDA graphs of G calls (G = steps when steps <= 2048) so
+        that the host launches a handful of graphs at most; a GPU spin kernel
+        queued just before the start event holds the device while the host
+        submits them, so the timed region holds device work only.  Returns
+        (seconds, clocks)."""
+        G = per_graph or (steps if steps <= 2048 else 1024)
         with torch.cuda.stream(stream):
-            for i in range(R):
+            for i in range(min(G, 64)):
                 call(i)
         torch.cuda.synchronize()
 
-        def capture(n):
+        def capture(n, first=0):
             gr = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gr, stream=stream):
                 for i in range(n):
-                    call(i)
+                    call(first + i)
             return gr
 
-        g = capture(R)
-        rem = steps % R
-        g_rem = capture(rem) if rem else None
-        reps = steps // R
+        g = capture(G)
+        reps, rem = divmod(steps, G)
+        g_rem = capture(rem, reps * G) if rem else None
+        wreps, wrem = divmod(warmup, G)
+        with torch.cuda.stream(stream):
+            for _ in range(wreps):
+                g.replay()
+            if wrem:
+                capture(wrem).replay()
+        barrier()
         clocks = ClockSampler(local)
         clocks.start()
-        with torch.cuda.stream(stream):
-            for _ in range(warmup // R):
-                g.replay()
-            for i in range(warmup % R):
-                call(i)
-        barrier()
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        spin_ms = 3.0 + 0.05 * (reps + 1)
         with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(spin_ms * 2.2e6))
             ev0.record(stream)
             for _ in range(reps):
                 g.replay()
@@ -278,7 +329,7 @@ def run_ours(args):
             ev1.record(stream)
         barrier()
         ck = clocks.stop()
-        return max_over_ranks(ev0.elapsed_time(ev1) / 1e3, dist), ck, reps
+        return max_over_ranks(ev0.elapsed_time(ev1) / 1e3, dist), ck
 
     def measure(w: wl.Workload, steps: int, warmup: int, kernel: str, want_e2e: bool, acc: int = 0):
         data = wl.generate(w)
@@ -305,31 +356,32 @@ def run_ours(args):
         yb = torch.empty((w.M, w.N), dtype=TORCH_DT[w.out_dtype], device="cuda")
         stream = torch.cuda.Stream()
 
-        def call(i, xin=None, yout=None):
+        def call(i):
             pb, s, zp = copies[i % R]
-            mnb.mnb_matmul_ex(x if xin is None else xin, pb, s, zp, yb if yout is None else yout, w.M, w.N,
-                              w.K, w.bits, w.bs, w.act_dtype, w.out_dtype, w.scale_dtype, kernel=kernel,
-                              stream=stream, flags=flags, accuracy_level=acc, workspace=ws)
+            mnb.mnb_matmul_ex(x, pb, s, zp, yb, w.M, w.N, w.K, w.bits, w.bs, w.act_dtype, w.out_dtype,
+                              w.scale_dtype, kernel=kernel, stream=stream, flags=flags, accuracy_level=acc,
+                              workspace=ws)
 
-        t, ck, reps = replay_timed(call, R, steps, warmup, stream)
-        steps_eff = steps
+        t, ck = replay_timed(call, steps, warmup, stream)
         unit, per_step = metric_of(w)
-        value = whole_job_value(world, steps_eff, per_step, t)
-        per_launch_s = t / steps_eff
+        value = whole_job_value(world, steps, per_step, t)
+        per_launch_s = t / steps
         kernels_per_step = 2 if acc == 4 else 1  # accuracy level 4: activation quantisation + GEMV
-        out = {"value": value, "unit": unit, "steps": steps_eff, "ms_per_step": per_launch_s * 1e3,
-               "kernel": chosen, "clocks": ck, "weight_copies": R, "launches": steps_eff * kernels_per_step}
+        out = {"workload": w.name, "value": value, "unit": unit, "steps": steps, "ms_per_step": per_launch_s * 1e3,
+               "kernel": chosen, "clocks": ck, "weight_copies": R, "launches": steps * kernels_per_step}
         if unit == "GB/s":
             peak = pk["hbm_gbs"]
             out["roofline"] = {"bound": "hbm", "achieved": per_step / per_launch_s, "peak": peak, "unit": "GB/s",
                                "frac": per_step / per_launch_s / peak,
                                "traffic": traffic_for(f"{chosen}:{w.name}"),
+                               "algorithmic_bytes": w.algorithmic_bytes(),
                                "peak_source": f"{pk_src} hbm_gbs"}
         else:
             peak = pk["bf16_tflops"]
             out["roofline"] = {"bound": "tensor", "achieved": per_step / per_launch_s, "peak": peak,
                                "unit": "TFLOP/s", "frac": per_step / per_launch_s / peak,
                                "traffic": traffic_for(f"{chosen}:{w.name}"),
+                               "algorithmic_bytes": w.algorithmic_bytes(), "flops": w.flops(),
                                "peak_source": f"{pk_src} bf16_tflops (burst)"}
         if want_e2e:
             # End to end through the C ABI with HOST buffers: X is read from pinned host memory and Y is
@@ -343,31 +395,14 @@ def run_ours(args):
                                        w.out_dtype, w.scale_dtype, kernel=kernel, stream=stream, flags=flags,
                                        accuracy_level=acc, workspace=ws)
 
-            with torch.cuda.stream(stream):
-                for i in range(R):
-                    call_host(i)
-            torch.cuda.synchronize()
-            ge = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(ge, stream=stream):
-                for i in range(R):
-                    call_host(i)
-            with torch.cuda.stream(stream):
-                ge.replay()
-            barrier()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                e0.record(stream)
-                for _ in range(max(1, reps)):
-                    ge.replay()
-                e1.record(stream)
-            barrier()
-            te = max_over_ranks(e0.elapsed_time(e1) / 1e3, dist)
-            out["e2e"] = {"value": whole_job_value(world, max(1, reps) * R, per_step, te), "unit": unit,
+            te, cke = replay_timed(call_host, steps, warmup, stream)
+            out["e2e"] = {"value": whole_job_value(world, steps, per_step, te), "unit": unit,
                           "h2d_bytes_per_step": x.numel() * x.element_size(),
                           "d2h_bytes_per_step": yb.numel() * yb.element_size(),
+                          "ms_per_step": te / steps * 1e3, "clocks": cke,
                           "mode": "CUDA graph of mnb_matmul_host_io per step: X read from pinned host memory, "
                                   "Y written to pinned host memory, both by the library's kernels"}
-            out["e2e_launches"] = max(1, reps) * R * (kernels_per_step + 1)  # + the X fetch kernel
+            out["e2e_launches"] = steps * (kernels_per_step + 1)  # + the X fetch kernel
         return out, data
 
     def measure_moe(w: wl.MoeWorkload, steps: int, warmup: int):
@@ -399,16 +434,16 @@ def run_ours(args):
             mnb.mnb_matmul_grouped(x, ids, pb, s, zp, y, w.T, w.S, w.E, w.N, w.K, w.bits, w.bs, w.act_dtype,
                                    w.out_dtype, w.scale_dtype, x_per_slot=w.x_per_slot, stream=stream)
 
-        t, ck, _ = replay_timed(call, R, steps, warmup, stream)
+        t, ck = replay_timed(call, steps, warmup, stream)
         per_step = step_bytes / 1e9
         per_launch_s = t / steps
         achieved = per_step / per_launch_s
         return {"workload": w.name, "value": whole_job_value(world, steps, per_step, t), "unit": "GB/s",
-                "kernel": "gemv_moe", "ms_per_step": per_launch_s * 1e3,
+                "kernel": "gemv_moe", "ms_per_step": per_launch_s * 1e3, "steps": steps,
                 "experts_active": int(len(np.unique(d["ids"]))), "experts": w.E, "tokens": w.T, "top_k": w.S,
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                              "frac": achieved / pk["hbm_gbs"], "traffic": traffic_for(f"gemv_moe:{w.name}"),
-                             "peak_source": f"{pk_src} hbm_gbs"},
+                             "algorithmic_bytes": step_bytes, "peak_source": f"{pk_src} hbm_gbs"},
                 "clocks": ck, "weight_copies": R}, steps
 
     w = wl.config(args.config)
@@ -424,23 +459,28 @@ def run_ours(args):
                    "zero_points": w.zp is not None, "kernel": main["kernel"],
                    "accuracy_level": args.accuracy_level,
                    "l2": f"inputs larger than L2: {main['weight_copies']} rotating weight copies (>= 3 x L2)",
-                   "launch": "CUDA graph replay, one kernel per step"},
+                   "launch": "CUDA graphs holding all timed steps (one kernel node per step), queued behind a "
+                             "GPU spin so the timed region holds device time only"},
         "roofline": main["roofline"], "clocks": main["clocks"], "e2e": main["e2e"],
         "gpu_launches": main["launches"] + main.get("e2e_launches", 0),
     }
-    if args.config == 1 and not args.no_secondary:
-        w2 = wl.config(4)
-        sec, _ = measure(w2, max(20, args.steps // 20), max(3, args.warmup // 20), "auto", False)
-        res["m512"] = {"workload": w2.name, "value": sec["value"], "unit": sec["unit"], "kernel": sec["kernel"],
-                       "ms_per_step": sec["ms_per_step"], "roofline": sec["roofline"], "clocks": sec["clocks"]}
+
+    def secondary(key, wk, steps, warmup, acc=0, extra=None):
+        sec, _ = measure(wk, steps, warmup, "auto", False, acc)
+        obj = {"workload": wk.name, "value": sec["value"], "unit": sec["unit"], "kernel": sec["kernel"],
+               "steps": sec["steps"], "ms_per_step": sec["ms_per_step"], "roofline": sec["roofline"],
+               "clocks": sec["clocks"]}
+        obj.update(extra or {})
+        res[key] = obj
         res["gpu_launches"] += sec["launches"]
+
     if args.config == 1 and args.accuracy_level == 0 and not args.no_secondary:
-        sec, _ = measure(w, max(20, args.steps // 4), max(3, args.warmup // 4), "auto", False, 4)
-        res["a8"] = {"workload": w.name, "accuracy_level": 4, "value": sec["value"], "unit": sec["unit"],
-                     "kernel": sec["kernel"], "ms_per_step": sec["ms_per_step"], "roofline": sec["roofline"],
-                     "clocks": sec["clocks"], "launches_per_step": 2}
-        res["gpu_launches"] += sec["launches"]
-    if args.config == 1 and args.accuracy_level == 0 and not args.no_secondary:
+        sw = max(3, args.warmup // 4)
+        secondary("m512", wl.config(4), max(20, args.steps // 20), max(3, args.warmup // 20))
+        secondary("int8_k11008", wl.config(2), max(20, args.steps // 2), sw)
+        secondary("int2_m8", wl.config(3), max(20, args.steps // 2), sw)
+        secondary("a8", w, max(20, args.steps // 4), sw, acc=4,
+                  extra={"accuracy_level": 4, "launches_per_step": 2})
         moe, n = measure_moe(wl.MOE_CONFIGS[0], max(20, args.steps // 10), max(3, args.warmup // 10))
         res["moe"] = moe
         res["gpu_launches"] += n

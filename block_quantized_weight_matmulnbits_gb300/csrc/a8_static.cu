@@ -2,7 +2,6 @@
 // the quantised activations and block scales go to a file-scope device array
 // instead of memory the caller allocates.  The library allocates nothing.
 #include <cstring>
-#include <mutex>
 
 #include "mnb.h"
 #include "mnb_internal.h"
@@ -10,29 +9,20 @@
 namespace {
 
 constexpr size_t kScratchBytes = MNB_A8_STATIC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 // One per device (a __device__ variable exists once in every context).
 static __device__ __align__(256) uint8_t g_a8_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch[kMaxDevices] = {};
+// In host code g_a8_scratch names a host-side stand-in, not device memory:
+// kernels get the device address that cudaGetSymbolAddress reports for the
+// current context (the device current at the call).
+cudaError_t lookup_scratch(void** p) { return cudaGetSymbolAddress(p, g_a8_scratch); }
+mnb::SymbolCache g_scratch_cache;
 
-// Address of this device's array, looked up once per device.
+// Address of the current context's array: looked up on the first call in a
+// context (device), then cached per context.
 cudaError_t scratch_for_current_device(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (g_scratch[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_a8_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch[dev] = p;
-    }
-    *out = g_scratch[dev];
-    return cudaSuccess;
+    return mnb::cached_symbol_address(g_scratch_cache, lookup_scratch, out);
 }
 
 }  // namespace

@@ -37,10 +37,13 @@ int64_t env_int(const char* name, int64_t dflt) {
 // One status word per device, in device memory owned by the library.
 __device__ int g_status_word;
 
+cudaError_t lookup_status_word(void** p) { return cudaGetSymbolAddress(p, g_status_word); }
+SymbolCache g_status_cache;
+
 struct PerDevice {
     bool init = false;
     DeviceInfo info{};
-    int* status = nullptr;  // device address of g_status_word
+    int* status = nullptr;  // device address of g_status_word in the current context
 };
 
 std::mutex g_mu;
@@ -63,12 +66,14 @@ PerDevice* per_device() {
         if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return nullptr;
         di.smem_optin = (size_t)v;
-        void* addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return nullptr;
-        pd.status = static_cast<int*>(addr);
         pd.info = di;
         pd.init = true;
     }
+    // The address belongs to the current context, not to the device index:
+    // after a device reset the array may live elsewhere.
+    void* addr = nullptr;
+    if (cached_symbol_address(g_status_cache, lookup_status_word, &addr) != cudaSuccess) return nullptr;
+    pd.status = static_cast<int*>(addr);
     return &pd;
 }
 
@@ -93,6 +98,61 @@ mnb_status from_cuda(cudaError_t e) {
 }
 
 }  // namespace
+
+bool current_context_id(unsigned long long* id) {
+    // cuCtxGetCurrent / cuCtxGetId through the runtime's driver entry points,
+    // so the library needs no link-time dependency on libcuda.
+    typedef int (*GetCurrentFn)(void**);
+    typedef int (*GetIdFn)(void*, unsigned long long*);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(f);
+        cudaGetLastError();
+    });
+    if (!get_current || !get_id) return false;
+    void* ctx = nullptr;
+    if (get_current(&ctx) != 0 || ctx == nullptr) return false;
+    return get_id(ctx, id) == 0;
+}
+
+cudaError_t cached_symbol_address(SymbolCache& cache, cudaError_t (*lookup)(void**), void** out) {
+    unsigned long long id = 0;
+    if (!current_context_id(&id)) {
+        // No context yet: the lookup creates the primary context.
+        void* p = nullptr;
+        const cudaError_t e = lookup(&p);
+        if (e != cudaSuccess) return e;
+        if (!current_context_id(&id)) {  // cannot key the cache: use the fresh address
+            *out = p;
+            return cudaSuccess;
+        }
+    }
+    std::lock_guard<std::mutex> lk(cache.mu);
+    for (int i = 0; i < cache.used; ++i) {
+        if (cache.ctx[i] == id) {
+            *out = cache.addr[i];
+            return cudaSuccess;
+        }
+    }
+    void* p = nullptr;
+    const cudaError_t e = lookup(&p);
+    if (e != cudaSuccess) return e;
+    const int slot = cache.used < SymbolCache::kSlots ? cache.used++ : (int)(id % SymbolCache::kSlots);
+    cache.ctx[slot] = id;
+    cache.addr[slot] = p;
+    *out = p;
+    return cudaSuccess;
+}
 
 // Test hook: MNB_FAIL_LAUNCH=1 makes every launch report a CUDA error without
 // launching anything (exercises the error path on the host, no GPU fault).

@@ -221,13 +221,13 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : 1)
             if (j < tpw && t0 + j < cta_t1) wv[j] = ldg_stream(wrow + (t0 + j) * kTileBytes);
     };
     load_round(0);
-    if (pdl) griddep_launch_dependents();
 
     // ---- zero points and weight scales of the CTA's (row, block)s ----
     if (p.scale_dtype == kF32) stage_entries<float>(p, L, rt, kb0, kb_cta, kbs, stage);
     else stage_entries<uint16_t>(p, L, rt, kb0, kb_cta, kbs, stage);
 
     griddep_wait();  // the workspace is written by the quantisation kernel
+    if (pdl) griddep_launch_dependents();  // after the wait: at most two chained kernels overlap
 
     // ---- activation scales and int8 words of this CTA's depths ----
     for (int it = tid; it < M * kb_cta; it += kThreads) {

@@ -270,7 +270,6 @@ __device__ __forceinline__ void gemv_tile(const MatmulParams& p, const Geom& geo
             if (j < tpw && t0 + j < cta_t1) wv[j] = ldg_stream(wrow + (t0 + j) * kTileBytes);
     };
     load_round(0);
-    if (pdl) griddep_launch_dependents();  // the next kernel may start filling SMs as CTAs retire
 
     // ---- 2. per (row, block) subtraction constant and scale; entry (r, j) at r * kbs + j ----
     auto decode_run = [&](int r, int run, int64_t n, int64_t kbr, bool vec16, bool vec32, bool zv,
@@ -339,7 +338,13 @@ __device__ __forceinline__ void gemv_tile(const MatmulParams& p, const Geom& geo
             decode_run(r, run, rt * 16 + r, kb0 + (int64_t)run * 8, false, false, false, sv0, sv1, 0);
         }
     }
-    if (pdl) griddep_wait();  // X (and Y) may belong to the previous kernel on the stream
+    if (pdl) {
+        griddep_wait();  // X (and Y) may belong to the previous kernel on the stream
+        // Only now may the next kernel launch: at most two kernels of a
+        // programmatic chain overlap (this one, once its predecessor is
+        // complete, and its successor's pre-wait part).
+        griddep_launch_dependents();
+    }
     rows.prepare();
     const int M = rows.M;
 

@@ -123,7 +123,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pers_kernel(MatmulParams p, 
         if (q + 1 < n_my) copy_raw(rbeg + q + 1, (q + 1) % kDepth);
         cp_async_commit();
     }
-    if (pdl) griddep_launch_dependents();
 
     // ---- decode a landed raw slot into the table: thread -> (row, run of kRun blocks) ----
     const int items = 16 * geo.runs;
@@ -167,7 +166,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pers_kernel(MatmulParams p, 
         }
     };
 
-    if (pdl) griddep_wait();  // X (and Y) may belong to the previous kernel on the stream
+    if (pdl) {
+        griddep_wait();  // X (and Y) may belong to the previous kernel on the stream
+        griddep_launch_dependents();  // after the wait: at most two chained kernels overlap
+    }
 
     // ---- activations (B fragments) of all K, staged once: item (m, k-step S) = 32 bytes ----
     {

@@ -7,6 +7,13 @@
 // scale and zero point follow g_idx[k] while the code keeps its block
 // position, MatMulNBitsKernel::dequantize_weight), then contracted with fp32
 // FMAs.  The bias is added after the product (MatMulNBitsKernel::execute).
+//
+// g_idx values outside [0, KB) are an error on the page (dequantize_weight
+// rejects them).  Here g_idx lives on the device, so the kernel checks each
+// value before using it: a bad value is never used as an index, the CTA that
+// met it writes none of its outputs, and the device status word becomes
+// MNB_ERR_INVALID_ARG.  Every output depends on every depth, so every CTA
+// meets the bad value and Y is left entirely unwritten.
 #include "mnb_internal.h"
 
 namespace mnb {
@@ -19,6 +26,7 @@ constexpr int TK = 32;   // depth per step
 __global__ __launch_bounds__(256) void generic_kernel(MatmulParams p) {
     __shared__ float ws[TN][TK + 1];
     __shared__ float xs[TM][TK + 1];
+    __shared__ int bad_gidx;
     const Layout& L = p.L;
     const int tid = threadIdx.x;
     const int64_t n0 = (int64_t)blockIdx.x * TN;
@@ -27,6 +35,8 @@ __global__ __launch_bounds__(256) void generic_kernel(MatmulParams p) {
     const int mg = tid / TN;        // 0..3 -> activation rows mg*4 .. mg*4+3
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const int mask = code_mask(L.bits);
+    if (tid == 0) bad_gidx = 0;
+    __syncthreads();
 
     for (int64_t k0 = 0; k0 < L.K; k0 += TK) {
         for (int i = tid; i < TN * TK; i += 256) {
@@ -37,9 +47,13 @@ __global__ __launch_bounds__(256) void generic_kernel(MatmulParams p) {
                 const int64_t bit = L.bit_of(n, k);
                 const int q = (p.packed[bit >> 3] >> (bit & 7)) & mask;
                 const int64_t g = p.g_idx ? (int64_t)p.g_idx[k] : k / L.bs;
-                const int z = load_zp(p.zp, L, n, g);
-                const float s = load_f32(p.scales, n * L.KB + g, p.scale_dtype);
-                w = __fmul_rn(__fsub_rn((float)q, (float)z), s);
+                if (g >= 0 && g < L.KB) {
+                    const int z = load_zp(p.zp, L, n, g);
+                    const float s = load_f32(p.scales, n * L.KB + g, p.scale_dtype);
+                    w = __fmul_rn(__fsub_rn((float)q, (float)z), s);
+                } else {
+                    bad_gidx = 1;  // never used as an index
+                }
             }
             ws[r][c] = w;
         }
@@ -56,6 +70,11 @@ __global__ __launch_bounds__(256) void generic_kernel(MatmulParams p) {
             for (int j = 0; j < 4; ++j) acc[j] = fmaf(xs[mg * 4 + j][c], w, acc[j]);
         }
         __syncthreads();
+    }
+    // bad_gidx was written before the loop's last barrier
+    if (bad_gidx) {
+        if (tid == 0) set_status(p.status, 1 /* MNB_ERR_INVALID_ARG */);
+        return;
     }
     const int64_t n = n0 + nl;
     if (n >= L.N) return;

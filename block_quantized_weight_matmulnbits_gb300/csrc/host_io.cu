@@ -29,23 +29,23 @@ constexpr int kFetchThreads = 256;
 static __device__ __align__(256) uint8_t g_host_x[2][kXBytes];
 
 std::mutex g_mu;
-void* g_x_dev[kMaxDevices] = {};
 unsigned g_calls[kMaxDevices] = {};
 
-// The staging buffer of this call: the two alternate call by call.
+cudaError_t lookup_x(void** p) { return cudaGetSymbolAddress(p, g_host_x); }
+mnb::SymbolCache g_x_cache;
+
+// The staging buffer of this call: the two alternate call by call.  The
+// arrays' address is looked up per context (see mnb::cached_symbol_address).
 cudaError_t x_buffer_for_current_device(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    void* base = nullptr;
+    e = mnb::cached_symbol_address(g_x_cache, lookup_x, &base);
+    if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (g_x_dev[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_host_x);
-        if (e != cudaSuccess) return e;
-        g_x_dev[dev] = p;
-    }
-    *out = static_cast<uint8_t*>(g_x_dev[dev]) + (size_t)(g_calls[dev]++ & 1u) * kXBytes;
+    *out = static_cast<uint8_t*>(base) + (size_t)(g_calls[dev]++ & 1u) * kXBytes;
     return cudaSuccess;
 }
 

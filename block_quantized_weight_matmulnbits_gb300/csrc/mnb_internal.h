@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cstddef>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "mnb_common.cuh"
@@ -68,5 +69,24 @@ int* device_status_word();
 
 // MNB_FAIL_LAUNCH=1: entry points report MNB_ERR_CUDA instead of launching.
 bool inject_launch_failure();
+
+// Identifier of the CUDA context current on the calling thread (the driver's
+// context id, unique for the life of the process, so a context created after
+// a device reset never matches an older one).  False when no context is
+// current or the driver cannot say.
+bool current_context_id(unsigned long long* id);
+
+// Device address of a file-scope __device__ array, cached per CUDA context.
+// `lookup` (defined in the .cu file that owns the array) calls
+// cudaGetSymbolAddress on it.  The first call in a context performs the
+// lookup, which may load the module: make it outside stream capture.
+struct SymbolCache {
+    static constexpr int kSlots = 32;
+    std::mutex mu;
+    unsigned long long ctx[kSlots] = {};
+    void* addr[kSlots] = {};
+    int used = 0;
+};
+cudaError_t cached_symbol_address(SymbolCache& cache, cudaError_t (*lookup)(void**), void** out);
 
 }  // namespace mnb

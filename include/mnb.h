@@ -206,8 +206,11 @@ MNB_API mnb_status mnb_quantize_activations(const void* x, int8_t* qa, float* sa
  *   need more return MNB_ERR_NO_MEM without launching.  Nothing in it needs
  *   to start at zero: the quantisation kernel writes every byte the GEMV
  *   reads.
- *   Set-up: the first call on a device looks the array up
- *   (cudaGetSymbolAddress); make that first call outside stream capture.
+ *   Set-up: the first call in a CUDA context (that is, on a device, with
+ *   that device current) looks the array's device address up with
+ *   cudaGetSymbolAddress and caches it for that context; make that first
+ *   call outside stream capture.  A context created later (after a device
+ *   reset, say) gets its own lookup.
  *   Concurrency: calls that overlap on the same device (different streams,
  *   threads or graphs in flight together) share the array and race; calls
  *   ordered on one stream are safe.
@@ -271,8 +274,9 @@ MNB_API mnb_status mnb_matmul_grouped(const void* x, const int32_t* ids, const v
  *   the addresses are used as given: under unified addressing the device
  *   address of page-locked memory is its host address.
  *   Limits: M*K*sizeof(act) > MNB_HOST_IO_X_BYTES returns MNB_ERR_NO_MEM
- *   without launching.  The first call on a device looks the arrays up
- *   (cudaGetSymbolAddress); make it outside stream capture.  Calls that
+ *   without launching.  The first call in a CUDA context looks the arrays'
+ *   device address up (cudaGetSymbolAddress) and caches it for that
+ *   context; make that first call outside stream capture.  Calls that
  *   overlap on one device (different streams, graphs in flight together)
  *   share the arrays and race; calls ordered on one stream are safe.
  * Returns the statuses of mnb_matmul_ex. */

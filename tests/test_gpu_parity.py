@@ -219,6 +219,43 @@ def test_bias_and_g_idx_generic(G, mnb):
     G.assert_within(P.y64(y), ref, mag, w.out_dtype, "g_idx+bias")
 
 
+@pytest.mark.parametrize("bad", ["one_past_end", "negative"])
+def test_g_idx_out_of_range_sets_status_and_writes_nothing(G, mnb, bad):
+    """A g_idx value outside [0, KB) is rejected as on the page
+    (MatMulNBitsKernel::dequantize_weight): the device status word becomes
+    MNB_ERR_INVALID_ARG and Y stays as it was.  The scale and zero-point
+    buffers carry one padding row before and after, so even an unchecked read
+    at the bad index would stay inside the allocation."""
+    bits, bs, N, K, M = 4, 16, 40, 64, 3
+    KB = K // bs
+    w = _w(M, N, K, bits, bs, DTYPES[0], True, 320)
+    P = G.Problem(w)
+    zp_row = P.zp.shape[1]
+    s_pad = torch.zeros((N + 2) * KB, dtype=P.s.dtype, device="cuda")
+    s_pad[KB:(N + 1) * KB] = P.s.reshape(-1)
+    z_pad = torch.zeros((N + 2) * zp_row, dtype=torch.uint8, device="cuda")
+    z_pad[zp_row:(N + 1) * zp_row] = P.zp.reshape(-1)
+    g = np.arange(K, dtype=np.int32) // bs
+    g[K // 2] = KB if bad == "one_past_end" else -1
+    sentinel = torch.full((M, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    y = sentinel.clone()
+    assert mnb.mnb_get_device_error() == 0
+    mnb.mnb_matmul_ex(P.x, P.packed, s_pad[KB:], z_pad[zp_row:], y, M, N, K, bits, bs, w.act_dtype,
+                      w.out_dtype, w.scale_dtype, g_idx=torch.from_numpy(g).cuda(), kernel="auto")
+    torch.cuda.synchronize()
+    assert mnb.mnb_get_device_error() == mnb.MNB_ERR_INVALID_ARG
+    assert torch.equal(y, sentinel)
+    # the next valid call is unaffected
+    g[K // 2] = (K // 2) // bs
+    y2 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    mnb.mnb_matmul_ex(P.x, P.packed, P.s, P.zp, y2, M, N, K, bits, bs, w.act_dtype, w.out_dtype,
+                      w.scale_dtype, g_idx=torch.from_numpy(g).cuda(), kernel="auto")
+    torch.cuda.synchronize()
+    assert mnb.mnb_get_device_error() == 0
+    ref, mag = P.oracle_full(g_idx=g)
+    G.assert_within(P.y64(y2), ref, mag, w.out_dtype, "g_idx after a rejected call")
+
+
 @pytest.mark.parametrize("kernel", ["gemv", "gemv_mma", "generic"])
 def test_bias_m1(G, mnb, kernel):
     w = _w(1, 100, 96, 4, 32, DTYPES[0], True, 310)

@@ -30,11 +30,16 @@ def test_static_scratch_matches_workspace_entry(mnb, oracle_mod, w):
     y_ref = P.y64(P.run(accuracy_level=4, workspace=ws))
     qa, sa = oracle_mod.quantize_act(P.x64.astype(np.float32), w.K, w.bs)
     _, mag = oracle_mod.matmul_a8(qa, sa, P.d["b"], P.s32, P.d["zp"], w.N, w.K, w.bits, w.bs)
+    y_ws = P.run(accuracy_level=4, workspace=ws)
     for call in range(2):  # two calls in a row reuse the same scratch
         y = torch.full((w.M, w.N), float("nan"), dtype=G.TORCH_DT[w.out_dtype], device="cuda")
         mnb.mnb_matmul_a8_static(P.x, P.packed, P.s, P.zp, y, w.M, w.N, w.K, w.bits, w.bs, w.act_dtype,
                                  w.out_dtype, w.scale_dtype)
         torch.cuda.synchronize()
+        # the same kernels on the same inputs: bit-identical to the workspace call
+        assert torch.equal(y.view(torch.int16 if y.element_size() == 2 else torch.int32),
+                           y_ws.view(torch.int16 if y_ws.element_size() == 2 else torch.int32)), \
+            f"static scratch call {call} differs from the workspace call"
         G.assert_within(P.y64(y), y_ref, mag, w.out_dtype, f"static scratch call {call}")
 
 
