@@ -154,6 +154,22 @@ cudaError_t cached_symbol_address(SymbolCache& cache, cudaError_t (*lookup)(void
     return cudaSuccess;
 }
 
+void wait_limits(uint32_t* limit, uint32_t* hint_ns) {
+    const int64_t n = env_int("MNB_WAIT_LIMIT", 0);
+    if (n > 0) {
+        *limit = (uint32_t)n;
+        *hint_ns = 0;
+        return;
+    }
+    // MNB_WAIT_MODE (tuning): 0 suspend with a time hint, 1 try_wait without a
+    // hint, 2 busy polling with test_wait; the limits keep every mode near two seconds.
+    switch (env_int("MNB_WAIT_MODE", 0)) {
+        case 1: *limit = 1u << 24; *hint_ns = 0; break;
+        case 2: *limit = 1u << 26; *hint_ns = kWaitPoll; break;
+        default: *limit = kWaitLimit; *hint_ns = kWaitHintNs; break;
+    }
+}
+
 // Test hook: MNB_FAIL_LAUNCH=1 makes every launch report a CUDA error without
 // launching anything (exercises the error path on the host, no GPU fault).
 bool inject_launch_failure() { return env_int("MNB_FAIL_LAUNCH", 0) == 1; }
@@ -301,6 +317,7 @@ mnb_status mnb_matmul_ex(const mnb_matmul_args* a) {
     p.workspace = a->workspace;
     p.workspace_bytes = a->workspace_bytes;
     p.flags = a->flags;
+    wait_limits(&p.wait_limit, &p.wait_hint_ns);
 
     mnb_kernel k = a->kernel;
     if (k == MNB_KERNEL_AUTO) {

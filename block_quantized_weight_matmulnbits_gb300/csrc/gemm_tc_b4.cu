@@ -1,14 +1,10 @@
-// Instantiation of the tcgen05 prefill GEMM for 4-bit codes (one
-// translation unit per code width keeps the build parallel).
-#include "gemm_ta.cuh"
+// Instantiation of the tcgen05 prefill GEMM for 4-bit codes (one translation
+// unit per code width keeps the build parallel).
+#include "gemm_bs.cuh"
 
 namespace mnb {
-cudaError_t launch_gemm_tc_b4(const MatmulParams& p, const gtc::TcGeom& geo, const gtc::Maps& m, cudaStream_t s) {
+cudaError_t launch_gemm_tc_b4(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s) {
     const bool bf = p.act_dtype == kBF16;
-    return bf ? gtc::launch<4, true>(p, geo, m, s) : gtc::launch<4, false>(p, geo, m, s);
-}
-cudaError_t launch_gemm_ta_b4(const MatmulParams& p, const gtc::TcGeom& geo, const gtc::Maps& m, cudaStream_t s) {
-    const bool bf = p.act_dtype == kBF16;
-    return bf ? gtc::launch_ta<4, true>(p, geo, m, s) : gtc::launch_ta<4, false>(p, geo, m, s);
+    return bf ? gbs::launch<4, true>(p, geo, m, s) : gbs::launch<4, false>(p, geo, m, s);
 }
 }  // namespace mnb

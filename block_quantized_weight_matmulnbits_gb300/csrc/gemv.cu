@@ -164,6 +164,7 @@ template <int BITS, int SPB_LOG>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(MatmulParams p, GemvGeom geo) {
     using U = Unpack<BITS>;
     const Layout& L = p.L;
+    if (blockIdx.x == 0 && threadIdx.x == 0) verify_header(p.packed_hdr, L, p.status);
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* ring = smem;                                               // [warps][slots][chunk]
     float* xs = reinterpret_cast<float*>(smem + geo.ring_bytes);        // permuted x'

@@ -424,6 +424,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : 1)
             store_f32(p.y, (int64_t)m * L.N + n, v, p.out_dtype);
         }
     }
+    if (blockIdx.x == 0 && tid == 0) verify_header(p.packed_hdr, L, p.status);
 }
 
 template <int BITS, int MT, int SPB_LOG>

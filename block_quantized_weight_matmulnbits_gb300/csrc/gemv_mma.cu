@@ -1,7 +1,13 @@
-// Host side of the small-batch tensor-core GEMV (kernel in gemv_mma.cuh).
+// Host side of the small-batch tensor-core GEMV: three schedules of the same
+// arithmetic (gemv_mma.cuh, one CTA per row tile; gemv_pers.cuh, a
+// persistent ring; gemv_stream.cuh, persistent with register prefetch).
+// MNB_GEMV_SCHED=stream|tile|pers forces one (MNB_GEMV_PERS=0/1 still
+// selects between the first two).
 #include <cstdlib>
+#include <cstring>
 
 #include "gemv_pers.cuh"
+#include "gemv_stream.cuh"
 
 namespace mnb {
 
@@ -11,6 +17,23 @@ cudaError_t launch_gemv_mma_b8(const MatmulParams& p, const gmma::Geom& geo, cud
 cudaError_t launch_gemv_pers_b2(const MatmulParams& p, const gpers::PGeom& geo, int grid, cudaStream_t s);
 cudaError_t launch_gemv_pers_b4(const MatmulParams& p, const gpers::PGeom& geo, int grid, cudaStream_t s);
 cudaError_t launch_gemv_pers_b8(const MatmulParams& p, const gpers::PGeom& geo, int grid, cudaStream_t s);
+cudaError_t launch_gemv_stream_b2(const MatmulParams& p, const gstr::SGeom& geo, cudaStream_t s);
+cudaError_t launch_gemv_stream_b4(const MatmulParams& p, const gstr::SGeom& geo, cudaStream_t s);
+cudaError_t launch_gemv_stream_b8(const MatmulParams& p, const gstr::SGeom& geo, cudaStream_t s);
+
+static const char* sched_env() {
+    const char* v = std::getenv("MNB_GEMV_SCHED");
+    return (v && *v) ? v : nullptr;
+}
+
+// The streaming schedule (opt-in with MNB_GEMV_SCHED=stream) takes every
+// shape with at least one K-unit per warp.
+static bool stream_ok(const MatmulParams& p, gstr::SGeom* out) {
+    const char* sc = sched_env();
+    if (!sc || std::strcmp(sc, "stream") != 0) return false;
+    const int sms = device_info().sm_count > 0 ? device_info().sm_count : 148;
+    return gstr::make_sgeom(p.L, p.M, p.M <= 8 ? 8 : 16, sms, device_info().smem_optin, out);
+}
 
 // The persistent schedule (gemv_pers.cuh) takes the shapes it was built for:
 // a row tile's K in one pass of 16 warps, enough row tiles to fill every SM at
@@ -20,7 +43,13 @@ cudaError_t launch_gemv_pers_b8(const MatmulParams& p, const gpers::PGeom& geo, 
 // 4096 x 14336 batch), so it is the default for M >= 2.  MNB_GEMV_PERS=0 / 1
 // forces either schedule.
 static bool pers_ok(const MatmulParams& p, gpers::PGeom* out, int* grid) {
-    const char* env = std::getenv("MNB_GEMV_PERS");
+    const char* sc = sched_env();
+    if (sc && std::strcmp(sc, "pers") == 0) {
+        // forced below like MNB_GEMV_PERS=1
+    } else if (sc) {
+        return false;
+    }
+    const char* env = sc ? "1" : std::getenv("MNB_GEMV_PERS");
     if (env && env[0] == '0') return false;
     if (!(env && env[0] == '1') && p.M < 2) return false;
     const Layout& L = p.L;
@@ -60,6 +89,15 @@ bool gemv_mma_supported(const MatmulParams& p) {
 }
 
 cudaError_t launch_gemv_mma(const MatmulParams& p, cudaStream_t s) {
+    gstr::SGeom sg;
+    if (stream_ok(p, &sg)) {
+        switch (p.L.bits) {
+            case 2: return launch_gemv_stream_b2(p, sg, s);
+            case 4: return launch_gemv_stream_b4(p, sg, s);
+            case 8: return launch_gemv_stream_b8(p, sg, s);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     gpers::PGeom pg;
     int grid = 0;
     if (pers_ok(p, &pg, &grid)) {

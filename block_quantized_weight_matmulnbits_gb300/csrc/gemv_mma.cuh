@@ -525,6 +525,7 @@ __global__ void __launch_bounds__(kThreads, BITS == 8 ? 4 : 3) gemv_mma_kernel(M
     const int64_t rt = blockIdx.x / geo.C;
     DenseRows rows{(int)p.M};
     gemv_tile<BITS, BF16X, MT, SPB_LOG>(p, geo, pdl, rt, (int)(blockIdx.x - rt * geo.C), rows, smem);
+    if (blockIdx.x == 0 && threadIdx.x == 0) verify_header(p.packed_hdr, p.L, p.status);
 }
 
 template <int BITS, bool BF16X, int MT, int SPB_LOG>

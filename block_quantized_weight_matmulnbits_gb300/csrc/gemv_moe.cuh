@@ -161,6 +161,8 @@ __global__ void __launch_bounds__(kThreads, BITS == 8 ? 4 : 3) gemv_moe_kernel(M
             gmma::gemv_tile<BITS, BF16X, MT, SPB_LOG>(q, geo, 0, rt, split, rows, smem);
             c0 += g.chunk;
         } while (c0 < s_count);
+        // each expert's header is checked by the first CTA that reads its weights
+        if (blockIdx.x == 0 && tid == 0) verify_header(hdr, p.L, p.status);
         __syncthreads();  // the list, s_expert and s_count are rewritten for the next expert
     }
 }

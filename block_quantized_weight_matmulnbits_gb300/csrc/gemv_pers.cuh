@@ -309,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pers_kernel(MatmulParams p, 
     cp_async_wait<0>();
     __syncthreads();
     if (n_my > 0) reduce_store(n_my - 1);
+    if (blockIdx.x == 0 && threadIdx.x == 0) verify_header(p.packed_hdr, p.L, p.status);
 }
 
 template <int BITS, bool BF16X, int MT, int SPB_LOG, int TPW>

@@ -36,6 +36,7 @@ __global__ __launch_bounds__(256) void generic_kernel(MatmulParams p) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const int mask = code_mask(L.bits);
     if (tid == 0) bad_gidx = 0;
+    if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) verify_header(p.packed_hdr, L, p.status);
     __syncthreads();
 
     for (int64_t k0 = 0; k0 < L.K; k0 += TK) {

@@ -57,8 +57,9 @@ __global__ void header_kernel(uint8_t* hdr, Layout L) {
 
 // One thread per ORT byte.
 __global__ void unpack_kernel(const uint8_t* __restrict__ packed, uint8_t* __restrict__ b_ort, Layout L,
-                              int64_t nbytes) {
+                              int64_t nbytes, int* status) {
     const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i == 0) verify_header(packed - kHeaderBytes, L, status);
     if (i >= nbytes) return;
     const int64_t row_bytes = L.KB * L.blob;
     const int64_t n = i / row_bytes;
@@ -76,8 +77,9 @@ __global__ void unpack_kernel(const uint8_t* __restrict__ packed, uint8_t* __res
 
 // One thread per (n, k).
 __global__ void dequant_kernel(const uint8_t* __restrict__ packed, const void* __restrict__ scales, int sdt,
-                               const uint8_t* __restrict__ zp, float* __restrict__ w, Layout L) {
+                               const uint8_t* __restrict__ zp, float* __restrict__ w, Layout L, int* status) {
     const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i == 0) verify_header(packed - kHeaderBytes, L, status);
     if (i >= L.N * L.K) return;
     const int64_t n = i / L.K, k = i - n * L.K;
     const int64_t kb = k / L.bs;
@@ -102,14 +104,15 @@ cudaError_t launch_pack(const uint8_t* b_ort, uint8_t* packed_hdr, const Layout&
 
 cudaError_t launch_unpack(const uint8_t* packed, uint8_t* b_ort, const Layout& L, cudaStream_t s) {
     const int64_t nbytes = L.N * L.KB * L.blob;
-    if (nbytes > 0) unpack_kernel<<<blocks_for(nbytes, 256), 256, 0, s>>>(packed, b_ort, L, nbytes);
+    if (nbytes > 0) unpack_kernel<<<blocks_for(nbytes, 256), 256, 0, s>>>(packed, b_ort, L, nbytes, device_status_word());
     return cudaGetLastError();
 }
 
 cudaError_t launch_dequant(const uint8_t* packed, const void* scales, int scale_dtype, const uint8_t* zp,
                            float* w, const Layout& L, cudaStream_t s) {
     const int64_t n = L.N * L.K;
-    if (n > 0) dequant_kernel<<<blocks_for(n, 256), 256, 0, s>>>(packed, scales, scale_dtype, zp, w, L);
+    if (n > 0) dequant_kernel<<<blocks_for(n, 256), 256, 0, s>>>(packed, scales, scale_dtype, zp, w, L,
+                                                                  device_status_word());
     return cudaGetLastError();
 }
 

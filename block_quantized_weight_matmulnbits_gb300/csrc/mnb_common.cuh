@@ -225,6 +225,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // records MNB_ERR_TIMEOUT) when the limit runs out.
 constexpr uint32_t kWaitHintNs = 100000;
 constexpr uint32_t kWaitLimit = 20000;
+constexpr uint32_t kWaitPoll = 0xFFFFFFFFu;  // hint value meaning: poll with test_wait, never suspend
+
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
     for (uint32_t i = 0; i < kWaitLimit; ++i) {
@@ -232,6 +243,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
     }
     set_status(status, 5 /* MNB_ERR_TIMEOUT */);
     return false;
+}
+
+// Compare the header mnb_pack_weights wrote at the start of a packed buffer
+// with the call's shape; a mismatch sets MNB_ERR_LAYOUT_MISMATCH.  Kernels run
+// it from one thread, after their main work, so it costs one 32-byte read.
+__device__ __forceinline__ void verify_header(const void* packed_hdr, const Layout& L, int* status) {
+    const PackedHeader* h = reinterpret_cast<const PackedHeader*>(packed_hdr);
+    if (h->magic != kMagic || h->version != kLayoutVersion || h->N != L.N || h->K != L.K || h->bits != L.bits ||
+        h->block_size != L.bs)
+        set_status(status, 6 /* MNB_ERR_LAYOUT_MISMATCH */);
 }
 
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes: multiple

@@ -27,7 +27,14 @@ struct MatmulParams {
     void* workspace;
     size_t workspace_bytes;
     int flags;               // MNB_FLAG_* of the call
+    uint32_t wait_limit;     // bounded mbarrier waits: tries before MNB_ERR_TIMEOUT
+    uint32_t wait_hint_ns;   // suspend hint of each try (0: poll)
 };
+
+// Wait limits of the call: kWaitLimit x kWaitHintNs (about two seconds), or
+// MNB_WAIT_LIMIT=n polls of 0 ns (a test hook that makes a kernel's first
+// wait that is not already satisfied run out).
+void wait_limits(uint32_t* limit, uint32_t* hint_ns);
 
 constexpr int kFlagPDL = 1;  // == MNB_FLAG_PDL
 

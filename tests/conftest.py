@@ -28,3 +28,10 @@ def mnb():
     import block_quantized_weight_matmulnbits_gb300 as m
     m.load()
     return m
+
+
+@pytest.fixture(scope="session")
+def G(mnb):
+    """GPU-test helpers (tests/_gpu.py), loaded once the library is."""
+    from tests import _gpu
+    return _gpu

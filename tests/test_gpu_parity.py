@@ -120,8 +120,9 @@ def test_matmul_gemv_mma(G, M, bits, bs, dt, asym, N, K):
     G.assert_within(y, ref, mag, w.out_dtype, f"gemv_mma {w.name}")
 
 
-# Enough row tiles (N >= 2 x 16 x SMs) and a short enough K for the persistent
-# decode schedule; ragged N and K, every code width, 1 <= M <= 16.
+# Enough row tiles (N >= 2 x 16 x SMs) for every decode schedule (the
+# streaming default, the persistent ring, one CTA per row tile); ragged N
+# and K, every code width, 1 <= M <= 16.
 PERS_CASES = [
     (1, 4, 32, (BF16, F16, BF16), True, 4801, 4096),
     (1, 4, 16, (F16, F32, F16), False, 4800, 1000),
@@ -135,14 +136,14 @@ PERS_CASES = [
 
 
 @pytest.mark.parametrize("M,bits,bs,dt,asym,N,K", PERS_CASES)
-@pytest.mark.parametrize("pers", ["1", "0"])  # persistent schedule opt-in, per-tile default
-def test_matmul_gemv_persistent(G, monkeypatch, M, bits, bs, dt, asym, N, K, pers):
-    monkeypatch.setenv("MNB_GEMV_PERS", pers)
+@pytest.mark.parametrize("sched", ["stream", "pers", "tile"])
+def test_matmul_gemv_schedules(G, monkeypatch, M, bits, bs, dt, asym, N, K, sched):
+    monkeypatch.setenv("MNB_GEMV_SCHED", sched)
     w = _w(M, N, K, bits, bs, dt, asym, 900 + M * 13 + bits * 7 + bs + N)
     P = G.Problem(w)
     y = P.y64(P.run("gemv_mma"))
     ref, mag = P.oracle_full()
-    G.assert_within(y, ref, mag, w.out_dtype, f"gemv_mma pers={pers} {w.name}")
+    G.assert_within(y, ref, mag, w.out_dtype, f"gemv_mma {sched} {w.name}")
 
 
 TC_CASES = []
@@ -156,9 +157,9 @@ TC_CASES += [(64, 4, 32, (BF16, F16, BF16), False, 4096, 512), (1, 4, 32, (BF16,
              (256, 4, 16, (BF16, BF16, F32), True, 520, 136), (300, 8, 16, (F16, F16, BF16), False, 48, 72)]
 
 
-# Shapes for the W-in-tensor-memory GEMM (scales / zero points 16-byte aligned
-# per row, enough blocks for one raw-scale box): every code width, ragged M
-# and N, both activation dtypes, with and without zero points.
+# Larger shapes for the tcgen05 GEMM, each run at every token-tile width
+# (MNB_TC_BT): every code width, ragged M and N, both activation dtypes, with
+# and without zero points.
 TA_CASES = [
     (128, 4, 32, (BF16, F16, BF16), True, 256, 1024),
     (200, 4, 32, (F16, F32, F16), False, 300, 2048),
@@ -173,14 +174,14 @@ TA_CASES = [
 
 
 @pytest.mark.parametrize("M,bits,bs,dt,asym,N,K", TA_CASES)
-@pytest.mark.parametrize("ta", ["1", "0"])
-def test_matmul_gemm_tmem_weights(G, monkeypatch, M, bits, bs, dt, asym, N, K, ta):
-    monkeypatch.setenv("MNB_TC_TA", ta)
+@pytest.mark.parametrize("bt", ["32", "64", "128"])
+def test_matmul_gemm_token_tiles(G, monkeypatch, M, bits, bs, dt, asym, N, K, bt):
+    monkeypatch.setenv("MNB_TC_BT", bt)
     w = _w(M, N, K, bits, bs, dt, asym, 1100 + M * 3 + bits * 7 + bs + N)
     P = G.Problem(w)
     y = P.y64(P.run("gemm_tc"))
     ref, mag = P.oracle_full()
-    G.assert_within(y, ref, mag, w.out_dtype, f"gemm_tc ta={ta} {w.name}")
+    G.assert_within(y, ref, mag, w.out_dtype, f"gemm_tc bt={bt} {w.name}")
 
 
 @pytest.mark.parametrize("M,bits,bs,dt,asym,N,K", TC_CASES)
