@@ -1,15 +1,23 @@
-// Host side of the tcgen05 prefill GEMM (kernel in gemm_bs.cuh): tile
-// geometry, tensor maps and dispatch to the per-code-width instantiations.
+// Host side of the tcgen05 prefill GEMM: tile geometry, tensor maps and
+// dispatch.  bf16 activations run the hi/lo kernel (gemm_hl.cuh: the weight
+// as an exact-enough sum of two bf16 values, one accumulator); f16
+// activations run the block-scaled kernel (gemm_bs.cuh: exact (q - zp) and
+// one TMEM partial per quantisation block), whose f32 rescale has no range
+// limit where an f16 weight would.  MNB_TC_KERNEL=bs forces the latter.
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 
 #include "gemm_bs.cuh"
+#include "gemm_hl.cuh"
 
 namespace mnb {
 cudaError_t launch_gemm_tc_b2(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s);
 cudaError_t launch_gemm_tc_b4(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s);
 cudaError_t launch_gemm_tc_b8(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s);
+cudaError_t launch_gemm_hl_b2(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s);
+cudaError_t launch_gemm_hl_b4(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s);
+cudaError_t launch_gemm_hl_b8(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s);
 
 namespace {
 using gbs::Geom;
@@ -75,6 +83,60 @@ Geom make_geom(const MatmulParams& p) {
     return g;
 }
 
+bool use_hl(const MatmulParams& p) {
+    const char* k = std::getenv("MNB_TC_KERNEL");
+    if (k && std::strcmp(k, "bs") == 0) return false;
+    return p.act_dtype == kBF16;
+}
+
+// hi/lo kernel: 128 W rows x 256 tokens per tile; the two CTAs of a cluster
+// split K when one tile per CTA would leave more than half the SMs idle.
+ghl::Geom make_geom_hl(const MatmulParams& p) {
+    ghl::Geom g{};
+    const Layout& L = p.L;
+    const int sms = device_info().sm_count > 0 ? device_info().sm_count : 148;
+    g.n_tiles = (int)((L.N + ghl::kRows - 1) / ghl::kRows);
+    g.m_tiles = (int)((p.M + ghl::kBT - 1) / ghl::kBT);
+    g.k_stages = (int)((L.Kpad + ghl::kBK - 1) / ghl::kBK);
+    const int64_t tiles = (int64_t)g.n_tiles * g.m_tiles;
+    g.splitk = (2 * tiles <= sms && g.k_stages >= 2) ? 2 : 1;
+    const char* env = std::getenv("MNB_TC_SPLITK");
+    if (env && (env[0] == '1' || env[0] == '2')) g.splitk = (env[0] == '2' && g.k_stages >= 2) ? 2 : 1;
+    const int tiles_per_stage = L.KT >= ghl::kBK ? 1 : (int)(ghl::kBK / L.KT);
+    g.wp_stage = (size_t)(ghl::kRows / 16) * tiles_per_stage * kTileBytes;
+    g.total_bytes = 1024 + ghl::kR * (ghl::kXStage + g.wp_stage) + (3 * ghl::kR + 1) * 8 + 16;
+    return g;
+}
+
+cudaError_t launch_hl(const MatmulParams& p, EncodeTiledFn enc, cudaStream_t s) {
+    const ghl::Geom geo = make_geom_hl(p);
+    ghl::Maps m;
+    std::memset(&m, 0, sizeof(m));
+    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t dims[2] = {(cuuint64_t)p.L.K, (cuuint64_t)p.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.L.K * 2};
+    const cuuint32_t box[2] = {ghl::kBK, ghl::kBT};
+    CUresult r = enc(&m.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.x), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    const cuuint64_t tdims[5] = {8, 8, 4, (cuuint64_t)p.L.KTILES, (cuuint64_t)p.L.NT};
+    const cuuint64_t tstrides[4] = {64, 16, (cuuint64_t)kTileBytes, (cuuint64_t)p.L.KTILES * kTileBytes};
+    const cuuint32_t tbox[5] = {8, 8, 4, (cuuint32_t)(p.L.KT >= ghl::kBK ? 1 : ghl::kBK / p.L.KT),
+                                (cuuint32_t)(ghl::kRows / 16)};
+    const cuuint32_t testr[5] = {1, 1, 1, 1, 1};
+    r = enc(&m.w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<uint8_t*>(p.packed), tdims, tstrides, tbox, testr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    switch (p.L.bits) {
+        case 2: return launch_gemm_hl_b2(p, geo, m, s);
+        case 4: return launch_gemm_hl_b4(p, geo, m, s);
+        case 8: return launch_gemm_hl_b8(p, geo, m, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
 
 bool gemm_tc_supported(const MatmulParams& p) {
@@ -86,14 +148,19 @@ bool gemm_tc_supported(const MatmulParams& p) {
     if ((reinterpret_cast<uintptr_t>(p.x) & 15) != 0) return false;
     if (p.L.K > (int64_t)1 << 31 || p.M > (int64_t)1 << 31) return false;
     if (!encode_fn()) return false;
+    if (use_hl(p)) {
+        const ghl::Geom h = make_geom_hl(p);
+        return h.total_bytes <= di.smem_optin && (int64_t)h.n_tiles * h.m_tiles * h.splitk < (int64_t)1 << 31;
+    }
     const Geom g = make_geom(p);
     return g.NP >= 2 && g.total_bytes <= di.smem_optin && (int64_t)g.n_tiles * g.m_tiles < (int64_t)1 << 31;
 }
 
 cudaError_t launch_gemm_tc(const MatmulParams& p, cudaStream_t s) {
-    const Geom geo = make_geom(p);
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
+    if (use_hl(p)) return launch_hl(p, enc, s);
+    const Geom geo = make_geom(p);
     Maps m;
     std::memset(&m, 0, sizeof(m));
     // X: [M][K] bf16/f16, 64-deep x BT-token boxes, 128-byte swizzle, zero fill past M and K

@@ -21,9 +21,18 @@ __device__ __forceinline__ int packed_code(const uint8_t* packed, const Layout& 
     return (packed[bit >> 3] >> (bit & 7)) & code_mask(L.bits);
 }
 
-// One thread per 32-bit word of tile data.
+// Code (n, k) of a [K, N] floating-point weight source (k < K, n < N).
+__device__ __forceinline__ int kn_code(const uint8_t* w, const Layout& L, int fmt, int64_t n, int64_t k) {
+    const int64_t f = k * L.N + n;
+    if (fmt == kWfNVFP4) return (w[f >> 1] >> ((f & 1) * 4)) & 0xF;
+    return w[f];
+}
+
+// One thread per 32-bit word of tile data.  fmt kWfInt reads ORT codes (the
+// padded depths [K, KB*bs) included); the floating-point formats read the
+// [K, N] source and zero-fill depths past K (a zero code decodes to +0).
 __global__ void pack_kernel(const uint8_t* __restrict__ b_ort, uint32_t* __restrict__ out, Layout L,
-                            int64_t words) {
+                            int64_t words, int fmt) {
     const int64_t wi = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (wi >= words) return;
     const int64_t tile = wi >> 7;  // 128 words per tile
@@ -35,12 +44,16 @@ __global__ void pack_kernel(const uint8_t* __restrict__ b_ort, uint32_t* __restr
     for (int f = 0; f < fields; ++f) {
         int64_t n, k;
         L.field_coords(nt, kt, lane, j, f, &n, &k);
-        if (n < L.N && k < L.Kpad) word |= (uint32_t)ort_code(b_ort, L, n, k) << (f * L.bits);
+        if (fmt == kWfInt) {
+            if (n < L.N && k < L.Kpad) word |= (uint32_t)ort_code(b_ort, L, n, k) << (f * L.bits);
+        } else if (n < L.N && k < L.K) {
+            word |= (uint32_t)kn_code(b_ort, L, fmt, n, k) << (f * L.bits);
+        }
     }
     out[wi] = word;
 }
 
-__global__ void header_kernel(uint8_t* hdr, Layout L) {
+__global__ void header_kernel(uint8_t* hdr, Layout L, int fmt) {
     const int i = threadIdx.x;
     if (i < kHeaderBytes / 4) reinterpret_cast<uint32_t*>(hdr)[i] = 0;
     __syncthreads();
@@ -52,6 +65,7 @@ __global__ void header_kernel(uint8_t* hdr, Layout L) {
         h->K = L.K;
         h->bits = L.bits;
         h->block_size = L.bs;
+        h->format = fmt;
     }
 }
 
@@ -93,12 +107,12 @@ unsigned blocks_for(int64_t n, int threads) { return (unsigned)((n + threads - 1
 
 }  // namespace
 
-cudaError_t launch_pack(const uint8_t* b_ort, uint8_t* packed_hdr, const Layout& L, cudaStream_t s) {
-    header_kernel<<<1, 64, 0, s>>>(packed_hdr, L);
+cudaError_t launch_pack(const uint8_t* b_ort, uint8_t* packed_hdr, const Layout& L, cudaStream_t s, int fmt) {
+    header_kernel<<<1, 64, 0, s>>>(packed_hdr, L, fmt);
     const int64_t words = (int64_t)(L.data_bytes() / 4);
     if (words > 0)
         pack_kernel<<<blocks_for(words, 256), 256, 0, s>>>(
-            b_ort, reinterpret_cast<uint32_t*>(packed_hdr + kHeaderBytes), L, words);
+            b_ort, reinterpret_cast<uint32_t*>(packed_hdr + kHeaderBytes), L, words, fmt);
     return cudaGetLastError();
 }
 

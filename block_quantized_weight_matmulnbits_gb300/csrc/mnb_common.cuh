@@ -51,7 +51,15 @@ struct PackedHeader {
     int64_t K;
     int32_t bits;
     int32_t block_size;
+    int32_t format;  // 0: MatMulNBits integer codes; else a floating-point weight format (WFormat)
 };
+
+// Weight formats of a packed buffer.  kWfInt: MatMulNBits codes (ORT source
+// [N, KB, blob]).  The floating-point formats of rlx-cpu 0.2.13,
+// src/thunk/ops/quant.rs (dequant_matmul_fp8, dequant_matmul_nvfp4) come from
+// a [K, N] source: FP8 one byte per weight at k * N + n (bits 8), NVFP4 one
+// nibble per weight at flat index k * N + n, low nibble first (bits 4).
+enum WFormat : int { kWfInt = 0, kWfE4M3 = 1, kWfE5M2 = 2, kWfNVFP4 = 3 };
 
 struct Layout {
     int bits;
@@ -248,10 +256,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
 // Compare the header mnb_pack_weights wrote at the start of a packed buffer
 // with the call's shape; a mismatch sets MNB_ERR_LAYOUT_MISMATCH.  Kernels run
 // it from one thread, after their main work, so it costs one 32-byte read.
-__device__ __forceinline__ void verify_header(const void* packed_hdr, const Layout& L, int* status) {
+__device__ __forceinline__ void verify_header(const void* packed_hdr, const Layout& L, int* status,
+                                              int format = kWfInt) {
     const PackedHeader* h = reinterpret_cast<const PackedHeader*>(packed_hdr);
     if (h->magic != kMagic || h->version != kLayoutVersion || h->N != L.N || h->K != L.K || h->bits != L.bits ||
-        h->block_size != L.bs)
+        h->block_size != L.bs || h->format != format)
         set_status(status, 6 /* MNB_ERR_LAYOUT_MISMATCH */);
 }
 

@@ -38,7 +38,8 @@ void wait_limits(uint32_t* limit, uint32_t* hint_ns);
 
 constexpr int kFlagPDL = 1;  // == MNB_FLAG_PDL
 
-cudaError_t launch_pack(const uint8_t* b_ort, uint8_t* packed_hdr, const Layout& L, cudaStream_t s);
+cudaError_t launch_pack(const uint8_t* b_ort, uint8_t* packed_hdr, const Layout& L, cudaStream_t s,
+                        int fmt = kWfInt);
 cudaError_t launch_unpack(const uint8_t* packed, uint8_t* b_ort, const Layout& L, cudaStream_t s);
 cudaError_t launch_dequant(const uint8_t* packed, const void* scales, int scale_dtype, const uint8_t* zp,
                            float* w, const Layout& L, cudaStream_t s);
