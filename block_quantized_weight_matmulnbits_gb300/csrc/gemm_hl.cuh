@@ -215,44 +215,72 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
         const int zmask = code_mask(BITS);
         const int sdt = p.scale_dtype;
         // block of the thread's 32 depths (bs >= 32) or of each of its two k-steps (bs = 16)
+        const int bs_log = __ffs(L.bs) - 1;  // block sizes are powers of two
         auto blocks_of = [&](int ks, int64_t* kb0, int64_t* kb1) {
             const int64_t d0 = (int64_t)ks * kBK + 32 * jh;
-            *kb0 = d0 / L.bs;
-            *kb1 = (d0 + 16) / L.bs;
+            *kb0 = d0 >> bs_log;
+            *kb1 = (d0 + 16) >> bs_log;
         };
-        auto fetch = [&](int ks, float* s0, float* s1, uint32_t* z0, uint32_t* z1) {
+        // raw loads only (a decode here would wait for the load): scale bits and the
+        // zero-point byte of the thread's block(s) of a stage; decoded when used
+        const bool two_blocks = L.bs < 32;
+        auto raw_scale = [&](int64_t kb) -> uint32_t {
+            if (!row_ok || kb >= L.KB) return 0u;
+            const int64_t i = n * L.KB + kb;
+            return sdt == kF32 ? __ldg(static_cast<const uint32_t*>(p.scales) + i)
+                               : (uint32_t)__ldg(static_cast<const unsigned short*>(p.scales) + i);
+        };
+        auto raw_zp = [&](int64_t kb) -> uint32_t {
+            if (!p.zp || !row_ok || kb >= L.KB) return 0u;
+            return __ldg(p.zp + n * L.zp_row + ((kb * BITS) >> 3));
+        };
+        auto fetch = [&](int ks, uint32_t* s0, uint32_t* s1, uint32_t* z0, uint32_t* z1) {
             int64_t kb0, kb1;
             blocks_of(ks, &kb0, &kb1);
-            *s0 = (row_ok && kb0 < L.KB) ? load_f32(p.scales, n * L.KB + kb0, sdt) : 0.f;
-            *s1 = kb1 == kb0 ? *s0 : ((row_ok && kb1 < L.KB) ? load_f32(p.scales, n * L.KB + kb1, sdt) : 0.f);
-            uint32_t za = 1u << (BITS - 1), zb = za;
-            if (p.zp) {
-                za = (row_ok && kb0 < L.KB) ? (uint32_t)load_zp(p.zp, L, n, kb0) : 0u;
-                zb = kb1 == kb0 ? za : ((row_ok && kb1 < L.KB) ? (uint32_t)load_zp(p.zp, L, n, kb1) : 0u);
+            *s0 = raw_scale(kb0);
+            *z0 = raw_zp(kb0);
+            if (two_blocks) {
+                *s1 = raw_scale(kb1);
+                *z1 = raw_zp(kb1);
             }
-            *z0 = za;
-            *z1 = zb;
         };
-        float ns0, ns1;
-        uint32_t nz0, nz1;
-        fetch(ks_lo, &ns0, &ns1, &nz0, &nz1);
-        bool ok = true;
-        for (int i = 0; i < KS; ++i) {
+        auto dec_scale = [&](uint32_t r) -> float {
+            if (sdt == kF32) return __uint_as_float(r);
+            if (sdt == kF16) return __half2float(__ushort_as_half((unsigned short)r));
+            return __uint_as_float(r << 16);
+        };
+        auto dec_zp = [&](uint32_t r, int ks, int half) -> uint32_t {
+            if (!p.zp) return 1u << (BITS - 1);
+            int64_t kb0, kb1;
+            blocks_of(ks, &kb0, &kb1);
+            const int64_t kb = half ? kb1 : kb0;
+            return (r >> ((kb * BITS) & 7)) & (uint32_t)zmask;
+        };
+        // scales and zero points are scattered loads (one row per thread): each is
+        // fetched kPF stages ahead into one of kPF named register slots, and the
+        // stage loop is unrolled kPF times so a slot is read in place (copying a
+        // register whose load is still in flight would wait for it)
+        constexpr int kPF = 3;
+        uint32_t ps0[kPF], ps1[kPF] = {}, pz0[kPF], pz1[kPF] = {};
+#pragma unroll
+        for (int q = 0; q < kPF; ++q)
+            if (q < KS) fetch(ks_lo + q, &ps0[q], &ps1[q], &pz0[q], &pz1[q]);
+        auto stage = [&](int i, uint32_t& slot_s0, uint32_t& slot_s1, uint32_t& slot_z0, uint32_t& slot_z1) -> bool {
             const int s = i % kR;
             const uint32_t ph = (uint32_t)((i / kR) & 1);
             const int ks = ks_lo + i;
-            const float sc0 = ns0, sc1 = ns1;
-            const uint32_t z0 = nz0, z1 = nz1;
-            if (i + 1 < KS) fetch(ks + 1, &ns0, &ns1, &nz0, &nz1);
             if (i >= kR && !tc::wait_bounded(&mma_done[s], ph ^ 1u, p.status, wl, wh)) {
-                ok = false;
-                break;
+                return false;
             }
             if (!tc::wait_bounded(&tma_full[s], ph, p.status, wl, wh)) {
-                ok = false;
-                break;
+                return false;
             }
-            if (*abort_v) break;
+            if (*abort_v) return false;
+            const float sc0 = dec_scale(slot_s0);
+            const float sc1 = two_blocks ? dec_scale(slot_s1) : sc0;
+            const uint32_t z0 = dec_zp(slot_z0, ks, 0);
+            const uint32_t z1 = two_blocks ? dec_zp(slot_z1, ks, 1) : z0;
+            if (i + kPF < KS) fetch(ks + kPF, &slot_s0, &slot_s1, &slot_z0, &slot_z1);
             uint32_t shi[2], slo[2], zc[2];
             split_scale(sc0, &shi[0], &slo[0]);
             split_scale(sc1, &shi[1], &slo[1]);
@@ -313,6 +341,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
             tc::fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_full[s]);
+            return true;
+        };
+        bool ok = true;
+        for (int i = 0; i < KS && ok; i += kPF) {
+            ok = stage(i, ps0[0], ps1[0], pz0[0], pz1[0]);
+            if (ok && i + 1 < KS) ok = stage(i + 1, ps0[1], ps1[1], pz0[1], pz1[1]);
+            if (ok && i + 2 < KS) ok = stage(i + 2, ps0[2], ps1[2], pz0[2], pz1[2]);
         }
         if (!ok) *abort_v = 1;
 

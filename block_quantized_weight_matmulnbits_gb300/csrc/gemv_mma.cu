@@ -1,13 +1,15 @@
-// Host side of the small-batch tensor-core GEMV: three schedules of the same
-// arithmetic (gemv_mma.cuh, one CTA per row tile; gemv_pers.cuh, a
-// persistent ring; gemv_stream.cuh, persistent with register prefetch).
-// MNB_GEMV_SCHED=stream|tile|pers forces one (MNB_GEMV_PERS=0/1 still
-// selects between the first two).
+// Host side of the small-batch tensor-core GEMV: four schedules of the same
+// arithmetic.  gemv_mma.cuh (the default): one CTA per row tile.
+// gemv_xr.cuh (M <= 8, a warp slice of at most 16 k-steps): one 16-warp CTA
+// per SM, X in registers, per-warp bulk-copy rings.  gemv_pers.cuh: a persistent cp.async ring.  gemv_stream.cuh:
+// persistent with register prefetch.  MNB_GEMV_SCHED=xr|tile|pers|stream
+// forces one (MNB_GEMV_PERS=0/1 still selects between tile and pers).
 #include <cstdlib>
 #include <cstring>
 
 #include "gemv_pers.cuh"
 #include "gemv_stream.cuh"
+#include "gemv_xr.cuh"
 
 namespace mnb {
 
@@ -20,10 +22,26 @@ cudaError_t launch_gemv_pers_b8(const MatmulParams& p, const gpers::PGeom& geo, 
 cudaError_t launch_gemv_stream_b2(const MatmulParams& p, const gstr::SGeom& geo, cudaStream_t s);
 cudaError_t launch_gemv_stream_b4(const MatmulParams& p, const gstr::SGeom& geo, cudaStream_t s);
 cudaError_t launch_gemv_stream_b8(const MatmulParams& p, const gstr::SGeom& geo, cudaStream_t s);
+cudaError_t launch_gemv_xr_b2(const MatmulParams& p, const gxr::XGeom& geo, cudaStream_t s);
+cudaError_t launch_gemv_xr_b4(const MatmulParams& p, const gxr::XGeom& geo, cudaStream_t s);
+cudaError_t launch_gemv_xr_b8(const MatmulParams& p, const gxr::XGeom& geo, cudaStream_t s);
 
 static const char* sched_env() {
     const char* v = std::getenv("MNB_GEMV_SCHED");
     return (v && *v) ? v : nullptr;
+}
+
+// The register-X schedule (opt-in with MNB_GEMV_SCHED=xr; measured slower
+// than the per-tile grid on GB300: 27.5 vs 10.5 us on the int4 4096 x 11008
+// decode).
+static bool xr_ok(const MatmulParams& p, gxr::XGeom* out) {
+    const char* sc = sched_env();
+    if (!sc || std::strcmp(sc, "xr") != 0) return false;
+    const int sms = device_info().sm_count > 0 ? device_info().sm_count : 148;
+    const int sbytes = p.scale_dtype == kF32 ? 4 : 2;
+    const bool aligned = (reinterpret_cast<uintptr_t>(p.scales) & 15) == 0 &&
+                         (p.zp == nullptr || (reinterpret_cast<uintptr_t>(p.zp) & 15) == 0);
+    return gxr::make_xgeom(p.L, p.M, sms, device_info().smem_optin, out, sbytes, aligned);
 }
 
 // The streaming schedule (opt-in with MNB_GEMV_SCHED=stream) takes every
@@ -49,7 +67,7 @@ static bool pers_ok(const MatmulParams& p, gpers::PGeom* out, int* grid) {
     } else if (sc) {
         return false;
     }
-    const char* env = sc ? "1" : std::getenv("MNB_GEMV_PERS");
+    const char* env = (sc && std::strcmp(sc, "pers") == 0) ? "1" : std::getenv("MNB_GEMV_PERS");
     if (env && env[0] == '0') return false;
     if (!(env && env[0] == '1') && p.M < 2) return false;
     const Layout& L = p.L;
@@ -89,6 +107,15 @@ bool gemv_mma_supported(const MatmulParams& p) {
 }
 
 cudaError_t launch_gemv_mma(const MatmulParams& p, cudaStream_t s) {
+    gxr::XGeom xg;
+    if (xr_ok(p, &xg)) {
+        switch (p.L.bits) {
+            case 2: return launch_gemv_xr_b2(p, xg, s);
+            case 4: return launch_gemv_xr_b4(p, xg, s);
+            case 8: return launch_gemv_xr_b8(p, xg, s);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     gstr::SGeom sg;
     if (stream_ok(p, &sg)) {
         switch (p.L.bits) {

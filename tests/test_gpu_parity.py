@@ -136,7 +136,7 @@ PERS_CASES = [
 
 
 @pytest.mark.parametrize("M,bits,bs,dt,asym,N,K", PERS_CASES)
-@pytest.mark.parametrize("sched", ["stream", "pers", "tile"])
+@pytest.mark.parametrize("sched", ["xr", "stream", "pers", "tile"])
 def test_matmul_gemv_schedules(G, monkeypatch, M, bits, bs, dt, asym, N, K, sched):
     monkeypatch.setenv("MNB_GEMV_SCHED", sched)
     w = _w(M, N, K, bits, bs, dt, asym, 900 + M * 13 + bits * 7 + bs + N)

@@ -94,6 +94,8 @@ SHAPES = [
 @pytest.mark.parametrize("x_mode", ["one_hot", "positive"])
 @pytest.mark.parametrize("bits,bs,act,sdt,zpm", SHAPES)
 @pytest.mark.parametrize("kernel,M,env", [
+    ("gemv_mma", 1, {"MNB_GEMV_SCHED": "xr"}),
+    ("gemv_mma", 8, {"MNB_GEMV_SCHED": "xr"}),
     ("gemv_mma", 1, {"MNB_GEMV_SCHED": "stream"}),
     ("gemv_mma", 8, {"MNB_GEMV_SCHED": "stream"}),
     ("gemv_mma", 16, {"MNB_GEMV_SCHED": "stream"}),
