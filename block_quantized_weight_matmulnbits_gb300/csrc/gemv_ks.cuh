@@ -1,0 +1,417 @@
+// Decode GEMV for 1 <= M <= 8, bf16 or f16 X, f32 / f16 / bf16 scales:
+//   Y[m, n] = sum_kb scale[n, kb] * sum_{k in kb} X[m, k] * (q[n, k] - zp[n, kb])   (+ bias[n]),
+// MatMulNBits as restated by onnx-runtime-ep-cpu 0.1.0-dev.5,
+// src/kernels/matmul_nbits.rs (fn dequantize_nbits_value; MatMulNBitsKernel::
+// execute), with the arithmetic of gemv_mma.cuh: (q - zp) exact in the
+// activation type (mantissa magic and one packed subtract), one mma.sync
+// m16n8k16 per 256 weights, the block's f32 scale applied to the fragment.
+//
+// Schedule, shaped for the fewest issue slots per weight byte (a 26 MB int4
+// weight must stream in ~4 us, so a k-step of 128 bytes has a budget of about
+// 16 warp instructions on 152 SMs):
+//   * one CTA of 16 warps per SM owns a contiguous range of 16-row tiles;
+//   * work items are (row tile, K-chunk) pairs, a K-chunk being 4 packed
+//     tiles: 64 bytes per lane, 16 k-steps of 4-bit codes (32 of 2-bit, 8 of
+//     8-bit); warp w takes items w, w + 16, ... of its CTA, so every warp
+//     gets the same number of items to within one;
+//   * each item's weights, raw scales and raw zero points go straight from
+//     global memory into registers one item ahead (double-buffered; no
+//     shared-memory staging, no tables); scales and zero points are decoded
+//     when their block starts (measured on GB300: asynchronous copies into a
+//     deeper shared-memory ring, with or without staged scales, were slower);
+//   * X is staged once in shared memory in B-fragment order, one 16-byte
+//     load per lane per two k-steps;
+//   * each warp keeps its partial sums of a row tile in registers and writes
+//     them once per row tile; one pass at the end adds the 16 warps' partials
+//     of every row in a fixed order, so results are bit-identical run to run.
+// There are no waits on other threads besides two CTA barriers.
+#pragma once
+
+#include "gemv_mma.cuh"
+
+namespace mnb {
+namespace gks {
+
+using gmma::mma16816;
+using gmma::Unpack;
+
+constexpr int kW = 16;
+constexpr int kThreads = kW * 32;
+constexpr int kTilesPerChunk = 4;  // 64 bytes per lane
+
+struct KGeom {
+    int G;        // CTAs
+    int KC;       // K-chunks per row tile
+    int max_rt;   // most row tiles of one CTA
+    int xrow;     // X row stride in 16-byte units (K / 8 + 4: padded against bank conflicts)
+    size_t x_bytes, red_bytes, total_bytes;
+};
+
+// k-steps per chunk for a code width: 4 packed tiles.
+__host__ __device__ constexpr int chunk_steps(int bits) { return kTilesPerChunk * (16 / bits); }
+
+// The shapes this schedule takes: the chunk depth divides K, a quantisation
+// block lies inside one chunk, a row's scales of one chunk are at most 32
+// bytes, and X (M + 1 rows) plus the partial sums fit in shared memory.
+inline bool make_kgeom(const Layout& L, int64_t M, int sms, size_t smem_limit, int sbytes, KGeom* out) {
+    if (M < 1 || M > 8) return false;
+    const int ch = chunk_steps(L.bits);
+    const int64_t chunk_k = (int64_t)ch * 16;
+    if (L.K % chunk_k != 0) return false;
+    const int spb = (int)(L.bs / 16);
+    if (L.bs % 16 != 0 || spb < 1 || spb > ch || (spb & (spb - 1)) != 0) return false;
+    if ((ch / spb) * sbytes > 32) return false;
+    // scale and zero-point offsets are formed in 32 bits
+    if ((uint64_t)L.N * (uint64_t)L.KB * 4u >= (1ull << 32) || (uint64_t)L.N * (uint64_t)L.zp_row >= (1ull << 32))
+        return false;
+    KGeom g{};
+    g.KC = (int)(L.K / chunk_k);
+    g.G = (int)(L.NT < sms ? L.NT : sms);
+    g.max_rt = (int)((L.NT + g.G - 1) / g.G);
+    g.xrow = (int)(L.K / 8) + 4;
+    g.x_bytes = (size_t)(M + 1) * g.xrow * 16;
+    g.red_bytes = (size_t)g.max_rt * kW * 16 * M * 4;
+    g.total_bytes = g.x_bytes + g.red_bytes;
+    if (g.total_bytes > smem_limit) return false;
+    *out = g;
+    return true;
+}
+
+template <int BYTES>
+__device__ __forceinline__ void ld_raw(const void* src, uint32_t (&w)[BYTES >= 4 ? BYTES / 4 : 1]) {
+    if constexpr (BYTES == 32) {
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
+        const uint4 b = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+        w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    } else if constexpr (BYTES == 16) {
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    } else if constexpr (BYTES == 8) {
+        const uint2 a = __ldg(reinterpret_cast<const uint2*>(src));
+        w[0] = a.x; w[1] = a.y;
+    } else if constexpr (BYTES == 4) {
+        w[0] = __ldg(reinterpret_cast<const uint32_t*>(src));
+    } else if constexpr (BYTES == 2) {
+        w[0] = __ldg(reinterpret_cast<const uint16_t*>(src));
+    } else {
+        w[0] = __ldg(reinterpret_cast<const uint8_t*>(src));
+    }
+}
+
+template <int BITS, bool BF16X, int SPB_LOG, int SDT>
+struct Item {
+    static constexpr int SPT = 16 / BITS;              // k-steps per packed tile
+    static constexpr int CH = kTilesPerChunk * SPT;     // k-steps per chunk
+    static constexpr int SPB = 1 << SPB_LOG;            // k-steps per block
+    static constexpr int BPC = CH / SPB;                // blocks per chunk
+    static constexpr int SBYTES = BPC * (SDT == kF32 ? 4 : 2);  // raw scales of a row
+    static constexpr int SW = SBYTES >= 4 ? SBYTES / 4 : 1;
+    static constexpr int ZBITS = BPC * BITS;            // raw zero-point bits of a row
+    static constexpr int ZBYTES = ZBITS >= 8 ? ZBITS / 8 : 1;
+    static constexpr int ZW = ZBYTES >= 4 ? ZBYTES / 4 : 1;
+    // zero points spread one per byte: block b in byte (b / NZS) % 4 of word
+    // (b % NZS) + NZS * (b / (4 * NZS)), NZS = 8 / BITS words per raw word
+    static constexpr int NZS = 8 / BITS;
+    static constexpr int ZSW = BITS == 8 ? ZW : ZW * NZS;
+    // every code field holding 2^(bits - 1): the zero point when none is given
+    static constexpr uint32_t kZDefault = BITS == 2 ? 0xAAAAAAAAu : BITS == 4 ? 0x88888888u : 0x80808080u;
+    // high byte of the subtraction constant (magic + z) in each 16-bit lane,
+    // or the f32 magic 2^23 for 8-bit codes under bf16 activations
+    static constexpr bool kF32Magic = BITS == 8 && BF16X;
+    static constexpr uint32_t kZHigh = kF32Magic ? 0x4B000000u : ((Unpack<BITS, BF16X>::kMagic16x2 >> 8) & 0xFFu);
+    static_assert(SPB <= CH && SBYTES <= 32, "block outside the chunk");
+
+    uint4 w[kTilesPerChunk];
+    uint32_t s0[SW], s8[SW];
+    uint32_t z0[ZW], z8[ZW];  // raw code fields (spread when the item is computed)
+    uint32_t zshift;          // bit offset of the chunk's first field (fields under 8 bits a chunk)
+
+    // Loads of item (row tile rt, chunk c): wp is the lane's 16 bytes of the
+    // item's first packed tile.  Rows past N read row N - 1 instead (their
+    // results are never stored, and every row's sum is independent), so the
+    // loads need no predicates; scale and zero-point offsets fit 32 bits.
+    __device__ __forceinline__ void load(const MatmulParams& p, const uint8_t* wp, int64_t rt, int c, int g) {
+        const Layout& L = p.L;
+#pragma unroll
+        for (int j = 0; j < kTilesPerChunk; ++j) w[j] = ldg_stream(wp + j * kTileBytes);
+        const uint32_t nlast = (uint32_t)L.N - 1u;
+        const uint32_t n0 = (uint32_t)rt * 16u + (uint32_t)g;
+        const uint32_t r0 = n0 < nlast ? n0 : nlast, r8 = n0 + 8u < nlast ? n0 + 8u : nlast;
+        const uint32_t srow = (uint32_t)L.KB * (SDT == kF32 ? 4u : 2u);
+        const uint8_t* sp = static_cast<const uint8_t*>(p.scales) + (uint32_t)c * (uint32_t)SBYTES;
+        ld_raw<SBYTES>(sp + r0 * srow, s0);
+        ld_raw<SBYTES>(sp + r8 * srow, s8);
+        if (p.zp != nullptr) {
+            const uint32_t zbit = (uint32_t)c * (uint32_t)ZBITS;
+            const uint8_t* zp = p.zp + (zbit >> 3);
+            const uint32_t zrow = (uint32_t)L.zp_row;
+            ld_raw<ZBYTES>(zp + r0 * zrow, z0);
+            ld_raw<ZBYTES>(zp + r8 * zrow, z8);
+            zshift = ZBITS < 8 ? (zbit & 7u) : 0u;
+        } else {
+#pragma unroll
+            for (int i = 0; i < ZW; ++i) z0[i] = z8[i] = kZDefault;
+            zshift = 0;
+        }
+    }
+
+    // Raw code fields to one field per byte (done once per item, so that a
+    // block's subtraction constant is a single byte permute).
+    __device__ __forceinline__ static void spread(const uint32_t (&raw)[ZW], uint32_t shift, uint32_t (&z)[ZSW]) {
+        uint32_t r[ZW];
+#pragma unroll
+        for (int i = 0; i < ZW; ++i) r[i] = raw[i];
+        if constexpr (ZBITS < 8) r[0] >>= shift;
+#pragma unroll
+        for (int i = 0; i < ZW; ++i) {
+            if constexpr (BITS == 8) {
+                z[i] = r[i];
+            } else if constexpr (BITS == 4) {
+                z[2 * i] = r[i] & 0x0F0F0F0Fu;
+                z[2 * i + 1] = (r[i] >> 4) & 0x0F0F0F0Fu;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) z[4 * i + j] = (r[i] >> (2 * j)) & 0x03030303u;
+            }
+        }
+    }
+
+    __device__ __forceinline__ static float scale(const uint32_t (&s)[SW], int b) {
+        if constexpr (SDT == kF32) return __uint_as_float(s[b]);
+        const uint32_t word = s[b >> 1];
+        if constexpr (SDT == kBF16) {
+            return __uint_as_float((b & 1) ? (word & 0xFFFF0000u) : (word << 16));
+        } else {
+            return __half2float(__ushort_as_half((unsigned short)((b & 1) ? (word >> 16) : (word & 0xFFFFu))));
+        }
+    }
+    // Subtraction constant of block b (Unpack::zconst of its zero point):
+    // (magic + z) in both 16-bit lanes, or the f32 2^23 + z.
+    __device__ __forceinline__ static uint32_t zconst(const uint32_t (&z)[ZSW], int b) {
+        const int word = (b % NZS) + NZS * (b / (4 * NZS));
+        const uint32_t byte = (uint32_t)((b / NZS) % 4);
+        const uint32_t sel = kF32Magic ? (0x7440u | byte) : (0x4040u | (byte << 8) | byte);
+        return prmt(z[word], kZHigh, sel);
+    }
+
+    // Adds this item's products to y (rows g, g+8 x tokens 2t, 2t+1); xa is the
+    // shared-memory address of the lane's B fragments of the chunk's first
+    // k-step pair.  M1: one activation row, so only token 0's sums are kept.
+    template <bool M1>
+    __device__ __forceinline__ void compute(uint32_t xa, float (&y)[4]) const {
+        using U = Unpack<BITS, BF16X>;
+        const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc[4];
+        uint32_t zg = 0, zg8 = 0;
+        float sg = 0.f, sg8 = 0.f;
+        uint4 xv = make_uint4(0, 0, 0, 0);
+        uint32_t zs0[ZSW], zs8[ZSW];
+        spread(z0, zshift, zs0);
+        spread(z8, zshift, zs8);
+#pragma unroll
+        for (int s = 0; s < CH; ++s) {
+            if (s % SPB == 0) {
+                const int b = s / SPB;
+                sg = scale(s0, b);
+                sg8 = scale(s8, b);
+                zg = zconst(zs0, b);
+                zg8 = zconst(zs8, b);
+            }
+            if ((s & 1) == 0) {
+                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(xv.x), "=r"(xv.y), "=r"(xv.z), "=r"(xv.w)
+                             : "r"(xa + (uint32_t)(s >> 1) * 64u));
+            }
+            uint32_t a[4];
+            U::kstep(w[s / SPT], s % SPT, zg, zg8, a);
+            const uint32_t b0 = (s & 1) ? xv.z : xv.x, b1 = (s & 1) ? xv.w : xv.y;
+            if (s % SPB == 0) mma16816<BF16X>(acc, a, b0, b1, zero4);
+            else mma16816<BF16X>(acc, a, b0, b1, acc);
+            if (s % SPB == SPB - 1) {
+                y[0] = fmaf(sg, acc[0], y[0]);
+                y[2] = fmaf(sg8, acc[2], y[2]);
+                if constexpr (!M1) {
+                    y[1] = fmaf(sg, acc[1], y[1]);
+                    y[3] = fmaf(sg8, acc[3], y[3]);
+                }
+            }
+        }
+    }
+};
+
+// Position of a warp in its CTA's item list.
+struct Cursor {
+    int i, rt, c;
+    __device__ __forceinline__ void advance(int KC) {
+        i += kW;
+        c += kW;
+        while (c >= KC) {
+            c -= KC;
+            ++rt;
+        }
+    }
+};
+
+template <int BITS, bool BF16X, int SPB_LOG, int SDT, bool M1>
+__global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KGeom geo, int pdl) {
+    using It = Item<BITS, BF16X, SPB_LOG, SDT>;
+    constexpr int CH = It::CH;
+    const Layout& L = p.L;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint4* xs = reinterpret_cast<uint4*>(smem);                  // [M + 1][xrow]: row M is zeros
+    float* red = reinterpret_cast<float*>(smem + geo.x_bytes);   // [max_rt][kW][16][M]
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int M = M1 ? 1 : (int)p.M;
+    const int KC = geo.KC;
+    const int64_t rt0 = (int64_t)blockIdx.x * L.NT / geo.G;
+    const int nrt = (int)((int64_t)(blockIdx.x + 1) * L.NT / geo.G - rt0);
+    const int n_items = nrt * KC;
+    // the packed tiles of (row tile, chunk) follow each other in item order
+    const uint8_t* wbase = p.packed + rt0 * L.KTILES * kTileBytes + lane * 16;
+    auto load = [&](It& b, const Cursor& it) {
+        if (it.i < n_items)
+            b.load(p, wbase + (size_t)(uint32_t)it.i * (size_t)(kTilesPerChunk * kTileBytes), rt0 + it.rt, it.c, g);
+    };
+
+    // ---- 1. this warp's first item (constant data: before the dependency
+    //         wait), X staged in B-fragment order, then the second item: X
+    //         queues behind one item of weights, not two ----
+    It buf[2];
+    Cursor cur = Cursor{warp, warp / KC, warp % KC};
+    Cursor nxt = cur;
+    nxt.advance(KC);
+    load(buf[0], cur);
+    for (int o = tid; o < nrt * kW * 16 * M; o += kThreads) red[o] = 0.f;
+    const int pairs = (int)(L.K / 32);
+    for (int o = tid; o < pairs * 4; o += kThreads) xs[(size_t)M * geo.xrow + o] = make_uint4(0, 0, 0, 0);
+    if (pdl) {
+        griddep_wait();               // X (and Y) may belong to the previous kernel on the stream
+        griddep_launch_dependents();  // after the wait: at most two chained kernels overlap
+    }
+    {
+        // item (m, pair P, lane class tt), k0 = 32 P:
+        // (x[k0 + 2tt..], x[k0 + 8 + 2tt..], x[k0 + 16 + 2tt..], x[k0 + 24 + 2tt..])
+        const uint32_t* x32 = static_cast<const uint32_t*>(p.x);  // K even: rows are 4-byte aligned
+        const int64_t kw = L.K / 2;
+        for (int o = tid; o < M * pairs * 4; o += kThreads) {
+            const int m = o / (pairs * 4), r = o - m * (pairs * 4);
+            const int P = r >> 2, tt = r & 3;
+            const uint32_t* src = x32 + m * kw + P * 16 + tt;
+            xs[(size_t)m * geo.xrow + r] = make_uint4(__ldg(src), __ldg(src + 4), __ldg(src + 8), __ldg(src + 12));
+        }
+    }
+    load(buf[1], nxt);
+    __syncthreads();
+
+    // ---- 2. items, two buffers: compute one while the next is in flight ----
+    const uint32_t xa_lane = smem_u32(xs + (size_t)(g < M ? g : M) * geo.xrow + t);
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+    auto flush = [&](int rt_l) {
+        float* r = red + (size_t)(rt_l * kW + warp) * 16 * M;
+        const int m0 = 2 * t, m1 = 2 * t + 1;
+        if (m0 < M) {
+            r[g * M + m0] = y[0];
+            r[(g + 8) * M + m0] = y[2];
+        }
+        if (!M1 && m1 < M) {
+            r[g * M + m1] = y[1];
+            r[(g + 8) * M + m1] = y[3];
+        }
+        y[0] = y[1] = y[2] = y[3] = 0.f;
+    };
+    // step: compute `cur` from b, refill b with the item after `nxt`, move on
+    auto step = [&](It& b) {
+        b.template compute<M1>(xa_lane + (uint32_t)cur.c * (uint32_t)(CH / 2) * 64u, y);
+        Cursor after = nxt;
+        after.advance(KC);
+        load(b, after);
+        if (nxt.i >= n_items || nxt.rt != cur.rt) flush(cur.rt);
+        cur = nxt;
+        nxt = after;
+        return cur.i < n_items;
+    };
+    if (cur.i < n_items) {
+        while (step(buf[0]) && step(buf[1])) {
+        }
+    }
+    __syncthreads();
+
+    // ---- 4. rows: the 16 warps' partials in a fixed order ----
+    for (int o = tid; o < nrt * 16 * M; o += kThreads) {
+        const int rt_l = o / (16 * M), rem = o - rt_l * 16 * M;
+        const int row = rem / M, m = rem - row * M;
+        const float* src = red + (size_t)rt_l * kW * 16 * M + row * M + m;
+        float v = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < kW; ++w2) v += src[(size_t)w2 * 16 * M];
+        const int64_t n = (rt0 + rt_l) * 16 + row;
+        if (n < L.N) {
+            if (p.bias) v += load_f32(p.bias, n, p.bias_dtype);
+            store_f32(p.y, (int64_t)m * L.N + n, v, p.out_dtype);
+        }
+    }
+    if (blockIdx.x == 0 && tid == 0) verify_header(p.packed_hdr, L, p.status);
+}
+
+template <int BITS, bool BF16X, int SPB_LOG, int SDT>
+cudaError_t launch_k(const MatmulParams& p, const KGeom& geo, cudaStream_t s) {
+    const int pdl = (p.flags & kFlagPDL) ? 1 : 0;
+    auto kern = p.M == 1 ? gemv_ks_kernel<BITS, BF16X, SPB_LOG, SDT, true> : gemv_ks_kernel<BITS, BF16X, SPB_LOG, SDT, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.total_bytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)geo.G);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = geo.total_bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p, geo, pdl);
+}
+
+template <int BITS, bool BF16X, int SPB_LOG>
+cudaError_t launch_sdt(const MatmulParams& p, const KGeom& geo, cudaStream_t s) {
+    constexpr int BPC = chunk_steps(BITS) >> SPB_LOG;
+    switch (p.scale_dtype) {
+        case kF32:
+            if constexpr (BPC * 4 <= 32) return launch_k<BITS, BF16X, SPB_LOG, kF32>(p, geo, s);
+            break;
+        case kF16: return launch_k<BITS, BF16X, SPB_LOG, kF16>(p, geo, s);
+        case kBF16: return launch_k<BITS, BF16X, SPB_LOG, kBF16>(p, geo, s);
+        default: break;
+    }
+    return cudaErrorNotSupported;
+}
+
+template <int BITS, bool BF16X>
+cudaError_t launch_bs(const MatmulParams& p, const KGeom& geo, cudaStream_t s) {
+    constexpr int CH = chunk_steps(BITS);
+    switch (p.L.bs) {
+        case 16:
+            if constexpr (CH <= 16) return launch_sdt<BITS, BF16X, 0>(p, geo, s);
+            break;
+        case 32: return launch_sdt<BITS, BF16X, 1>(p, geo, s);
+        case 64: return launch_sdt<BITS, BF16X, 2>(p, geo, s);
+        case 128: return launch_sdt<BITS, BF16X, 3>(p, geo, s);
+        case 256:
+            if constexpr (CH >= 16) return launch_sdt<BITS, BF16X, 4>(p, geo, s);
+            break;
+        default: break;
+    }
+    return cudaErrorNotSupported;
+}
+
+template <int BITS>
+cudaError_t launch_bits(const MatmulParams& p, const KGeom& geo, cudaStream_t s) {
+    return p.act_dtype == kBF16 ? launch_bs<BITS, true>(p, geo, s) : launch_bs<BITS, false>(p, geo, s);
+}
+
+}  // namespace gks
+}  // namespace mnb

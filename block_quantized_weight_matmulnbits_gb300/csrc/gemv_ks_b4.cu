@@ -1,0 +1,8 @@
+// Instantiation of the k-chunk decode GEMV (gemv_ks.cuh) for 4-bit codes.
+#include "gemv_ks.cuh"
+
+namespace mnb {
+cudaError_t launch_gemv_ks_b4(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s) {
+    return gks::launch_bits<4>(p, geo, s);
+}
+}  // namespace mnb

@@ -1,0 +1,8 @@
+// Instantiation of the k-chunk decode GEMV (gemv_ks.cuh) for 8-bit codes.
+#include "gemv_ks.cuh"
+
+namespace mnb {
+cudaError_t launch_gemv_ks_b8(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s) {
+    return gks::launch_bits<8>(p, geo, s);
+}
+}  // namespace mnb

@@ -1,7 +1,9 @@
-// Host side of the small-batch tensor-core GEMV: four schedules of the same
-// arithmetic.  gemv_mma.cuh (the default): one CTA per row tile.
-// gemv_xr.cuh (M <= 8, a warp slice of at most 16 k-steps): one 16-warp CTA
-// per SM, X in registers, per-warp bulk-copy rings.  gemv_pers.cuh: a persistent cp.async ring.  gemv_stream.cuh:
+// Host side of the small-batch tensor-core GEMV: five schedules of the same
+// arithmetic.  gemv_ks.cuh (the default where it applies: M <= 8, K a
+// multiple of the K-chunk): one 16-warp CTA per SM,
+// (row tile, K-chunk) items streamed through registers.  gemv_mma.cuh (every
+// other shape): one CTA per row tile.  gemv_xr.cuh: one 16-warp CTA per SM,
+// X in registers, per-warp bulk-copy rings.  gemv_pers.cuh: a persistent cp.async ring.  gemv_stream.cuh:
 // persistent with register prefetch.  MNB_GEMV_SCHED=xr|tile|pers|stream
 // forces one (MNB_GEMV_PERS=0/1 still selects between tile and pers).
 #include <cstdlib>
@@ -9,6 +11,7 @@
 
 #include "gemv_pers.cuh"
 #include "gemv_stream.cuh"
+#include "gemv_ks.cuh"
 #include "gemv_xr.cuh"
 
 namespace mnb {
@@ -22,6 +25,9 @@ cudaError_t launch_gemv_pers_b8(const MatmulParams& p, const gpers::PGeom& geo, 
 cudaError_t launch_gemv_stream_b2(const MatmulParams& p, const gstr::SGeom& geo, cudaStream_t s);
 cudaError_t launch_gemv_stream_b4(const MatmulParams& p, const gstr::SGeom& geo, cudaStream_t s);
 cudaError_t launch_gemv_stream_b8(const MatmulParams& p, const gstr::SGeom& geo, cudaStream_t s);
+cudaError_t launch_gemv_ks_b2(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s);
+cudaError_t launch_gemv_ks_b4(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s);
+cudaError_t launch_gemv_ks_b8(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s);
 cudaError_t launch_gemv_xr_b2(const MatmulParams& p, const gxr::XGeom& geo, cudaStream_t s);
 cudaError_t launch_gemv_xr_b4(const MatmulParams& p, const gxr::XGeom& geo, cudaStream_t s);
 cudaError_t launch_gemv_xr_b8(const MatmulParams& p, const gxr::XGeom& geo, cudaStream_t s);
@@ -29,6 +35,18 @@ cudaError_t launch_gemv_xr_b8(const MatmulParams& p, const gxr::XGeom& geo, cuda
 static const char* sched_env() {
     const char* v = std::getenv("MNB_GEMV_SCHED");
     return (v && *v) ? v : nullptr;
+}
+
+// The k-chunk schedule: the default unless another one is forced.
+static bool ks_ok(const MatmulParams& p, gks::KGeom* out) {
+    const char* sc = sched_env();
+    if (sc && std::strcmp(sc, "ks") != 0) return false;
+    if (!sc && std::getenv("MNB_GEMV_PERS")) return false;
+    if ((reinterpret_cast<uintptr_t>(p.scales) & 15) != 0) return false;
+    if (p.zp && (reinterpret_cast<uintptr_t>(p.zp) & 15) != 0) return false;
+    if ((reinterpret_cast<uintptr_t>(p.x) & 3) != 0) return false;
+    const int sms = device_info().sm_count > 0 ? device_info().sm_count : 148;
+    return gks::make_kgeom(p.L, p.M, sms, device_info().smem_optin, p.scale_dtype == kF32 ? 4 : 2, out);
 }
 
 // The register-X schedule (opt-in with MNB_GEMV_SCHED=xr; measured slower
@@ -107,6 +125,15 @@ bool gemv_mma_supported(const MatmulParams& p) {
 }
 
 cudaError_t launch_gemv_mma(const MatmulParams& p, cudaStream_t s) {
+    gks::KGeom kg;
+    if (ks_ok(p, &kg)) {
+        switch (p.L.bits) {
+            case 2: return launch_gemv_ks_b2(p, kg, s);
+            case 4: return launch_gemv_ks_b4(p, kg, s);
+            case 8: return launch_gemv_ks_b8(p, kg, s);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     gxr::XGeom xg;
     if (xr_ok(p, &xg)) {
         switch (p.L.bits) {

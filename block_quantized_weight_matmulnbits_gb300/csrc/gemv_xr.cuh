@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_xr_kernel(MatmulParams p, XG
     {
         const int rows = nrt * 16;
         bool have_raw = geo.raw_copy != 0;
-        if (have_raw && nrows > 0 && !mbar_wait(raw_full, 0, p.status)) have_raw = false;
+        if (have_raw && nrows > 0 && !mbar_wait_lim(raw_full, 0, p.status, p.wait_limit, p.wait_hint_ns)) have_raw = false;
         for (int rr = warp; rr < rows; rr += kW) {  // local row rr: lanes walk its blocks
             const int64_t n = rt0 * 16 + rr;
             Entry* dst = ent + (size_t)rr * L.KB;
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_xr_kernel(MatmulParams p, XG
     bool ok = true;
     for (int r = 0; r < nrt && ok; ++r) {
         const int d = r % D;
-        if (!mbar_wait(&wbar[d], (uint32_t)((r / D) & 1), p.status)) {
+        if (!mbar_wait_lim(&wbar[d], (uint32_t)((r / D) & 1), p.status, p.wait_limit, p.wait_hint_ns)) {
             ok = false;
             break;
         }
@@ -293,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_xr_kernel(MatmulParams p, XG
         }
         // ---- partial sums of row tile r: write, then one warp reduces ----
         const int rb = r & 1;
-        if (r >= 2 && !mbar_wait(&red_free[rb], (uint32_t)(((r >> 1) - 1) & 1), p.status)) {
+        if (r >= 2 && !mbar_wait_lim(&red_free[rb], (uint32_t)(((r >> 1) - 1) & 1), p.status, p.wait_limit,
+                                    p.wait_hint_ns)) {
             ok = false;
             break;
         }
@@ -303,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_xr_kernel(MatmulParams p, XG
         __syncwarp();
         if (lane == 0) mbar_arrive(&red_full[rb]);
         if (warp == r % kW) {
-            if (!mbar_wait(&red_full[rb], (uint32_t)((r >> 1) & 1), p.status)) {
+            if (!mbar_wait_lim(&red_full[rb], (uint32_t)((r >> 1) & 1), p.status, p.wait_limit, p.wait_hint_ns)) {
                 ok = false;
                 break;
             }

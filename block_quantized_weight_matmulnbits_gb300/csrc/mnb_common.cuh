@@ -245,6 +245,20 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same with the call's limits: `limit` tries, each a suspending try_wait
+// with hint_ns (kWaitPoll: test_wait polling, 0: try_wait without a hint).
+__device__ __forceinline__ bool mbar_wait_lim(uint64_t* bar, uint32_t parity, int* status, uint32_t limit,
+                                              uint32_t hint_ns) {
+    for (uint32_t i = 0; i < limit; ++i) {
+        const bool ok = hint_ns == kWaitPoll ? mbar_test_wait(bar, parity)
+                        : hint_ns          ? mbar_try_wait_sleep(bar, parity, hint_ns)
+                                           : mbar_try_wait(bar, parity);
+        if (ok) return true;
+    }
+    set_status(status, 5 /* MNB_ERR_TIMEOUT */);
+    return false;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
     for (uint32_t i = 0; i < kWaitLimit; ++i) {
         if (mbar_try_wait_sleep(bar, parity, kWaitHintNs)) return true;

@@ -136,7 +136,7 @@ PERS_CASES = [
 
 
 @pytest.mark.parametrize("M,bits,bs,dt,asym,N,K", PERS_CASES)
-@pytest.mark.parametrize("sched", ["xr", "stream", "pers", "tile"])
+@pytest.mark.parametrize("sched", ["ks", "xr", "stream", "pers", "tile"])
 def test_matmul_gemv_schedules(G, monkeypatch, M, bits, bs, dt, asym, N, K, sched):
     monkeypatch.setenv("MNB_GEMV_SCHED", sched)
     w = _w(M, N, K, bits, bs, dt, asym, 900 + M * 13 + bits * 7 + bs + N)
@@ -144,6 +144,38 @@ def test_matmul_gemv_schedules(G, monkeypatch, M, bits, bs, dt, asym, N, K, sche
     y = P.y64(P.run("gemv_mma"))
     ref, mag = P.oracle_full()
     G.assert_within(y, ref, mag, w.out_dtype, f"gemv_mma {sched} {w.name}")
+
+
+# Shapes the k-chunk schedule takes (K a multiple of 4 packed tiles): every
+# code width, block size and scale type it serves, ragged N, a partial last
+# CTA, with and without zero points.
+KS_CASES = [
+    (1, 4, 32, (BF16, BF16, BF16), True, 4801, 4096),
+    (1, 4, 128, (F16, F16, F16), False, 1000, 2048),
+    (2, 2, 64, (BF16, BF16, F32), True, 333, 1536),
+    (8, 2, 32, (BF16, BF16, BF16), True, 3000, 2048),
+    (5, 8, 32, (F16, F16, F16), True, 777, 1152),
+    (3, 8, 128, (BF16, BF16, BF16), False, 2500, 11008),
+    (1, 4, 256, (BF16, BF16, BF16), True, 150, 768),
+    (7, 4, 16, (F16, F16, F32), True, 4800, 512),
+    (1, 2, 256, (F16, F16, F16), True, 16, 1024),
+    (4, 8, 16, (BF16, BF16, BF16), True, 40, 256),
+    (1, 4, 32, (BF16, F16, BF16), True, 11008, 4096),
+    (1, 8, 128, (F16, F32, F16), True, 1000, 11008),
+    (8, 2, 64, (BF16, F16, BF16), True, 2000, 4096),
+    (2, 4, 64, (F16, BF16, F32), False, 500, 1024),
+    (6, 2, 128, (BF16, F32, F32), True, 700, 2048),
+]
+
+
+@pytest.mark.parametrize("M,bits,bs,dt,asym,N,K", KS_CASES)
+def test_matmul_gemv_ks(G, monkeypatch, M, bits, bs, dt, asym, N, K):
+    monkeypatch.setenv("MNB_GEMV_SCHED", "ks")
+    w = _w(M, N, K, bits, bs, dt, asym, 950 + M * 13 + bits * 7 + bs + N)
+    P = G.Problem(w)
+    y = P.y64(P.run("gemv_mma"))
+    ref, mag = P.oracle_full()
+    G.assert_within(y, ref, mag, w.out_dtype, f"gemv_mma ks {w.name}")
 
 
 TC_CASES = []

@@ -116,6 +116,24 @@ def test_worst_case_float_kernels(G, monkeypatch, kernel, M, env, bits, bs, act,
     check(G, _wl(M, N, K, bits, bs, act, sdt, zpm), data, kernel, x_mode)
 
 
+# The k-chunk decode schedule takes K a multiple of 4 packed tiles (1024 /
+# bits depths) and at most 32 bytes of scales per row and chunk.
+KS_SHAPES = [(4, 32, BF16, BF16, "low"), (4, 16, F16, F16, "none"), (2, 64, BF16, F16, "low"),
+             (2, 256, F16, F16, "low"), (8, 32, BF16, BF16, "low"), (8, 128, F16, F32, "none"),
+             (4, 256, BF16, F32, "low"), (4, 32, BF16, F32, "low"), (2, 64, F16, F32, "low")]
+
+
+@pytest.mark.parametrize("x_mode", ["one_hot", "positive"])
+@pytest.mark.parametrize("bits,bs,act,sdt,zpm", KS_SHAPES)
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_worst_case_gemv_ks(G, monkeypatch, M, bits, bs, act, sdt, zpm, x_mode):
+    monkeypatch.setenv("MNB_GEMV_SCHED", "ks")
+    N, K = 150, 3 * (1024 // bits)
+    extra = F32_EXTRA if sdt == F32 else ()
+    data = build(M, N, K, bits, bs, act, sdt, zpm, x_mode, 4300 + M + bits + bs, extra)
+    check(G, _wl(M, N, K, bits, bs, act, sdt, zpm), data, "gemv_mma", x_mode)
+
+
 @pytest.mark.parametrize("x_mode", ["one_hot", "positive"])
 @pytest.mark.parametrize("bits,bs,sdt,zpm", [(4, 32, F32, "low"), (8, 128, F32, "none"), (2, 16, F16, "low")])
 def test_worst_case_f32_activation_gemv(G, bits, bs, sdt, zpm, x_mode):
