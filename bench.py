@@ -446,6 +446,50 @@ def run_ours(args):
                              "algorithmic_bytes": step_bytes, "peak_source": f"{pk_src} hbm_gbs"},
                 "clocks": ck, "weight_copies": R}, steps
 
+    def measure_fp(fmt: int, M: int, N: int, K: int, steps: int, warmup: int):
+        """FP8 (E4M3, f32 column scales) or NVFP4 (E4M3 block scales x global) weights, bf16 X and Y:
+        native-format bytes (codes, scales, X, Y) per step."""
+        rng = np.random.default_rng(wl.SEED_BASE + 50 + fmt)
+        act, out = wl.BF16, wl.BF16
+        if fmt == mnb.MNB_WF_NVFP4:
+            kb = -(-K // 16)
+            codes = rng.integers(0, 256, size=(K * N + 1) // 2).astype(np.uint8)
+            sc = torch.from_numpy(rng.choice([c for c in range(0x08, 0x40)], size=(kb, N)).astype(np.uint8)).cuda()
+            name, wbytes, sbytes = f"decode_m{M}_k{K}_n{N}_nvfp4_bf16", (K * N + 1) // 2, kb * N
+        else:
+            codes = rng.choice([c for c in range(256) if (c >> 3) & 15 != 15], size=K * N).astype(np.uint8)
+            sc = torch.from_numpy(rng.uniform(1e-3, 1e-2, size=N).astype(np.float32)).cuda()
+            name, wbytes, sbytes = f"decode_m{M}_k{K}_n{N}_fp8e4m3_bf16", K * N, 4 * N
+        wdev = torch.from_numpy(codes).cuda()
+        packed = aligned_empty(mnb.mnb_fp_packed_size(N, K, fmt))
+        mnb.mnb_pack_fp_weights(wdev, packed, N, K, fmt)
+        del wdev
+        x = to_dev(wl.to_storage(rng.standard_normal((M, K)), act), act)
+        yb = torch.empty((M, N), dtype=TORCH_DT[out], device="cuda")
+        l2 = torch.cuda.get_device_properties(local).L2_cache_size
+        R = max(2, math.ceil(3 * l2 / (packed.numel() + sbytes)))
+        copies = [(packed, sc)]
+        for _ in range(R - 1):
+            pb = aligned_empty(packed.numel())
+            pb.copy_(packed)
+            copies.append((pb, sc.clone()))
+        stream = torch.cuda.Stream()
+
+        def call(i):
+            pb, s = copies[i % R]
+            mnb.mnb_matmul_fp(x, pb, s, 0.05, yb, M, N, K, fmt, act, out, stream=stream)
+
+        t, ck = replay_timed(call, steps, warmup, stream)
+        per_step = (wbytes + sbytes + M * K * 2 + M * N * 2) / 1e9
+        per_launch_s = t / steps
+        achieved = per_step / per_launch_s
+        return {"workload": name, "value": whole_job_value(world, steps, per_step, t), "unit": "GB/s",
+                "kernel": "fp_generic", "ms_per_step": per_launch_s * 1e3, "steps": steps,
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                             "frac": achieved / pk["hbm_gbs"], "traffic": traffic_for(f"fp_generic:{name}"),
+                             "algorithmic_bytes": int(per_step * 1e9), "peak_source": f"{pk_src} hbm_gbs"},
+                "clocks": ck, "weight_copies": R}, steps
+
     w = wl.config(args.config)
     main, data = measure(w, args.steps, args.warmup, args.kernel, True, args.accuracy_level)
     res = {
@@ -484,6 +528,10 @@ def run_ours(args):
         moe, n = measure_moe(wl.MOE_CONFIGS[0], max(20, args.steps // 10), max(3, args.warmup // 10))
         res["moe"] = moe
         res["gpu_launches"] += n
+        for key, fmt in (("fp8", mnb.MNB_WF_E4M3), ("nvfp4", mnb.MNB_WF_NVFP4)):
+            fo, n = measure_fp(fmt, 1, 11008, 4096, max(20, args.steps // 10), sw)
+            res[key] = fo
+            res["gpu_launches"] += n
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = cpu_oracle_rate(w, data, args.cpu_seconds)
         res["cpu_baseline"] = {"value": v, "unit": main["unit"], "cores": cores, "kind": "oracle", "sample": sample}

@@ -18,6 +18,7 @@ MNB_OK, MNB_ERR_INVALID_ARG, MNB_ERR_UNSUPPORTED, MNB_ERR_CUDA, MNB_ERR_NO_MEM, 
     MNB_ERR_LAYOUT_MISMATCH = range(7)
 MNB_F32, MNB_F16, MNB_BF16 = 0, 1, 2
 MNB_FLAG_PDL = 1
+MNB_WF_E4M3, MNB_WF_E5M2, MNB_WF_NVFP4 = 1, 2, 3
 KERNELS = {"auto": 0, "gemv": 1, "gemv_mma": 2, "gemm_tc": 3, "generic": 4, "gemv_i8": 5}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
 
@@ -26,7 +27,7 @@ EXPORTS = [
     "mnb_packed_size", "mnb_pack_weights", "mnb_unpack_codes", "mnb_dequantize", "mnb_matmul",
     "mnb_matmul_ex", "mnb_workspace_size", "mnb_quantize_activations", "mnb_select_kernel",
     "mnb_get_device_error", "mnb_status_string", "mnb_kernel_name", "mnb_abi_version", "mnb_matmul_a8_static",
-    "mnb_matmul_host_io", "mnb_matmul_grouped",
+    "mnb_matmul_host_io", "mnb_matmul_grouped", "mnb_fp_packed_size", "mnb_pack_fp_weights", "mnb_matmul_fp",
 ]
 MNB_A8_STATIC_SCRATCH_BYTES = 1 << 20
 MNB_HOST_IO_X_BYTES = 8 << 20
@@ -85,6 +86,9 @@ def load(build: bool = True):
             "mnb_matmul_host_io": (ci, [ctypes.POINTER(MatmulArgs)]),
             "mnb_matmul_grouped": (ci, [vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, i64, i64, ci, ci, ci, ci, ci,
                                         vp]),
+            "mnb_fp_packed_size": (sz, [i64, i64, ci]),
+            "mnb_pack_fp_weights": (ci, [vp, vp, sz, i64, i64, ci, vp]),
+            "mnb_matmul_fp": (ci, [vp, vp, vp, ctypes.c_float, vp, i64, i64, i64, ci, ci, ci, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -198,6 +202,22 @@ def mnb_matmul_grouped(x, ids, packed_b, scales, zero_points, y, T, S, E, N, K, 
     _check(load().mnb_matmul_grouped(_ptr(x), _ptr(ids), _ptr(packed_b), _ptr(scales), _ptr(zero_points), _ptr(y),
                                      T, S, E, 1 if x_per_slot else 0, N, K, bits, block_size, act_dtype, out_dtype,
                                      scale_dtype, _stream(stream)), "mnb_matmul_grouped")
+
+
+def mnb_fp_packed_size(N, K, fmt) -> int:
+    return load().mnb_fp_packed_size(N, K, fmt)
+
+
+def mnb_pack_fp_weights(w_kn, packed, N, K, fmt, stream=None):
+    """Re-tile a [K, N] FP8 / NVFP4 weight (device uint8) for mnb_matmul_fp."""
+    _check(load().mnb_pack_fp_weights(_ptr(w_kn), _ptr(packed), packed.numel() * packed.element_size(), N, K, fmt,
+                                      _stream(stream)), "mnb_pack_fp_weights")
+
+
+def mnb_matmul_fp(x, packed, scales, global_scale, y, M, N, K, fmt, act_dtype, out_dtype, stream=None):
+    """Y = X . W for an FP8 (scales f32 [N] or None) or NVFP4 (e4m3 [ceil(K/16), N] scales) weight."""
+    _check(load().mnb_matmul_fp(_ptr(x), _ptr(packed), _ptr(scales), float(global_scale), _ptr(y), M, N, K, fmt,
+                                act_dtype, out_dtype, _stream(stream)), "mnb_matmul_fp")
 
 
 def mnb_workspace_size(M, N, K, bits, block_size, accuracy_level) -> int:

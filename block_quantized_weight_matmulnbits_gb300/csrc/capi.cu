@@ -261,6 +261,63 @@ mnb_status mnb_dequantize(const void* packed_b, const void* scales, const uint8_
                                     zero_points, w_nk, L, (cudaStream_t)stream));
 }
 
+static_assert((int)MNB_WF_E4M3 == kWfE4M3 && (int)MNB_WF_E5M2 == kWfE5M2 && (int)MNB_WF_NVFP4 == kWfNVFP4,
+              "weight format codes of the C API and the kernels agree");
+
+static bool valid_fp(int64_t N, int64_t K, int format) {
+    return N > 0 && K > 0 && N <= (int64_t(1) << 31) && K <= (int64_t(1) << 31) &&
+           (format == MNB_WF_E4M3 || format == MNB_WF_E5M2 || format == MNB_WF_NVFP4);
+}
+
+size_t mnb_fp_packed_size(int64_t N, int64_t K, mnb_wformat format) {
+    if (!valid_fp(N, K, format)) return 0;
+    Layout L;
+    fp_layout(&L, N, K, format);
+    return L.total_bytes();
+}
+
+mnb_status mnb_pack_fp_weights(const uint8_t* w_kn, void* packed, size_t packed_bytes, int64_t N, int64_t K,
+                               mnb_wformat format, mnb_stream_t stream) {
+    if (!valid_fp(N, K, format) || !w_kn || !packed || !aligned(packed, 256)) return MNB_ERR_INVALID_ARG;
+    Layout L;
+    fp_layout(&L, N, K, format);
+    if (packed_bytes < L.total_bytes()) return MNB_ERR_NO_MEM;
+    if (inject_launch_failure()) return MNB_ERR_CUDA;
+    return from_cuda(launch_pack(w_kn, static_cast<uint8_t*>(packed), L, (cudaStream_t)stream, format));
+}
+
+mnb_status mnb_matmul_fp(const void* x, const void* packed, const void* scales, float global_scale, void* y,
+                         int64_t M, int64_t N, int64_t K, mnb_wformat format, mnb_dtype act_dtype,
+                         mnb_dtype out_dtype, mnb_stream_t stream) {
+    if (!valid_fp(N, K, format) || M < 0 || !valid_dtype(act_dtype) || !valid_dtype(out_dtype))
+        return MNB_ERR_INVALID_ARG;
+    if (M == 0) return MNB_OK;
+    if (!x || !packed || !y || (format == MNB_WF_NVFP4 && !scales)) return MNB_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(packed, 256) ||
+        (format != MNB_WF_NVFP4 && scales && !aligned(scales, 4)))
+        return MNB_ERR_INVALID_ARG;
+    PerDevice* pd = per_device();
+    if (!pd) return from_cuda(cudaGetLastError());
+    FpParams p{};
+    p.x = x;
+    p.packed_hdr = packed;
+    p.packed = static_cast<const uint8_t*>(packed) + kHeaderBytes;
+    p.scales = scales;
+    p.global_scale = global_scale;
+    p.y = y;
+    p.M = M;
+    fp_layout(&p.L, N, K, format);
+    p.fmt = format;
+    p.act_dtype = act_dtype;
+    p.out_dtype = out_dtype;
+    p.status = pd->status;
+    if (inject_launch_failure()) return MNB_ERR_CUDA;
+    if (log_enabled())
+        std::fprintf(stderr, "[mnb] matmul_fp M=%lld N=%lld K=%lld format=%d kernel=fp_generic\n", (long long)M,
+                     (long long)N, (long long)K, (int)format);
+    return from_cuda(launch_fp_generic(p, (cudaStream_t)stream));
+}
+
 size_t mnb_workspace_size(int64_t M, int64_t N, int64_t K, int bits, int block_size, int accuracy_level) {
     if (!valid_shape(N, K, bits, block_size) || M < 0) return 0;
     if (accuracy_level != 4) return 0;

@@ -38,6 +38,33 @@ void wait_limits(uint32_t* limit, uint32_t* hint_ns);
 
 constexpr int kFlagPDL = 1;  // == MNB_FLAG_PDL
 
+// A matmul with a floating-point weight format (WFormat kWfE4M3, kWfE5M2,
+// kWfNVFP4): FP8 scales are f32 [N] or null, NVFP4 scales are E4M3 bytes
+// [ceil(K / 16), N] times global_scale.
+struct FpParams {
+    const void* x;
+    const uint8_t* packed;   // tile data (header already skipped)
+    const void* packed_hdr;
+    const void* scales;
+    float global_scale;
+    void* y;
+    int64_t M;
+    Layout L;
+    int fmt;
+    int act_dtype, out_dtype;
+    int* status;
+    int flags;
+};
+
+// The packed layout of a floating-point format: FP8 as 8-bit codes with
+// 128-deep tiling blocks, NVFP4 as 4-bit codes with its 16-deep scale blocks.
+inline void fp_layout(Layout* L, int64_t N, int64_t K, int fmt) {
+    if (fmt == kWfNVFP4) L->init(N, K, 4, 16);
+    else L->init(N, K, 8, 128);
+}
+
+cudaError_t launch_fp_generic(const FpParams& p, cudaStream_t s);
+
 cudaError_t launch_pack(const uint8_t* b_ort, uint8_t* packed_hdr, const Layout& L, cudaStream_t s,
                         int fmt = kWfInt);
 cudaError_t launch_unpack(const uint8_t* packed, uint8_t* b_ort, const Layout& L, cudaStream_t s);

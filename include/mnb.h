@@ -148,9 +148,10 @@ MNB_API mnb_status mnb_matmul(const void* x, const void* packed_b, const void* s
 /* Extended call: everything of mnb_matmul plus
  *   g_idx          device int32 [K] or NULL: group (scale/zero-point column) of
  *                  each depth, each in [0, KB) (onnx-runtime-ep-cpu matmul_nbits.rs,
- *                  MatMulNBitsKernel::dequantize_weight, grouped path).  Values are
- *                  not range-checked on the device; out-of-range values are the
- *                  caller's error.  Only MNB_KERNEL_GENERIC handles g_idx.
+ *                  MatMulNBitsKernel::dequantize_weight, grouped path).  The kernel
+ *                  checks every value: a depth whose group is outside [0, KB)
+ *                  sets MNB_ERR_INVALID_ARG in the device status word and the call
+ *                  writes no element of Y.  Only MNB_KERNEL_GENERIC handles g_idx.
  *   bias           device [N] of bias_dtype or NULL, added after the product
  *                  (MatMulNBitsKernel::execute).
  *   accuracy_level 0..3: float path.  4: activations quantised per K-block to
@@ -283,19 +284,68 @@ MNB_API mnb_status mnb_matmul_grouped(const void* x, const int32_t* ids, const v
 #define MNB_HOST_IO_X_BYTES (8u << 20)
 MNB_API mnb_status mnb_matmul_host_io(const mnb_matmul_args* args);
 
+/* ---- floating-point weight formats --------------------------------------
+ * dequant_matmul_fp8 and dequant_matmul_nvfp4 of rlx-cpu 0.2.13,
+ * src/thunk/ops/quant.rs: Y[m, n] = sum_k X[m, k] * w(k, n) with
+ *   FP8:   w(k, n) = fp8(W[k, n]) * s[n]   (s = 1 when scales is NULL), one f32
+ *          rounding; E4M3 as that page decodes it (bias 7, exponent 15 is
+ *          infinity for a zero mantissa and NaN otherwise), or E5M2;
+ *   NVFP4: w(k, n) = f32(f32(e2m1(W[k, n]) * e4m3(S[k / 16, n])) * global_scale),
+ *          OCP E2M1 codes and OCP E4M3 ("fn") block scales, two f32 roundings.
+ * The weights are re-tiled once like the integer codes (the same 512-byte
+ * tiles: FP8 as 8-bit codes, NVFP4 as 4-bit codes); the products are
+ * accumulated in f32 and the result rounded once to out_dtype.  Non-finite
+ * weights propagate as IEEE arithmetic does. */
+
+typedef enum mnb_wformat { MNB_WF_E4M3 = 1, MNB_WF_E5M2 = 2, MNB_WF_NVFP4 = 3 } mnb_wformat;
+
+/* Bytes of the packed buffer for an N x K weight of `format`, or 0 if the
+ * arguments are invalid. */
+MNB_API size_t mnb_fp_packed_size(int64_t N, int64_t K, mnb_wformat format);
+
+/* Re-tile a [K, N] weight (device, any alignment; FP8: K*N bytes, row-major,
+ * element (k, n) at k*N + n; NVFP4: ceil(K*N/2) bytes, element (k, n) is the
+ * nibble of flat index k*N + n, low nibble first) into packed (device,
+ * 256-byte aligned, packed_bytes >= mnb_fp_packed_size()).  Codes are moved,
+ * never changed; depths past K are zero codes (+0).  MNB_ERR_NO_MEM if
+ * packed_bytes is too small. */
+MNB_API mnb_status mnb_pack_fp_weights(const uint8_t* w_kn, void* packed, size_t packed_bytes, int64_t N,
+                               int64_t K, mnb_wformat format, mnb_stream_t stream);
+
+/* Y = X . W with the weight packed by mnb_pack_fp_weights for the same N, K
+ * and format.
+ *   x        device [M, K] act_dtype, row-major (16-byte aligned)
+ *   scales   FP8: device f32 [N] (4-byte aligned) or NULL;
+ *            NVFP4: device uint8 [ceil(K/16), N] E4M3 block scales (required)
+ *   global_scale  NVFP4 only (ignored for FP8)
+ *   y        device [M, N] out_dtype, row-major (16-byte aligned)
+ * A header that does not match (N, K, format) sets MNB_ERR_LAYOUT_MISMATCH in
+ * the device status word.  M == 0 is a no-op. */
+MNB_API mnb_status mnb_matmul_fp(const void* x, const void* packed, const void* scales, float global_scale,
+                         void* y, int64_t M, int64_t N, int64_t K, mnb_wformat format, mnb_dtype act_dtype,
+                         mnb_dtype out_dtype, mnb_stream_t stream);
+
 /* ---- diagnostics ------------------------------------------------------- */
 
 /* Environment overrides, read at each call (none changes a result beyond
  * rounding order; none is needed for normal use):
  *   MNB_LOG=1              print the kernel family chosen for each call
  *   MNB_GEMV_MAX_M         largest M routed to the decode GEMV (default 16)
- *   MNB_GEMV_PERS=0|1      force the per-tile or the persistent decode GEMV
+ *   MNB_GEMV_SCHED=ks|tile|pers|stream|xr
+ *                          force one schedule of the tensor-core decode GEMV
+ *                          (default: the K-chunk schedule where it applies,
+ *                          else one CTA per row tile)
+ *   MNB_GEMV_PERS=0|1      per-tile or persistent decode GEMV when no
+ *                          schedule is forced
  *   MNB_MMA_TPW, MNB_I8_TPW  k-tiles per warp of the decode / int8 GEMV (1..8)
- *   MNB_TC_TA=0            prefill GEMM dequantises into shared memory
- *                          instead of tensor memory
- *   MNB_TC_BN, MNB_TC_STAGES, MNB_TC_NO_SCALE_TMA=1
- *                          tile width, ring depth and scale path of the
- *                          shared-memory prefill GEMM
+ *   MNB_TC_KERNEL=bs       prefill GEMM for bf16 X with per-block partial sums
+ *                          instead of the hi/lo weight split
+ *   MNB_TC_BT=32|64|128    token tile of the block-scaled prefill GEMM
+ *   MNB_TC_SPLITK=0|1      K split over a 2-CTA cluster in the hi/lo GEMM
+ *   MNB_WAIT_MODE=0|1|2    bounded mbarrier waits: suspend with a time hint,
+ *                          try_wait without a hint, or test_wait polling
+ *   MNB_WAIT_LIMIT=n       test hook: n tries per bounded wait (then
+ *                          MNB_ERR_TIMEOUT in the status word)
  *   MNB_GEMV_STAGE_BUFS, MNB_GEMV_MAX_SLOTS  ring shape of the f32 GEMV
  *   MNB_MOE_SETS           expert sets per row tile of mnb_matmul_grouped
  *   MNB_FAIL_LAUNCH=1      test hook: every launch reports MNB_ERR_CUDA

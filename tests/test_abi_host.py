@@ -56,6 +56,30 @@ def test_packed_size_rejects_invalid(bad):
     assert mnb.mnb_packed_size(*bad) == 0
 
 
+@pytest.mark.parametrize("N,K", [(4096, 4096), (37, 300), (1, 1), (150, 261)])
+def test_fp_packed_size_formula(N, K):
+    nt = -(-N // 16)
+    # FP8: 8-bit codes in 128-deep blocks, 32 depths per tile
+    assert mnb.mnb_fp_packed_size(N, K, mnb.MNB_WF_E4M3) == 256 + nt * (-(-K // 128) * 128 // 32) * 512
+    assert mnb.mnb_fp_packed_size(N, K, mnb.MNB_WF_E5M2) == mnb.mnb_fp_packed_size(N, K, mnb.MNB_WF_E4M3)
+    # NVFP4: 4-bit codes in 16-deep scale blocks, 64 depths per tile
+    assert mnb.mnb_fp_packed_size(N, K, mnb.MNB_WF_NVFP4) == 256 + nt * (-(-(-(-K // 16) * 16) // 64)) * 512
+
+
+@pytest.mark.parametrize("bad", [(0, 64, 1), (8, 0, 1), (8, 64, 0), (8, 64, 4), (-1, 64, 3)])
+def test_fp_packed_size_rejects_invalid(bad):
+    assert mnb.mnb_fp_packed_size(*bad) == 0
+
+
+def test_fp_matmul_rejects_invalid_before_cuda():
+    """Argument errors come back before any CUDA call (null pointers, NVFP4 without scales)."""
+    lib = mnb.load()
+    assert lib.mnb_matmul_fp(None, None, None, 1.0, None, 1, 8, 8, 3, 0, 0, None) == mnb.MNB_ERR_INVALID_ARG
+    assert lib.mnb_matmul_fp(None, None, None, 1.0, None, 0, 8, 8, 1, 0, 0, None) == mnb.MNB_OK  # M == 0
+    assert lib.mnb_matmul_fp(None, None, None, 1.0, None, 1, 8, 8, 9, 0, 0, None) == mnb.MNB_ERR_INVALID_ARG
+    assert lib.mnb_pack_fp_weights(None, None, 0, 8, 8, 1, None) == mnb.MNB_ERR_INVALID_ARG
+
+
 def test_kernel_selection():
     assert mnb.mnb_select_kernel(1, 11008, 4096, 4, 32, mnb.MNB_BF16) == "gemv_mma"
     assert mnb.mnb_select_kernel(1, 4096, 11008, 8, 128, mnb.MNB_F16) == "gemv_mma"

@@ -1,0 +1,210 @@
+"""FP8 (E4M3 / E5M2) and NVFP4 weights on the GPU against the oracle:
+dequant_matmul_fp8 and dequant_matmul_nvfp4 of rlx-cpu 0.2.13,
+src/thunk/ops/quant.rs.
+
+* One-hot activation rows read single weights, so every one of the 256 FP8
+  codes (and every E2M1 nibble under every E4M3 block-scale code) is compared
+  bit for bit with the oracle's decode.
+* The page's E4M3 rule makes exponent 15 infinite (zero mantissa) or NaN;
+  columns holding such codes must come out non-finite exactly where the
+  oracle's do.
+* Random activations at ragged shapes (partial 16-deep NVFP4 scale blocks,
+  N not a multiple of 16) are held to the per-element bound
+  |y - y_ref| <= 2e-3 * sum_k |x_k w_k| + 1e-6 (+ half an output ulp)."""
+import numpy as np
+import pytest
+import torch
+
+import block_quantized_weight_matmulnbits_gb300 as mnb
+import oracle
+from block_quantized_weight_matmulnbits_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+F32, F16, BF16 = wl.F32, wl.F16, wl.BF16
+
+
+@pytest.fixture(scope="module")
+def G(mnb_lib):
+    from tests import _gpu
+    return _gpu
+
+
+@pytest.fixture(scope="module")
+def mnb_lib():
+    return mnb.load()
+
+
+def _pack(G, w_kn_bytes, N, K, fmt):
+    w = torch.from_numpy(np.ascontiguousarray(w_kn_bytes)).cuda()
+    packed = G.aligned_empty(mnb.mnb_fp_packed_size(N, K, fmt))
+    mnb.mnb_pack_fp_weights(w, packed, N, K, fmt)
+    return packed
+
+
+def _run(G, x_stored, act, packed, scales_t, gs, M, N, K, fmt, out_dtype):
+    x = G.to_dev(x_stored, act)
+    y = torch.empty((M, N), dtype=G.TORCH_DT[out_dtype], device="cuda")
+    mnb.mnb_matmul_fp(x, packed, scales_t, gs, y, M, N, K, fmt, act, out_dtype)
+    torch.cuda.synchronize()
+    assert mnb.mnb_get_device_error() == mnb.MNB_OK
+    return G.to_host_f64(y, out_dtype)
+
+
+def _nibbles(codes_kn):
+    """[K, N] nibble codes to the packed byte stream (flat index k*N + n, low nibble first)."""
+    flat = np.asarray(codes_kn, dtype=np.uint8).ravel()
+    if flat.size % 2:
+        flat = np.concatenate([flat, np.zeros(1, np.uint8)])
+    return (flat[0::2] | (flat[1::2] << 4)).astype(np.uint8)
+
+
+def _same_class(y, ref):
+    """Non-finite elements agree in kind (NaN, +inf, -inf); returns the finite mask."""
+    assert np.array_equal(np.isnan(y), np.isnan(ref))
+    assert np.array_equal(np.isposinf(y), np.isposinf(ref))
+    assert np.array_equal(np.isneginf(y), np.isneginf(ref))
+    return np.isfinite(ref)
+
+
+def _finite_fp8_codes(e5m2):
+    c = np.arange(256, dtype=np.uint8)
+    exp = (c >> 2) & 31 if e5m2 else (c >> 3) & 15
+    return c[exp != (31 if e5m2 else 15)]
+
+
+@pytest.mark.parametrize("fmt", [mnb.MNB_WF_E4M3, mnb.MNB_WF_E5M2])
+@pytest.mark.parametrize("with_scales", [False, True])
+def test_fp8_every_code_one_hot(G, fmt, with_scales):
+    """Y row m = W row m (x one-hot at k = m): each finite code times its column scale, rounded once
+    to f32 (the page's acc += x * w * s with x = 1)."""
+    e5m2 = fmt == mnb.MNB_WF_E5M2
+    codes = _finite_fp8_codes(e5m2)
+    N, K = 150, len(codes) // 2 + 7
+    rng = np.random.default_rng(61 + fmt)
+    w = rng.choice(codes, size=(K, N)).astype(np.uint8)
+    w.reshape(-1)[: len(codes)] = codes  # every finite code at least once
+    s = rng.uniform(0.25, 4.0, size=N).astype(np.float32) if with_scales else None
+    M = K
+    x = np.eye(M, K)
+    packed = _pack(G, w, N, K, fmt)
+    st = None if s is None else torch.from_numpy(s).cuda()
+    y = _run(G, wl.to_storage(x, F32), F32, packed, st, 0.0, M, N, K, fmt, F32)
+    ref, _ = oracle.matmul_fp8(x, w, s, K, N, e5m2=e5m2)
+    # the oracle's product w * s is exact (fp64); a one-hot row returns it rounded once to f32
+    assert np.array_equal(y, ref.astype(np.float32).astype(np.float64))
+
+
+@pytest.mark.parametrize("fmt", [mnb.MNB_WF_E4M3, mnb.MNB_WF_E5M2])
+def test_fp8_non_finite_codes(G, fmt):
+    """Infinity and NaN codes (exponent all ones) poison exactly the columns that hold them."""
+    e5m2 = fmt == mnb.MNB_WF_E5M2
+    N, K, M = 40, 33, 3
+    rng = np.random.default_rng(7 + fmt)
+    w = rng.choice(_finite_fp8_codes(e5m2), size=(K, N)).astype(np.uint8)
+    specials = [0x7C, 0xFC, 0x7D, 0x7F] if e5m2 else [0x78, 0xF8, 0x79, 0xFF]  # +inf, -inf, NaN, NaN
+    for j, code in enumerate(specials):
+        w[5 + j, 3 * j + 1] = code
+    x = rng.uniform(0.5, 1.0, size=(M, K))
+    packed = _pack(G, w, N, K, fmt)
+    y = _run(G, wl.to_storage(x, F32), F32, packed, None, 0.0, M, N, K, fmt, F32)
+    ref, mag = oracle.matmul_fp8(x, w, None, K, N, e5m2=e5m2)
+    fin = _same_class(y, ref)
+    assert (~fin).sum() == M * len(specials)
+    G.assert_within(np.where(fin, y, 0), np.where(fin, ref, 0), np.where(fin, mag, 0), F32, "fp8 finite columns")
+
+
+def test_nvfp4_every_nibble_and_scale_code_one_hot(G):
+    """Every E2M1 nibble under every E4M3 block-scale code, formed as the page forms it."""
+    N = 256
+    K = 16 * 16 + 5  # 17 scale blocks, the last partial
+    KB = -(-K // 16)
+    rng = np.random.default_rng(404)
+    w4 = rng.integers(0, 16, size=(K, N)).astype(np.uint8)
+    w4[:16, :] = np.arange(16, dtype=np.uint8)[:, None]  # block 0: all nibbles in every column
+    finite_scales = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    s8 = rng.choice(finite_scales, size=(KB, N)).astype(np.uint8)
+    s8[0, :] = np.arange(256, dtype=np.uint8)  # block 0: every scale code (NaN ones included), one per column
+    gs = np.float32(0.7351)
+    M = K
+    x = np.eye(M, K)
+    packed = _pack(G, _nibbles(w4), N, K, mnb.MNB_WF_NVFP4)
+    y = _run(G, wl.to_storage(x, F32), F32, packed, torch.from_numpy(s8).cuda(), float(gs), M, N, K,
+             mnb.MNB_WF_NVFP4, F32)
+    ref, _ = oracle.matmul_nvfp4(x, _nibbles(w4), s8, float(gs), K, N)
+    fin = _same_class(y, ref)
+    assert np.array_equal(y[fin], ref[fin])
+    # block-0 columns with the scale NaN codes (0x7F, 0xFF) are the only non-finite ones
+    assert set(np.nonzero(~fin)[1].tolist()) == {0x7F, 0xFF}
+
+
+CASES = [
+    # (M, N, K, act, out)
+    (1, 4096, 4096, BF16, BF16),
+    (1, 333, 1000, F16, F16),
+    (7, 150, 261, F32, F32),
+    (33, 77, 512, BF16, F32),
+    (16, 1024, 130, F16, BF16),
+]
+
+
+@pytest.mark.parametrize("M,N,K,act,out", CASES)
+@pytest.mark.parametrize("fmt", [mnb.MNB_WF_E4M3, mnb.MNB_WF_E5M2])
+def test_fp8_random(G, M, N, K, act, out, fmt):
+    e5m2 = fmt == mnb.MNB_WF_E5M2
+    rng = np.random.default_rng(M * 131 + N + K + fmt)
+    w = rng.choice(_finite_fp8_codes(e5m2), size=(K, N)).astype(np.uint8)
+    s = rng.uniform(1e-3, 1e-2, size=N).astype(np.float32)
+    x = rng.standard_normal((M, K))
+    xs = wl.to_storage(x, act)
+    x64 = wl.widen_f64(xs, act) if act != F32 else xs.astype(np.float64)
+    packed = _pack(G, w, N, K, fmt)
+    y = _run(G, xs, act, packed, torch.from_numpy(s).cuda(), 0.0, M, N, K, fmt, out)
+    ref, mag = oracle.matmul_fp8(x64, w, s, K, N, e5m2=e5m2)
+    G.assert_within(y, ref, mag, out, f"fp8 fmt={fmt} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K,act,out", CASES)
+def test_nvfp4_random(G, M, N, K, act, out):
+    rng = np.random.default_rng(M * 17 + N + K)
+    KB = -(-K // 16)
+    w4 = rng.integers(0, 16, size=(K, N)).astype(np.uint8)
+    s8 = rng.choice([c for c in range(256) if (c & 0x7F) != 0x7F], size=(KB, N)).astype(np.uint8)
+    gs = float(np.float32(rng.uniform(0.01, 0.1)))
+    x = rng.standard_normal((M, K))
+    xs = wl.to_storage(x, act)
+    x64 = wl.widen_f64(xs, act) if act != F32 else xs.astype(np.float64)
+    packed = _pack(G, _nibbles(w4), N, K, mnb.MNB_WF_NVFP4)
+    y = _run(G, xs, act, packed, torch.from_numpy(s8).cuda(), gs, M, N, K, mnb.MNB_WF_NVFP4, out)
+    ref, mag = oracle.matmul_nvfp4(x64, _nibbles(w4), s8, gs, K, N)
+    G.assert_within(y, ref, mag, out, f"nvfp4 {M}x{N}x{K}")
+
+
+def test_fp_format_mismatch_sets_status(G):
+    """A buffer packed as E4M3 called as E5M2 (same N, K) sets MNB_ERR_LAYOUT_MISMATCH."""
+    N, K, M = 64, 64, 2
+    w = np.zeros((K, N), np.uint8)
+    packed = _pack(G, w, N, K, mnb.MNB_WF_E4M3)
+    x = G.to_dev(wl.to_storage(np.ones((M, K)), F32), F32)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    mnb.mnb_matmul_fp(x, packed, None, 0.0, y, M, N, K, mnb.MNB_WF_E5M2, F32, F32)
+    torch.cuda.synchronize()
+    assert mnb.mnb_get_device_error() == mnb.MNB_ERR_LAYOUT_MISMATCH
+    assert mnb.mnb_get_device_error() == mnb.MNB_OK  # read and cleared
+
+
+def test_fp_pack_is_a_permutation(G):
+    """Packing FP8 moves codes only: the integer unpack of the same buffer (8-bit codes, 128-deep
+    blocks) returns the [N, K] transpose of the source."""
+    N, K = 37, 300
+    rng = np.random.default_rng(5)
+    w = rng.integers(0, 256, size=(K, N)).astype(np.uint8)
+    packed = _pack(G, w, N, K, mnb.MNB_WF_E4M3)
+    KB = -(-K // 128)
+    out = torch.zeros(N * KB * 128, dtype=torch.uint8, device="cuda")
+    # the header records the FP format, so the integer unpack flags a mismatch but still moves the bytes
+    mnb.mnb_unpack_codes(packed, out, N, K, 8, 128)
+    torch.cuda.synchronize()
+    mnb.mnb_get_device_error()
+    got = out.cpu().numpy().reshape(N, KB * 128)[:, :K]
+    assert np.array_equal(got, w.T)
