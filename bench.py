@@ -366,7 +366,7 @@ def run_ours(args):
         unit, per_step = metric_of(w)
         value = whole_job_value(world, steps, per_step, t)
         per_launch_s = t / steps
-        kernels_per_step = 2 if acc == 4 else 1  # accuracy level 4: activation quantisation + GEMV
+        kernels_per_step = 2 if acc == 4 else 1  # accuracy level 4: activation quantisation + product
         out = {"workload": w.name, "value": value, "unit": unit, "steps": steps, "ms_per_step": per_launch_s * 1e3,
                "kernel": chosen, "clocks": ck, "weight_copies": R, "launches": steps * kernels_per_step}
         if unit == "GB/s":
@@ -524,6 +524,8 @@ def run_ours(args):
         secondary("int8_k11008", wl.config(2), max(20, args.steps // 2), sw)
         secondary("int2_m8", wl.config(3), max(20, args.steps // 2), sw)
         secondary("a8", w, max(20, args.steps // 4), sw, acc=4,
+                  extra={"accuracy_level": 4, "launches_per_step": 2})
+        secondary("a8_m512", wl.config(4), max(20, args.steps // 20), max(3, args.warmup // 20), acc=4,
                   extra={"accuracy_level": 4, "launches_per_step": 2})
         moe, n = measure_moe(wl.MOE_CONFIGS[0], max(20, args.steps // 10), max(3, args.warmup // 10))
         res["moe"] = moe

@@ -323,7 +323,10 @@ size_t mnb_workspace_size(int64_t M, int64_t N, int64_t K, int bits, int block_s
     if (accuracy_level != 4) return 0;
     Layout L;
     L.init(N, K, bits, block_size);
-    return i8_workspace_bytes(M, L);
+    const size_t i8 = i8_workspace_bytes(M, L);
+    if (M <= 16) return i8;  // the int8 GEMV
+    const size_t g = a8_gemm_workspace_bytes(M, L);  // the prefill GEMM (bf16 activation codes)
+    return g > i8 ? g : i8;
 }
 
 mnb_kernel mnb_select_kernel(int64_t M, int64_t N, int64_t K, int bits, int block_size, mnb_dtype act_dtype,
@@ -333,7 +336,7 @@ mnb_kernel mnb_select_kernel(int64_t M, int64_t N, int64_t K, int bits, int bloc
     (void)bits;
     (void)block_size;
     const int64_t gemv_max_m = env_int("MNB_GEMV_MAX_M", 16);
-    if (accuracy_level == 4) return MNB_KERNEL_GEMV_I8;
+    if (accuracy_level == 4) return M <= 16 ? MNB_KERNEL_GEMV_I8 : MNB_KERNEL_GEMM_TC;
     if (act_dtype == MNB_F32) return M == 1 ? MNB_KERNEL_GEMV : MNB_KERNEL_GENERIC;
     if (M <= gemv_max_m) return MNB_KERNEL_GEMV_MMA;
     return MNB_KERNEL_GEMM_TC;
@@ -377,7 +380,9 @@ mnb_status mnb_matmul_ex(const mnb_matmul_args* a) {
     wait_limits(&p.wait_limit, &p.wait_hint_ns);
 
     mnb_kernel k = a->kernel;
-    if (k == MNB_KERNEL_AUTO) {
+    if (k == MNB_KERNEL_AUTO && a->accuracy_level == 4) {
+        k = a->M <= 16 && gemv_i8_supported(p) ? MNB_KERNEL_GEMV_I8 : MNB_KERNEL_GEMM_TC;
+    } else if (k == MNB_KERNEL_AUTO) {
         k = mnb_select_kernel(a->M, a->N, a->K, a->bits, a->block_size, a->act_dtype, a->accuracy_level);
         // The specialised kernels decline what they cannot do; the generic
         // kernel takes every float-path call.
@@ -387,7 +392,7 @@ mnb_status mnb_matmul_ex(const mnb_matmul_args* a) {
         if (k == MNB_KERNEL_GEMV && !gemv_supported(p)) k = MNB_KERNEL_GENERIC;
         if (k == MNB_KERNEL_GEMM_TC && !gemm_tc_supported(p)) k = MNB_KERNEL_GENERIC;
     }
-    if (a->accuracy_level == 4 && k != MNB_KERNEL_GEMV_I8) return MNB_ERR_UNSUPPORTED;
+    if (a->accuracy_level == 4 && k != MNB_KERNEL_GEMV_I8 && k != MNB_KERNEL_GEMM_TC) return MNB_ERR_UNSUPPORTED;
     if (a->accuracy_level != 4 && k == MNB_KERNEL_GEMV_I8) return MNB_ERR_UNSUPPORTED;
 
     cudaStream_t s = (cudaStream_t)a->stream;
@@ -408,6 +413,15 @@ mnb_status mnb_matmul_ex(const mnb_matmul_args* a) {
             e = launch_gemv_mma(p, s);
             break;
         case MNB_KERNEL_GEMM_TC:
+            if (a->accuracy_level == 4) {
+                if (a->g_idx || !gemm_a8_supported(p)) return MNB_ERR_UNSUPPORTED;
+                const size_t need = a8_gemm_workspace_bytes(a->M, p.L);
+                if (a->workspace_bytes < need || !a->workspace) return MNB_ERR_NO_MEM;
+                if (!aligned(a->workspace, 256)) return MNB_ERR_INVALID_ARG;
+                if (inject_launch_failure()) return MNB_ERR_CUDA;
+                e = launch_gemm_a8(p, s);
+                break;
+            }
             if (a->g_idx || !gemm_tc_supported(p)) return MNB_ERR_UNSUPPORTED;
             if (inject_launch_failure()) return MNB_ERR_CUDA;
             e = launch_gemm_tc(p, s);

@@ -66,13 +66,18 @@ struct Geom {
     int tmem_cols;      // allocated columns (power of two)
     int a_col0;         // first column of the A ring (= NP * BT)
     size_t x_stage, wp_stage, total_bytes;
+    const float* sa;    // accuracy level 4: activation scales s_a [M, KB] (X holds the int8 codes as bf16)
 };
 
 struct Maps {
     CUtensorMap x, w;
 };
 
-template <int BITS, bool BF16X, int BT>
+// A8: accuracy level 4 (onnx-runtime-ep-cpu matmul_nbits.rs, int8_row /
+// int8_matmul_amx): X is the per-block int8 activation codes widened to bf16,
+// so a block's partial is the exact integer dot (|sum| < 2^24), and the
+// rescale multiplies it by f32(s_w[n, kb] * s_a[m, kb]).
+template <int BITS, bool BF16X, int BT, bool A8>
 __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Geom geo,
                                                                const __grid_constant__ CUtensorMap xmap,
                                                                const __grid_constant__ CUtensorMap wmap) {
@@ -338,6 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Ge
         bool ok = true;
         for (int64_t b = 0; b < L.KB; ++b) {
             const int pb = (int)(b % NP);
+            float sa_col[A8 ? CW : 1];  // the tokens' activation scales of block b (loaded before the wait)
+            if constexpr (A8) {
+                const int64_t mc = m0 + cs * CW;
+#pragma unroll
+                for (int j = 0; j < CW; ++j) sa_col[j] = mc + j < p.M ? __ldg(geo.sa + (mc + j) * L.KB + b) : 0.f;
+            }
             if (!tc::wait_bounded(&part_full[pb], (uint32_t)((b / NP) & 1), p.status, wl, wh)) {
                 ok = false;
                 break;
@@ -362,8 +373,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Ge
                     if (lane == 0) mbar_arrive(&part_free[pb]);
                 }
 #pragma unroll
-                for (int i = 0; i < CH / 2; ++i)
-                    y2[c0 / 2 + i] = ffma2(pack2u(P[2 * i], P[2 * i + 1]), sc2, y2[c0 / 2 + i]);
+                for (int i = 0; i < CH / 2; ++i) {
+                    if constexpr (A8) {
+                        const uint64_t sj = pack2(__fmul_rn(sc, sa_col[c0 + 2 * i]), __fmul_rn(sc, sa_col[c0 + 2 * i + 1]));
+                        y2[c0 / 2 + i] = ffma2(pack2u(P[2 * i], P[2 * i + 1]), sj, y2[c0 / 2 + i]);
+                    } else {
+                        y2[c0 / 2 + i] = ffma2(pack2u(P[2 * i], P[2 * i + 1]), sc2, y2[c0 / 2 + i]);
+                    }
+                }
             }
         }
         if (!ok) *abort_v = 1;
@@ -388,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Ge
     if (blockIdx.x == 0 && tid == 0) verify_header(p.packed_hdr, L, p.status);
 }
 
-template <int BITS, bool BF16X>
+template <int BITS, bool BF16X, bool A8 = false>
 cudaError_t launch(const MatmulParams& p, const Geom& geo, const Maps& m, cudaStream_t s) {
     auto go = [&](auto kern) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.total_bytes);
@@ -396,10 +413,18 @@ cudaError_t launch(const MatmulParams& p, const Geom& geo, const Maps& m, cudaSt
         kern<<<(unsigned)(geo.n_tiles * geo.m_tiles), kThreads, geo.total_bytes, s>>>(p, geo, m.x, m.w);
         return cudaGetLastError();
     };
-    switch (geo.BT) {
-        case 32: return go(gemm_bs_kernel<BITS, BF16X, 32>);
-        case 64: return go(gemm_bs_kernel<BITS, BF16X, 64>);
-        default: return go(gemm_bs_kernel<BITS, BF16X, 128>);
+    if constexpr (A8) {  // at most 64 tokens per tile: a rescale thread holds CW activation scales
+        switch (geo.BT) {
+            case 32: return go(gemm_bs_kernel<BITS, true, 32, true>);
+            case 64: return go(gemm_bs_kernel<BITS, true, 64, true>);
+            default: return cudaErrorInvalidValue;
+        }
+    } else {
+        switch (geo.BT) {
+            case 32: return go(gemm_bs_kernel<BITS, BF16X, 32, false>);
+            case 64: return go(gemm_bs_kernel<BITS, BF16X, 64, false>);
+            default: return go(gemm_bs_kernel<BITS, BF16X, 128, false>);
+        }
     }
 }
 

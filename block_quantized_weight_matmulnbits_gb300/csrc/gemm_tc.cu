@@ -15,6 +15,9 @@ namespace mnb {
 cudaError_t launch_gemm_tc_b2(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s);
 cudaError_t launch_gemm_tc_b4(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s);
 cudaError_t launch_gemm_tc_b8(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s);
+cudaError_t launch_gemm_a8_b2(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s);
+cudaError_t launch_gemm_a8_b4(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s);
+cudaError_t launch_gemm_a8_b8(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s);
 cudaError_t launch_gemm_hl_b2(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s);
 cudaError_t launch_gemm_hl_b4(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s);
 cudaError_t launch_gemm_hl_b8(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s);
@@ -42,9 +45,10 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Tokens per tile BT in {32, 64, 128}: fewest waves of (128-row x BT) tiles
-// over the SMs, then the least padded work; MNB_TC_BT forces one.
-Geom make_geom(const MatmulParams& p) {
+// Tokens per tile BT in {32, 64, 128} (at most max_bt): fewest waves of
+// (128-row x BT) tiles over the SMs, then the least padded work; MNB_TC_BT
+// forces one.
+Geom make_geom(const MatmulParams& p, int max_bt = 128) {
     Geom g{};
     const Layout& L = p.L;
     const int sms = device_info().sm_count > 0 ? device_info().sm_count : 148;
@@ -52,7 +56,7 @@ Geom make_geom(const MatmulParams& p) {
     const char* env = std::getenv("MNB_TC_BT");
     const int forced = env ? std::atoi(env) : 0;
     double best = 1e30;
-    for (int bt = 32; bt <= 128; bt *= 2) {
+    for (int bt = 32; bt <= max_bt; bt *= 2) {
         if (forced && bt != forced) continue;
         const int64_t mt = (p.M + bt - 1) / bt;
         const int64_t waves = (nt * mt + sms - 1) / sms;
@@ -64,7 +68,7 @@ Geom make_geom(const MatmulParams& p) {
             g.BT = bt;
         }
     }
-    if (g.BT == 0) g.BT = 128;
+    if (g.BT == 0) g.BT = max_bt;
     g.n_tiles = (int)nt;
     g.m_tiles = (int)((p.M + g.BT - 1) / g.BT);
     g.k_stages = (int)((L.Kpad + gbs::kBK - 1) / gbs::kBK);
@@ -81,6 +85,36 @@ Geom make_geom(const MatmulParams& p) {
     while (g.tmem_cols < g.a_col0 + g.R * gbs::kACols) g.tmem_cols <<= 1;
     g.total_bytes = fixed + g.R * (g.x_stage + g.wp_stage);
     return g;
+}
+
+// Tensor maps of the block-scaled kernel: X [M][xk] (bf16 / f16, row stride
+// xk * 2 bytes), 64-deep x BT-token boxes, 128-byte swizzle, zero fill past M
+// and xk; the packed codes, each 512-byte tile loaded as [chunk t][row group
+// g][16 B] (dims: 8 x u16, g (stride 64 B), t (stride 16 B), k tile, row tile).
+cudaError_t make_bs_maps(const MatmulParams& p, const Geom& geo, EncodeTiledFn enc, const void* x, int64_t xk,
+                         int x_dtype, Maps* m) {
+    std::memset(m, 0, sizeof(*m));
+    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t dims[2] = {(cuuint64_t)xk, (cuuint64_t)p.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)xk * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)geo.BT};
+    const CUtensorMapDataType dt =
+        x_dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = enc(&m->x, dt, 2, const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    const cuuint64_t tdims[5] = {8, 8, 4, (cuuint64_t)p.L.KTILES, (cuuint64_t)p.L.NT};
+    const cuuint64_t tstrides[4] = {64, 16, (cuuint64_t)kTileBytes, (cuuint64_t)p.L.KTILES * kTileBytes};
+    const cuuint32_t tbox[5] = {8, 8, 4, (cuuint32_t)(gbs::kBK / p.L.KT), (cuuint32_t)(gbs::kRows / 16)};
+    const cuuint32_t testr[5] = {1, 1, 1, 1, 1};
+    r = enc(&m->w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<uint8_t*>(p.packed), tdims, tstrides, tbox, testr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        if (std::getenv("MNB_LOG")) std::fprintf(stderr, "[mnb] 5-D code map rejected (%d)\n", (int)r);
+        return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
 }
 
 bool use_hl(const MatmulParams& p) {
@@ -162,34 +196,45 @@ cudaError_t launch_gemm_tc(const MatmulParams& p, cudaStream_t s) {
     if (use_hl(p)) return launch_hl(p, enc, s);
     const Geom geo = make_geom(p);
     Maps m;
-    std::memset(&m, 0, sizeof(m));
-    // X: [M][K] bf16/f16, 64-deep x BT-token boxes, 128-byte swizzle, zero fill past M and K
-    const cuuint32_t estr[2] = {1, 1};
-    const cuuint64_t dims[2] = {(cuuint64_t)p.L.K, (cuuint64_t)p.M};
-    const cuuint64_t strides[1] = {(cuuint64_t)p.L.K * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)geo.BT};
-    const CUtensorMapDataType dt =
-        p.act_dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUresult r = enc(&m.x, dt, 2, const_cast<void*>(p.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    // Packed codes, each 512-byte tile loaded as [chunk t][row group g][16 B]
-    // (dims: 8 x u16, g (stride 64 B), t (stride 16 B), k tile, row tile).
-    const cuuint64_t tdims[5] = {8, 8, 4, (cuuint64_t)p.L.KTILES, (cuuint64_t)p.L.NT};
-    const cuuint64_t tstrides[4] = {64, 16, (cuuint64_t)kTileBytes, (cuuint64_t)p.L.KTILES * kTileBytes};
-    const cuuint32_t tbox[5] = {8, 8, 4, (cuuint32_t)(gbs::kBK / p.L.KT), (cuuint32_t)(gbs::kRows / 16)};
-    const cuuint32_t testr[5] = {1, 1, 1, 1, 1};
-    r = enc(&m.w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<uint8_t*>(p.packed), tdims, tstrides, tbox, testr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        if (std::getenv("MNB_LOG")) std::fprintf(stderr, "[mnb] 5-D code map rejected (%d)\n", (int)r);
-        return cudaErrorInvalidValue;
-    }
+    const cudaError_t me = make_bs_maps(p, geo, enc, p.x, p.L.K, p.act_dtype, &m);
+    if (me != cudaSuccess) return me;
     switch (p.L.bits) {
         case 2: return launch_gemm_tc_b2(p, geo, m, s);
         case 4: return launch_gemm_tc_b4(p, geo, m, s);
         case 8: return launch_gemm_tc_b8(p, geo, m, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+bool gemm_a8_supported(const MatmulParams& p) {
+    if (p.g_idx != nullptr || p.M < 1 || p.M > (int64_t)1 << 31 || p.L.Kpad > (int64_t)1 << 31) return false;
+    const DeviceInfo& di = device_info();
+    if (di.major != 10 || !encode_fn()) return false;
+    const Geom g = make_geom(p, 64);
+    return g.NP >= 2 && g.total_bytes <= di.smem_optin && (int64_t)g.n_tiles * g.m_tiles < (int64_t)1 << 31;
+}
+
+// Accuracy level 4 prefill: quantise X per block into bf16 codes and f32
+// scales in the workspace, then the block-scaled GEMM over the codes.
+cudaError_t launch_gemm_a8(const MatmulParams& p, cudaStream_t s) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    uint16_t* qab = static_cast<uint16_t*>(p.workspace);
+    float* sa = reinterpret_cast<float*>(static_cast<uint8_t*>(p.workspace) + a8_gemm_codes_bytes(p.M, p.L));
+    cudaError_t e = launch_quant_act_bf16(p.x, p.act_dtype, qab, sa, p.M, p.L, (p.flags & kFlagPDL) != 0, s);
+    if (e != cudaSuccess) return e;
+    MatmulParams q = p;
+    q.x = qab;
+    q.act_dtype = kBF16;
+    Geom geo = make_geom(q, 64);
+    geo.sa = sa;
+    Maps m;
+    e = make_bs_maps(q, geo, enc, qab, p.L.Kpad, kBF16, &m);
+    if (e != cudaSuccess) return e;
+    switch (p.L.bits) {
+        case 2: return launch_gemm_a8_b2(q, geo, m, s);
+        case 4: return launch_gemm_a8_b4(q, geo, m, s);
+        case 8: return launch_gemm_a8_b8(q, geo, m, s);
         default: return cudaErrorInvalidValue;
     }
 }

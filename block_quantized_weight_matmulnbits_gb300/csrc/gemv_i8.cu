@@ -5,8 +5,10 @@ namespace mnb {
 namespace gi8 {
 
 // ---- 1. activation quantisation: one warp per (m, kb) ----
-__global__ void __launch_bounds__(256) quant_act_kernel(const void* x, int dt, int8_t* qa, float* sa, int64_t M,
-                                                        Layout L) {
+// Codes go to qa (int8) or, for the prefill GEMM, to qab as bf16 values
+// (|code| <= 127: exact); rows are Kpad long either way.
+__global__ void __launch_bounds__(256) quant_act_kernel(const void* x, int dt, int8_t* qa, uint16_t* qab, float* sa,
+                                                        int64_t M, Layout L) {
     // The previous kernel on the stream may have written x, or may still be
     // reading this workspace; no-op when not launched as a dependent.
     griddep_wait();
@@ -23,14 +25,14 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const void* x, int dt, i
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
     const float s = __fdiv_rn(amax, 127.0f);
     if (lane == 0) sa[m * L.KB + kb] = s;
-    int8_t* row = qa + m * L.Kpad;
     for (int64_t k = k0 + lane; k < k0 + L.bs; k += 32) {
         int code = 0;
         if (k < L.K && amax > 0.f) {
             const float r = roundf(__fdiv_rn(load_f32(x, m * L.K + k, dt), s));  // half away from zero
             code = (int)fminf(fmaxf(r, -127.f), 127.f);
         }
-        row[k] = (int8_t)code;
+        if (qab) qab[m * L.Kpad + k] = (uint16_t)(__float_as_uint((float)code) >> 16);  // exact in bf16
+        else qa[m * L.Kpad + k] = (int8_t)code;
     }
 }
 
@@ -56,8 +58,8 @@ bool gemv_i8_supported(const MatmulParams& p) {
     return g.total_bytes <= device_info().smem_optin && p.L.NT * g.C <= 0x7FFFFFFF;
 }
 
-static cudaError_t quant_launch(const void* x, int act_dtype, int8_t* qa, float* sa, int64_t M, const Layout& L,
-                                bool pdl, cudaStream_t s) {
+static cudaError_t quant_launch(const void* x, int act_dtype, int8_t* qa, uint16_t* qab, float* sa, int64_t M,
+                                const Layout& L, bool pdl, cudaStream_t s) {
     const int64_t warps = M * L.KB;
     const int64_t blocks = (warps + 7) / 8;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
@@ -71,12 +73,17 @@ static cudaError_t quant_launch(const void* x, int act_dtype, int8_t* qa, float*
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gi8::quant_act_kernel, x, act_dtype, qa, sa, M, L);
+    return cudaLaunchKernelEx(&cfg, gi8::quant_act_kernel, x, act_dtype, qa, qab, sa, M, L);
 }
 
 cudaError_t launch_quant_act(const void* x, int act_dtype, int8_t* qa, float* sa, int64_t M, const Layout& L,
                              cudaStream_t s) {
-    return quant_launch(x, act_dtype, qa, sa, M, L, false, s);
+    return quant_launch(x, act_dtype, qa, nullptr, sa, M, L, false, s);
+}
+
+cudaError_t launch_quant_act_bf16(const void* x, int act_dtype, uint16_t* qab, float* sa, int64_t M, const Layout& L,
+                                  bool pdl, cudaStream_t s) {
+    return quant_launch(x, act_dtype, nullptr, qab, sa, M, L, pdl, s);
 }
 
 cudaError_t launch_gemv_i8(const MatmulParams& p, cudaStream_t s) {
@@ -84,7 +91,7 @@ cudaError_t launch_gemv_i8(const MatmulParams& p, cudaStream_t s) {
     if (geo.total_bytes > device_info().smem_optin) return cudaErrorNotSupported;
     int8_t* qa = static_cast<int8_t*>(p.workspace);
     float* sa = reinterpret_cast<float*>(static_cast<uint8_t*>(p.workspace) + gi8::qa_bytes(p.M, p.L));
-    cudaError_t e = quant_launch(p.x, p.act_dtype, qa, sa, p.M, p.L, (p.flags & kFlagPDL) != 0, s);
+    cudaError_t e = quant_launch(p.x, p.act_dtype, qa, nullptr, sa, p.M, p.L, (p.flags & kFlagPDL) != 0, s);
     if (e != cudaSuccess) return e;
     switch (p.L.bits) {
         case 2: return launch_gemv_i8_b2(p, geo, qa, sa, s);

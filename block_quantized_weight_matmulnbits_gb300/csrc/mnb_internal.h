@@ -65,6 +65,19 @@ inline void fp_layout(Layout* L, int64_t N, int64_t K, int fmt) {
 
 cudaError_t launch_fp_generic(const FpParams& p, cudaStream_t s);
 
+// Accuracy level 4 on the prefill GEMM: workspace = activation codes as bf16
+// [M, Kpad] (256-byte aligned size) followed by the f32 scales s_a [M, KB].
+inline size_t a8_gemm_codes_bytes(int64_t M, const Layout& L) {
+    return ((size_t)M * (size_t)L.Kpad * 2 + 255) & ~size_t(255);
+}
+inline size_t a8_gemm_workspace_bytes(int64_t M, const Layout& L) {
+    return a8_gemm_codes_bytes(M, L) + (size_t)M * (size_t)L.KB * sizeof(float);
+}
+cudaError_t launch_quant_act_bf16(const void* x, int act_dtype, uint16_t* qab, float* sa, int64_t M, const Layout& L,
+                                  bool pdl, cudaStream_t s);
+bool gemm_a8_supported(const MatmulParams& p);
+cudaError_t launch_gemm_a8(const MatmulParams& p, cudaStream_t s);
+
 cudaError_t launch_pack(const uint8_t* b_ort, uint8_t* packed_hdr, const Layout& L, cudaStream_t s,
                         int fmt = kWfInt);
 cudaError_t launch_unpack(const uint8_t* packed, uint8_t* b_ort, const Layout& L, cudaStream_t s);

@@ -156,8 +156,11 @@ MNB_API mnb_status mnb_matmul(const void* x, const void* packed_b, const void* s
  *                  (MatMulNBitsKernel::execute).
  *   accuracy_level 0..3: float path.  4: activations quantised per K-block to
  *                  int8 (scale = max|x|/127, round half away from zero), exact
- *                  integer block dot, then one f32 rescale (fn
- *                  quantize_activation_signed, fn int8_row).  Needs workspace.
+ *                  integer block dot, then one f32 rescale by
+ *                  f32(scale * s_a) (fn quantize_activation_signed, fn int8_row,
+ *                  int8_matmul_amx).  M <= 16 runs the int8 GEMV; larger M the
+ *                  tensor-core GEMM over the codes widened to bf16 (each block's
+ *                  dot stays an exact integer in its f32 partial).  Needs workspace.
  *   workspace      device scratch of at least mnb_workspace_size() bytes
  *                  (256-byte aligned) or NULL when that size is 0.
  *   kernel         MNB_KERNEL_AUTO or a forced family.

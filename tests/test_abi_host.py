@@ -80,6 +80,15 @@ def test_fp_matmul_rejects_invalid_before_cuda():
     assert lib.mnb_pack_fp_weights(None, None, 0, 8, 8, 1, None) == mnb.MNB_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("M,K,bs", [(17, 4096, 32), (512, 4096, 32), (64, 1000, 128)])
+def test_a8_prefill_workspace_size(M, K, bs):
+    """Accuracy level 4 above 16 rows: bf16 activation codes [M, Kpad] (256-byte aligned) then
+    f32 block scales [M, KB]."""
+    kb = -(-K // bs)
+    codes = -(-(M * kb * bs * 2) // 256) * 256
+    assert mnb.mnb_workspace_size(M, 4096, K, 4, bs, 4) == codes + M * kb * 4
+
+
 def test_kernel_selection():
     assert mnb.mnb_select_kernel(1, 11008, 4096, 4, 32, mnb.MNB_BF16) == "gemv_mma"
     assert mnb.mnb_select_kernel(1, 4096, 11008, 8, 128, mnb.MNB_F16) == "gemv_mma"
@@ -90,6 +99,8 @@ def test_kernel_selection():
     assert mnb.mnb_select_kernel(512, 4096, 4096, 4, 32, mnb.MNB_BF16) == "gemm_tc"
     assert mnb.mnb_select_kernel(8, 4096, 4096, 4, 32, mnb.MNB_F32) == "generic"
     assert mnb.mnb_select_kernel(1, 4096, 4096, 4, 32, mnb.MNB_BF16, 4) == "gemv_i8"
+    assert mnb.mnb_select_kernel(16, 4096, 4096, 4, 32, mnb.MNB_BF16, 4) == "gemv_i8"
+    assert mnb.mnb_select_kernel(17, 4096, 4096, 4, 32, mnb.MNB_BF16, 4) == "gemm_tc"
 
 
 FAKE = 1 << 20  # aligned, never dereferenced: validation fails before any CUDA call

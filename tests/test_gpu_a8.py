@@ -183,3 +183,83 @@ def test_full_size_decode_workloads_a8(G, mnb, oracle_mod, ci):
     y = _run_a8(G, mnb, P)
     ref, mag = _oracle_a8(oracle_mod, P)
     G.assert_within(P.y64(y), ref, mag, w.out_dtype, f"a8 {w.name}")
+
+
+# ---- accuracy level 4 above 16 rows: the tensor-core prefill GEMM ----------------
+
+A8_GEMM_CASES = [
+    # M, bits, bs, dtypes (act, scale, out), asym, N, K
+    (17, 4, 32, (BF16, F16, BF16), True, 300, 4096),
+    (64, 2, 64, (F16, F16, F32), True, 257, 2048),
+    (512, 4, 32, (BF16, F16, BF16), False, 1024, 4096),
+    (40, 8, 128, (F32, F32, F16), True, 200, 1152),
+    (100, 4, 16, (BF16, BF16, BF16), True, 130, 1000),
+    (33, 2, 256, (F16, F16, F16), True, 64, 1536),
+    (20, 4, 512, (BF16, F16, F32), True, 70, 2048),
+    (129, 8, 32, (BF16, F16, BF16), False, 129, 640),
+]
+
+
+@pytest.mark.parametrize("M,bits,bs,dt,asym,N,K", A8_GEMM_CASES)
+def test_matmul_a8_prefill(G, mnb, oracle_mod, M, bits, bs, dt, asym, N, K):
+    w = _w(M, N, K, bits, bs, dt, asym, 60 + M + bits + bs)
+    P = G.Problem(w)
+    assert mnb.mnb_select_kernel(M, N, K, bits, bs, dt[0], 4) == "gemm_tc"
+    y = _run_a8(G, mnb, P)
+    assert mnb.mnb_get_device_error() == mnb.MNB_OK
+    ref, mag = _oracle_a8(oracle_mod, P)
+    G.assert_within(P.y64(y), ref, mag, w.out_dtype, f"a8 prefill {w.name}")
+
+
+def test_matmul_a8_prefill_forced_at_small_m(G, mnb, oracle_mod):
+    """The prefill GEMM also runs below 17 rows when forced, with its own (larger) workspace."""
+    w = _w(5, 150, 1024, 4, 32, (BF16, F16, BF16), True, 61)
+    P = G.Problem(w)
+    kb = -(-w.K // w.bs)
+    need = -(-(w.M * kb * w.bs * 2) // 256) * 256 + w.M * kb * 4
+    y = P.run(kernel="gemm_tc", accuracy_level=4, workspace=G.aligned_empty(need))
+    ref, mag = _oracle_a8(oracle_mod, P)
+    G.assert_within(P.y64(y), ref, mag, w.out_dtype, "a8 prefill forced")
+    with pytest.raises(mnb.MnbError) as e:
+        P.run(kernel="gemm_tc", accuracy_level=4, workspace=G.aligned_empty(need - 256))
+    assert e.value.status == mnb.MNB_ERR_NO_MEM
+
+
+def test_matmul_a8_prefill_bias_pdl_deterministic(G, mnb, oracle_mod):
+    w = _w(70, 111, 2048, 4, 32, (BF16, F16, BF16), True, 62)
+    P = G.Problem(w)
+    bias_h = np.random.default_rng(6).uniform(-1, 1, w.N).astype(np.float32)
+    bias = torch.from_numpy(bias_h).cuda()
+    ref, mag = _oracle_a8(oracle_mod, P, bias=bias_h.astype(np.float64))
+    ys = []
+    for flags in (0, mnb.MNB_FLAG_PDL, 0):
+        y = _run_a8(G, mnb, P, bias=bias, flags=flags)
+        G.assert_within(P.y64(y), ref, mag, w.out_dtype, f"a8 prefill bias flags={flags}")
+        ys.append(y.clone())
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
+
+
+def test_matmul_a8_prefill_all_codes_equal_zero_point_give_zero(G, mnb):
+    from tests._golden import pack_matrix_test, pack_zp_test
+    N, K, bs = 150, 512, 32
+    for bits in (2, 4, 8):
+        z = np.random.default_rng(10 + bits).integers(0, 1 << bits, size=(N, K // bs))
+        w = _w(40, N, K, bits, bs, (BF16, F16, F32), True, 63)
+        d = wl.generate(w)
+        d["b"] = pack_matrix_test(np.repeat(z, bs, axis=1), bits, bs)
+        d["zp"] = pack_zp_test(z, bits)
+        P = G.Problem(w, d)
+        y = P.y64(_run_a8(G, mnb, P))
+        assert np.all(y == 0.0), f"bits {bits}"
+
+
+def test_full_size_prefill_workload_a8(G, mnb, oracle_mod):
+    """The 512 x 4096 x 4096 int4 prefill at accuracy level 4, against the oracle on 24 sampled rows
+    (rows are independent: the oracle takes those rows' codes and scales)."""
+    w = wl.CONFIGS[4]
+    P = G.Problem(w)
+    y = P.y64(_run_a8(G, mnb, P))
+    qa, sa = oracle_mod.quantize_act(P.x64.astype(np.float32), w.K, w.bs)
+    rows = np.unique(np.linspace(0, w.M - 1, 24).astype(int))
+    ref, mag = oracle_mod.matmul_a8(qa[rows], sa[rows], P.d["b"], P.s32, P.d["zp"], w.N, w.K, w.bits, w.bs)
+    G.assert_within(y[rows], ref, mag, w.out_dtype, "a8 prefill full size")

@@ -144,12 +144,13 @@ def test_worst_case_f32_activation_gemv(G, bits, bs, sdt, zpm, x_mode):
 
 @pytest.mark.parametrize("x_mode", ["one_hot", "positive"])
 @pytest.mark.parametrize("bits,bs,act,sdt,zpm", SHAPES[:4])
-def test_worst_case_int8_activations(G, mnb, oracle_mod, bits, bs, act, sdt, zpm, x_mode):
+@pytest.mark.parametrize("M", [3, 40])
+def test_worst_case_int8_activations(G, mnb, oracle_mod, M, bits, bs, act, sdt, zpm, x_mode):
     """Accuracy level 4 against the a8 oracle (activations quantised per block
     as the page does): one-hot rows quantise exactly, positive rows do not
-    cancel."""
-    M, N, K = 3, 150, 4 * bs + 3 * 128
-    data = build(M, N, K, bits, bs, act, sdt, zpm, x_mode, 4200 + bits, F32_EXTRA if sdt == F32 else ())
+    cancel.  M = 3 runs the int8 GEMV, M = 40 the prefill GEMM."""
+    N, K = 150, 4 * bs + 3 * 128
+    data = build(M, N, K, bits, bs, act, sdt, zpm, x_mode, 4200 + bits + M, F32_EXTRA if sdt == F32 else ())
     w = _wl(M, N, K, bits, bs, act, sdt, zpm)
     P = G.Problem(w, data)
     ws = G.aligned_empty(mnb.mnb_workspace_size(M, N, K, bits, bs, 4))
