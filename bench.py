@@ -484,9 +484,9 @@ def run_ours(args):
         per_launch_s = t / steps
         achieved = per_step / per_launch_s
         return {"workload": name, "value": whole_job_value(world, steps, per_step, t), "unit": "GB/s",
-                "kernel": "fp_generic", "ms_per_step": per_launch_s * 1e3, "steps": steps,
+                "kernel": "gemv_fp", "ms_per_step": per_launch_s * 1e3, "steps": steps,
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                             "frac": achieved / pk["hbm_gbs"], "traffic": traffic_for(f"fp_generic:{name}"),
+                             "frac": achieved / pk["hbm_gbs"], "traffic": traffic_for(f"gemv_fp:{name}"),
                              "algorithmic_bytes": int(per_step * 1e9), "peak_source": f"{pk_src} hbm_gbs"},
                 "clocks": ck, "weight_copies": R}, steps
 

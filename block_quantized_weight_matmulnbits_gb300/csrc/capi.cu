@@ -312,10 +312,11 @@ mnb_status mnb_matmul_fp(const void* x, const void* packed, const void* scales, 
     p.out_dtype = out_dtype;
     p.status = pd->status;
     if (inject_launch_failure()) return MNB_ERR_CUDA;
+    const bool fast = gemv_fp_supported(p);
     if (log_enabled())
-        std::fprintf(stderr, "[mnb] matmul_fp M=%lld N=%lld K=%lld format=%d kernel=fp_generic\n", (long long)M,
-                     (long long)N, (long long)K, (int)format);
-    return from_cuda(launch_fp_generic(p, (cudaStream_t)stream));
+        std::fprintf(stderr, "[mnb] matmul_fp M=%lld N=%lld K=%lld format=%d kernel=%s\n", (long long)M,
+                     (long long)N, (long long)K, (int)format, fast ? "gemv_fp" : "fp_generic");
+    return from_cuda(fast ? launch_gemv_fp(p, (cudaStream_t)stream) : launch_fp_generic(p, (cudaStream_t)stream));
 }
 
 size_t mnb_workspace_size(int64_t M, int64_t N, int64_t K, int bits, int block_size, int accuracy_level) {

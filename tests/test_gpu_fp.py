@@ -208,3 +208,82 @@ def test_fp_pack_is_a_permutation(G):
     mnb.mnb_get_device_error()
     got = out.cpu().numpy().reshape(N, KB * 128)[:, :K]
     assert np.array_equal(got, w.T)
+
+
+# ---- the decode GEMV (M <= 4, bf16 / f16 X, K a multiple of 128 for FP8 and 256 for NVFP4) ----
+
+FAST_CASES = [
+    # (M, N, K, act, out)
+    (1, 11008, 4096, BF16, BF16),
+    (1, 150, 512, F16, F32),
+    (3, 333, 1024, BF16, F32),
+    (4, 4096, 2048, F16, F16),
+    (2, 17, 256, BF16, BF16),
+]
+
+
+@pytest.mark.parametrize("M,N,K,act,out", FAST_CASES)
+@pytest.mark.parametrize("fmt", [mnb.MNB_WF_E4M3, mnb.MNB_WF_E5M2, mnb.MNB_WF_NVFP4])
+def test_fp_decode_gemv(G, monkeypatch, M, N, K, act, out, fmt):
+    """The decode GEMV against the oracle, and against the exact kernel forced with MNB_FP_KERNEL=generic."""
+    rng = np.random.default_rng(M * 7 + N + K + 13 * fmt)
+    x = rng.standard_normal((M, K))
+    xs = wl.to_storage(x, act)
+    x64 = wl.widen_f64(xs, act)
+    if fmt == mnb.MNB_WF_NVFP4:
+        w4 = rng.integers(0, 16, size=(K, N)).astype(np.uint8)
+        s8 = rng.choice([c for c in range(256) if (c & 0x7F) != 0x7F], size=(K // 16, N)).astype(np.uint8)
+        gs = float(np.float32(0.0371))
+        src, st = _nibbles(w4), torch.from_numpy(s8).cuda()
+        ref, mag = oracle.matmul_nvfp4(x64, src, s8, gs, K, N)
+    else:
+        e5m2 = fmt == mnb.MNB_WF_E5M2
+        src = rng.choice(_finite_fp8_codes(e5m2), size=(K, N)).astype(np.uint8)
+        s = rng.uniform(1e-3, 1e-2, size=N).astype(np.float32)
+        gs, st = 0.0, torch.from_numpy(s).cuda()
+        ref, mag = oracle.matmul_fp8(x64, src, s, K, N, e5m2=e5m2)
+    packed = _pack(G, src, N, K, fmt)
+    y = _run(G, xs, act, packed, st, gs, M, N, K, fmt, out)
+    G.assert_within(y, ref, mag, out, f"fp gemv fmt={fmt} {M}x{N}x{K}")
+    monkeypatch.setenv("MNB_FP_KERNEL", "generic")
+    y2 = _run(G, xs, act, packed, st, gs, M, N, K, fmt, out)
+    G.assert_within(y2, ref, mag, out, f"fp generic fmt={fmt} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("fmt", [mnb.MNB_WF_E4M3, mnb.MNB_WF_E5M2])
+def test_fp8_decode_gemv_non_finite_codes(G, fmt):
+    """The decode GEMV's decode tables keep the page's exponent-all-ones rule: infinity and NaN codes
+    poison exactly their columns."""
+    e5m2 = fmt == mnb.MNB_WF_E5M2
+    N, K, M = 48, 256, 1
+    rng = np.random.default_rng(70 + fmt)
+    w = rng.choice(_finite_fp8_codes(e5m2), size=(K, N)).astype(np.uint8)
+    specials = [0x7C, 0xFC, 0x7D, 0xFF] if e5m2 else [0x78, 0xF8, 0x7A, 0xFF]
+    for j, code in enumerate(specials):
+        w[40 + 3 * j, 5 * j + 2] = code
+    x = rng.uniform(0.5, 1.0, size=(M, K))
+    xs = wl.to_storage(x, BF16)
+    packed = _pack(G, w, N, K, fmt)
+    y = _run(G, xs, BF16, packed, None, 0.0, M, N, K, fmt, F32)
+    ref, mag = oracle.matmul_fp8(wl.widen_f64(xs, BF16), w, None, K, N, e5m2=e5m2)
+    fin = _same_class(y, ref)
+    assert (~fin).sum() == len(specials)
+    G.assert_within(np.where(fin, y, 0), np.where(fin, ref, 0), np.where(fin, mag, 0), F32, "fp8 gemv finite")
+
+
+def test_nvfp4_decode_gemv_nan_scale_codes(G):
+    """NaN block-scale codes (0x7F, 0xFF) make their columns NaN; every other column stays within the bound."""
+    N, K, M = 64, 512, 2
+    rng = np.random.default_rng(77)
+    w4 = rng.integers(0, 16, size=(K, N)).astype(np.uint8)
+    s8 = rng.choice([c for c in range(256) if (c & 0x7F) != 0x7F], size=(K // 16, N)).astype(np.uint8)
+    s8[3, 10] = 0x7F
+    s8[30, 41] = 0xFF
+    x = rng.uniform(0.5, 1.0, size=(M, K))
+    xs = wl.to_storage(x, F16)
+    packed = _pack(G, _nibbles(w4), N, K, mnb.MNB_WF_NVFP4)
+    y = _run(G, xs, F16, packed, torch.from_numpy(s8).cuda(), 0.5, M, N, K, mnb.MNB_WF_NVFP4, F32)
+    ref, mag = oracle.matmul_nvfp4(wl.widen_f64(xs, F16), _nibbles(w4), s8, 0.5, K, N)
+    fin = _same_class(y, ref)
+    assert set(np.nonzero(~fin)[1].tolist()) == {10, 41}
+    G.assert_within(np.where(fin, y, 0), np.where(fin, ref, 0), np.where(fin, mag, 0), F32, "nvfp4 gemv finite")
