@@ -47,7 +47,8 @@ constexpr int kBT = 256;         // tokens per tile = MMA N
 constexpr int kBK = 64;          // depths per stage (4 k-steps)
 constexpr int kACols = 64;       // TMEM columns of one A slot: A_hi (32) then A_lo (32)
 constexpr int kCtlWarps = 4;
-constexpr int kDqWarps = 8;
+constexpr int kDqWarps = 16;
+constexpr int kKK = 16 / kDqWarps;  // k-steps a dequant warp writes per stage
 constexpr int kThreads = (kCtlWarps + kDqWarps) * 32;
 constexpr int kR = 4;            // ring depth (shared-memory stages and TMEM A slots)
 constexpr int kXStage = kBT * kBK * 2;  // 32 KB
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
         // ---------------- A_hi, A_lo: one W row per thread ----------------
         const int dw = warp - kCtlWarps;
         const int q4 = warp & 3;          // TMEM lane quadrant
-        const int jh = dw >> 2;           // k-steps 2 jh, 2 jh + 1 of every stage (32 depths)
+        const int jh = dw >> 2;           // k-steps kKK jh .. kKK jh + kKK - 1 of every stage
         const int r = q4 * 32 + lane;     // W row inside the tile
         const int rt = r >> 4, g = r & 7, hi = (r >> 3) & 1;
         const int64_t n = n0 + r;
@@ -217,13 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
         // block of the thread's 32 depths (bs >= 32) or of each of its two k-steps (bs = 16)
         const int bs_log = __ffs(L.bs) - 1;  // block sizes are powers of two
         auto blocks_of = [&](int ks, int64_t* kb0, int64_t* kb1) {
-            const int64_t d0 = (int64_t)ks * kBK + 32 * jh;
+            const int64_t d0 = (int64_t)ks * kBK + 16 * kKK * jh;
             *kb0 = d0 >> bs_log;
             *kb1 = (d0 + 16) >> bs_log;
         };
         // raw loads only (a decode here would wait for the load): scale bits and the
         // zero-point byte of the thread's block(s) of a stage; decoded when used
-        const bool two_blocks = L.bs < 32;
+        const bool two_blocks = kKK == 2 && L.bs < 32;
         auto raw_scale = [&](int64_t kb) -> uint32_t {
             if (!row_ok || kb >= L.KB) return 0u;
             const int64_t i = n * L.KB + kb;
@@ -287,13 +288,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
             zc[0] = ((kMag & 0xFFFFu) + z0) * 0x10001u;
             zc[1] = ((kMag & 0xFFFFu) + z1) * 0x10001u;
             // (q - zp) pairs of the thread's two k-steps: column c of k-step kk = depths 2c, 2c + 1
-            uint32_t qz[16];
+            uint32_t qz[8 * kKK];
             const uint8_t* cb = wp + s * geo.wp_stage + rt * TILES * kTileBytes + g * 16;
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    const int st = 2 * jh + kk;  // k-step inside the stage
+                for (int kk = 0; kk < kKK; ++kk) {
+                    const int st = kKK * jh + kk;  // k-step inside the stage
                     uint32_t v0, v1;             // depths 2t/2t+1 and 2t+8/2t+9 of the row
                     if constexpr (BITS == 4) {
                         // stage = one packed tile (4 k-steps): word st of chunk t
@@ -325,18 +326,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
                     qz[8 * kk + t + 4] = v1;
                 }
             }
-            uint32_t ah[16], al[16];
+            uint32_t ah[8 * kKK], al[8 * kKK];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
+            for (int c = 0; c < 8 * kKK; ++c) {
                 const int kk = c >> 3;
                 const uint32_t h = bmul2(qz[c], shi[kk]);
                 const uint32_t rr = bfma2(qz[c], shi[kk], h ^ 0x80008000u);  // qz * s_hi - h, exact
                 ah[c] = h;
                 al[c] = bfma2(qz[c], slo[kk], rr);
             }
-            const uint32_t col = a_base + (uint32_t)(s * kACols + 16 * jh) + lane_addr;
-            tc::st_32x32b_x16(col, ah);
-            tc::st_32x32b_x16(col + 32u, al);
+            const uint32_t col = a_base + (uint32_t)(s * kACols + 8 * kKK * jh) + lane_addr;
+            if constexpr (kKK == 2) {
+                tc::st_32x32b_x16(col, *reinterpret_cast<const uint32_t(*)[16]>(ah));
+                tc::st_32x32b_x16(col + 32u, *reinterpret_cast<const uint32_t(*)[16]>(al));
+            } else {
+                tc::st_32x32b_x8(col, *reinterpret_cast<const uint32_t(*)[8]>(ah));
+                tc::st_32x32b_x8(col + 32u, *reinterpret_cast<const uint32_t(*)[8]>(al));
+            }
             tc::wait_st();
             tc::fence_before();
             __syncwarp();
@@ -356,8 +362,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
         tc::fence_after();
         const float bias = (p.bias && row_ok) ? load_f32(p.bias, n, p.bias_dtype) : 0.f;
         if (geo.splitk == 1) {
-            // columns 128 jh .. 128 jh + 127 of this thread's row
-            for (int c0 = 128 * jh; c0 < 128 * jh + 128 && fine; c0 += 32) {
+            // columns kEpi jh .. kEpi jh + kEpi - 1 of this thread's row
+            constexpr int kEpi = kBT / (kDqWarps / 4);
+            for (int c0 = kEpi * jh; c0 < kEpi * jh + kEpi && fine; c0 += 32) {
                 uint32_t v[32];
                 tc::ld_32x32b<32>(tmem + (uint32_t)c0 + lane_addr, v);
                 tc::wait_ld();
@@ -374,8 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
             // of the other 128 columns through shared memory ([col / 4][row][4] floats)
             float4* xbuf = reinterpret_cast<float4*>(smem);  // 64 KB, the X ring is idle now
             const int other = 128 * (rank ^ 1), mine = 128 * rank;
+            constexpr int kHalf = (kBT / 2) / (kDqWarps / 4);  // columns of a half a thread moves
             if (fine) {
-                for (int c0 = other + 64 * jh; c0 < other + 64 * jh + 64; c0 += 32) {
+                for (int c0 = other + kHalf * jh; c0 < other + kHalf * jh + kHalf; c0 += 32) {
                     uint32_t v[32];
                     tc::ld_32x32b<32>(tmem + (uint32_t)c0 + lane_addr, v);
                     tc::wait_ld();
@@ -390,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
             asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
             if (fine) {
                 const uint32_t peer = rank ^ 1;
-                for (int c0 = mine + 64 * jh; c0 < mine + 64 * jh + 64; c0 += 32) {
+                for (int c0 = mine + kHalf * jh; c0 < mine + kHalf * jh + kHalf; c0 += 32) {
                     uint32_t v[32];
                     tc::ld_32x32b<32>(tmem + (uint32_t)c0 + lane_addr, v);
                     tc::wait_ld();
