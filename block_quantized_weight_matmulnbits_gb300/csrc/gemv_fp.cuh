@@ -124,9 +124,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fp_kernel(FpParams p, FGeom 
             for (int j = 0; j < kTilesPerChunk; ++j) w[j] = ldg_stream(src + j * kTileBytes);
         }
     };
+    const int q16 = kW / KC, r16 = kW % KC;
     Cursor cur{warp, warp / KC, warp % KC};
     Cursor nxt = cur;
-    nxt.advance(KC);
+    nxt.advance(KC, q16, r16);
     load(wb[0], cur);
     load(wb[1], nxt);
     for (int c = tid; c < 256; c += kThreads) {
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fp_kernel(FpParams p, FGeom 
     auto step = [&](uint4 (&w)[kTilesPerChunk]) {
         compute(w, cur);
         Cursor after = nxt;
-        after.advance(KC);
+        after.advance(KC, q16, r16);
         load(w, after);
         if (nxt.i >= n_items || nxt.rt != cur.rt) flush(cur.rt);
         cur = nxt;

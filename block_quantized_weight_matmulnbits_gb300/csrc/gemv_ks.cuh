@@ -38,10 +38,12 @@ using gmma::Unpack;
 constexpr int kW = 16;
 constexpr int kThreads = kW * 32;
 constexpr int kTilesPerChunk = 4;  // 64 bytes per lane
+constexpr int kItemBytes = kTilesPerChunk * kTileBytes;
 
 struct KGeom {
     int G;        // CTAs
     int KC;       // K-chunks per row tile
+    int q16, r16; // a step of kW items: q16 row tiles and r16 chunks
     int max_rt;   // most row tiles of one CTA
     int xrow;     // X row stride in 16-byte units (K / 8 + 4: padded against bank conflicts)
     size_t x_bytes, red_bytes, total_bytes;
@@ -61,13 +63,18 @@ inline bool make_kgeom(const Layout& L, int64_t M, int sms, size_t smem_limit, i
     const int spb = (int)(L.bs / 16);
     if (L.bs % 16 != 0 || spb < 1 || spb > ch || (spb & (spb - 1)) != 0) return false;
     if ((ch / spb) * sbytes > 32) return false;
-    // scale and zero-point offsets are formed in 32 bits
+    // scale, zero-point and a CTA's weight offsets are formed in 32 bits
     if ((uint64_t)L.N * (uint64_t)L.KB * 4u >= (1ull << 32) || (uint64_t)L.N * (uint64_t)L.zp_row >= (1ull << 32))
         return false;
     KGeom g{};
     g.KC = (int)(L.K / chunk_k);
     g.G = (int)(L.NT < sms ? L.NT : sms);
     g.max_rt = (int)((L.NT + g.G - 1) / g.G);
+    if ((uint64_t)g.max_rt * (uint64_t)g.KC * (uint64_t)kItemBytes >= (1ull << 32)) return false;
+    // CTA ranges are formed in 32 bits
+    if ((uint64_t)L.NT * (uint64_t)(g.G + 1) >= (1ull << 31)) return false;
+    g.q16 = kW / g.KC;
+    g.r16 = kW % g.KC;
     g.xrow = (int)(L.K / 8) + 4;
     g.x_bytes = (size_t)(M + 1) * g.xrow * 16;
     g.red_bytes = (size_t)g.max_rt * kW * 16 * M * 4;
@@ -127,27 +134,23 @@ struct Item {
     uint32_t z0[ZW], z8[ZW];  // raw code fields (spread when the item is computed)
     uint32_t zshift;          // bit offset of the chunk's first field (fields under 8 bits a chunk)
 
-    // Loads of item (row tile rt, chunk c): wp is the lane's 16 bytes of the
-    // item's first packed tile.  Rows past N read row N - 1 instead (their
-    // results are never stored, and every row's sum is independent), so the
-    // loads need no predicates; scale and zero-point offsets fit 32 bits.
-    __device__ __forceinline__ void load(const MatmulParams& p, const uint8_t* wp, int64_t rt, int c, int g) {
-        const Layout& L = p.L;
+    // Loads of item (local row tile, chunk c): wp is the lane's 16 bytes of the
+    // item's first packed tile; sb / zb the scale / zero-point bytes of the
+    // CTA's first row; r0, r8 the lane's two rows (local, clamped to the last
+    // row: rows past N read row N - 1, whose results are never stored, so the
+    // loads need no predicates).  Offsets fit 32 bits.
+    __device__ __forceinline__ void load(const uint8_t* wp, const uint8_t* sb, const uint8_t* zb, uint32_t srow,
+                                         uint32_t zrow, uint32_t r0, uint32_t r8, uint32_t c) {
 #pragma unroll
         for (int j = 0; j < kTilesPerChunk; ++j) w[j] = ldg_stream(wp + j * kTileBytes);
-        const uint32_t nlast = (uint32_t)L.N - 1u;
-        const uint32_t n0 = (uint32_t)rt * 16u + (uint32_t)g;
-        const uint32_t r0 = n0 < nlast ? n0 : nlast, r8 = n0 + 8u < nlast ? n0 + 8u : nlast;
-        const uint32_t srow = (uint32_t)L.KB * (SDT == kF32 ? 4u : 2u);
-        const uint8_t* sp = static_cast<const uint8_t*>(p.scales) + (uint32_t)c * (uint32_t)SBYTES;
-        ld_raw<SBYTES>(sp + r0 * srow, s0);
-        ld_raw<SBYTES>(sp + r8 * srow, s8);
-        if (p.zp != nullptr) {
-            const uint32_t zbit = (uint32_t)c * (uint32_t)ZBITS;
-            const uint8_t* zp = p.zp + (zbit >> 3);
-            const uint32_t zrow = (uint32_t)L.zp_row;
-            ld_raw<ZBYTES>(zp + r0 * zrow, z0);
-            ld_raw<ZBYTES>(zp + r8 * zrow, z8);
+        const uint32_t cs = c * (uint32_t)SBYTES;
+        ld_raw<SBYTES>(sb + (r0 * srow + cs), s0);
+        ld_raw<SBYTES>(sb + (r8 * srow + cs), s8);
+        if (zb != nullptr) {
+            const uint32_t zbit = c * (uint32_t)ZBITS;
+            const uint32_t zo = zbit >> 3;
+            ld_raw<ZBYTES>(zb + (r0 * zrow + zo), z0);
+            ld_raw<ZBYTES>(zb + (r8 * zrow + zo), z8);
             zshift = ZBITS < 8 ? (zbit & 7u) : 0u;
         } else {
 #pragma unroll
@@ -241,12 +244,15 @@ struct Item {
 };
 
 // Position of a warp in its CTA's item list.
+// Position of a warp in its CTA's item list: item i = (local row tile rt,
+// chunk c); a step of kW items moves q16 row tiles and r16 chunks.
 struct Cursor {
     int i, rt, c;
-    __device__ __forceinline__ void advance(int KC) {
+    __device__ __forceinline__ void advance(int KC, int q16, int r16) {
         i += kW;
-        c += kW;
-        while (c >= KC) {
+        c += r16;
+        rt += q16;
+        if (c >= KC) {
             c -= KC;
             ++rt;
         }
@@ -267,23 +273,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     const int g = lane >> 2, t = lane & 3;
     const int M = M1 ? 1 : (int)p.M;
     const int KC = geo.KC;
-    const int64_t rt0 = (int64_t)blockIdx.x * L.NT / geo.G;
-    const int nrt = (int)((int64_t)(blockIdx.x + 1) * L.NT / geo.G - rt0);
+    const uint32_t NT32 = (uint32_t)L.NT;
+    const int64_t rt0 = (int64_t)(blockIdx.x * NT32 / (uint32_t)geo.G);
+    const int nrt = (int)((blockIdx.x + 1) * NT32 / (uint32_t)geo.G - (uint32_t)rt0);
     const int n_items = nrt * KC;
     // the packed tiles of (row tile, chunk) follow each other in item order
     const uint8_t* wbase = p.packed + rt0 * L.KTILES * kTileBytes + lane * 16;
+    const uint32_t srow = (uint32_t)L.KB * (SDT == kF32 ? 4u : 2u), zrow = (uint32_t)L.zp_row;
+    const uint8_t* sb = static_cast<const uint8_t*>(p.scales) + (size_t)rt0 * 16 * srow;
+    const uint8_t* zb = p.zp != nullptr ? p.zp + (size_t)rt0 * 16 * zrow : nullptr;
+    const uint32_t nlast = (uint32_t)(L.N - 1 - rt0 * 16);  // last row, local
+    const int q16 = geo.q16, r16 = geo.r16;
     auto load = [&](It& b, const Cursor& it) {
-        if (it.i < n_items)
-            b.load(p, wbase + (size_t)(uint32_t)it.i * (size_t)(kTilesPerChunk * kTileBytes), rt0 + it.rt, it.c, g);
+        if (it.i < n_items) {
+            const uint32_t nl = (uint32_t)it.rt * 16u + (uint32_t)g;
+            const uint32_t r0 = min(nl, nlast), r8 = min(nl + 8u, nlast);
+            b.load(wbase + (uint32_t)it.i * (uint32_t)kItemBytes, sb, zb, srow, zrow, r0, r8, (uint32_t)it.c);
+        }
     };
 
     // ---- 1. this warp's first item (constant data: before the dependency
     //         wait), X staged in B-fragment order, then the second item: X
     //         queues behind one item of weights, not two ----
     It buf[2];
-    Cursor cur = Cursor{warp, warp / KC, warp % KC};
+    Cursor cur = Cursor{warp, 0, warp};
+    while (cur.c >= KC) {  // at most kW - 1 times
+        cur.c -= KC;
+        ++cur.rt;
+    }
     Cursor nxt = cur;
-    nxt.advance(KC);
+    nxt.advance(KC, q16, r16);
     load(buf[0], cur);
     for (int o = tid; o < nrt * kW * 16 * M; o += kThreads) red[o] = 0.f;
     const int pairs = (int)(L.K / 32);
@@ -297,11 +316,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
         // (x[k0 + 2tt..], x[k0 + 8 + 2tt..], x[k0 + 16 + 2tt..], x[k0 + 24 + 2tt..])
         const uint32_t* x32 = static_cast<const uint32_t*>(p.x);  // K even: rows are 4-byte aligned
         const int64_t kw = L.K / 2;
-        for (int o = tid; o < M * pairs * 4; o += kThreads) {
-            const int m = o / (pairs * 4), r = o - m * (pairs * 4);
-            const int P = r >> 2, tt = r & 3;
-            const uint32_t* src = x32 + m * kw + P * 16 + tt;
-            xs[(size_t)m * geo.xrow + r] = make_uint4(__ldg(src), __ldg(src + 4), __ldg(src + 8), __ldg(src + 12));
+        for (int m = 0; m < M; ++m) {
+            for (int r = tid; r < pairs * 4; r += kThreads) {
+                const int P = r >> 2, tt = r & 3;
+                const uint32_t* src = x32 + m * kw + P * 16 + tt;
+                xs[(size_t)m * geo.xrow + r] = make_uint4(__ldg(src), __ldg(src + 4), __ldg(src + 8), __ldg(src + 12));
+            }
         }
     }
     load(buf[1], nxt);
@@ -327,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     auto step = [&](It& b) {
         b.template compute<M1>(xa_lane + (uint32_t)cur.c * (uint32_t)(CH / 2) * 64u, y);
         Cursor after = nxt;
-        after.advance(KC);
+        after.advance(KC, q16, r16);
         load(b, after);
         if (nxt.i >= n_items || nxt.rt != cur.rt) flush(cur.rt);
         cur = nxt;
