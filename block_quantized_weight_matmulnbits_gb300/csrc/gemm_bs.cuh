@@ -56,6 +56,11 @@ constexpr int kRsWarps = 16;      // rescale + epilogue
 constexpr int kThreads = (kCtlWarps + kDqWarps + kRsWarps) * 32;
 constexpr int kMaxR = 4;
 constexpr int kMaxNP = 4;
+constexpr int kSaR = 4;           // accuracy level 4: ring slots of activation scales
+constexpr int kSaNB = 8;          // blocks per slot
+// mbarriers, the tensor-memory address and the abort flag (rounded to 256 B:
+// the activation-scale ring after them takes 16-byte aligned bulk copies)
+constexpr size_t kBarBytes = ((3 * kMaxR + 2 * kMaxNP + 1 + 2 * kSaR) * 8 + 16 + 255) / 256 * 256;
 
 struct Geom {
     int BT;             // tokens per tile (MMA N): 32, 64 or 128
@@ -66,7 +71,8 @@ struct Geom {
     int tmem_cols;      // allocated columns (power of two)
     int a_col0;         // first column of the A ring (= NP * BT)
     size_t x_stage, wp_stage, total_bytes;
-    const float* sa;    // accuracy level 4: activation scales s_a [M, KB] (X holds the int8 codes as bf16)
+    const float* sa;    // accuracy level 4: activation scales s_a, [KB][sa_ld] (X holds the int8 codes as bf16)
+    int64_t sa_ld;      // tokens per row of s_a (a multiple of BT; zeros past M)
 };
 
 struct Maps {
@@ -98,8 +104,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Ge
     uint64_t* part_full = bars + 3 * kMaxR;                // partial of a block complete
     uint64_t* part_free = part_full + kMaxNP;              // partial read out (kRsWarps arrivals)
     uint64_t* done = part_free + kMaxNP;                   // every MMA finished
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    uint64_t* sa_full = done + 1;                          // [kSaR] activation scales of a slot landed
+    uint64_t* sa_free = sa_full + kSaR;                    // [kSaR] slot read out (kRsWarps arrivals)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sa_free + kSaR);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+    // [kSaR][kSaNB][BT] f32 (accuracy level 4 only)
+    float* sa_ring = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kBarBytes);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -123,6 +133,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Ge
             mbar_init(&part_free[b], kRsWarps);
         }
         mbar_init(done, 1);
+        for (int s = 0; s < kSaR; ++s) {
+            mbar_init(&sa_full[s], 1);
+            mbar_init(&sa_free[s], kRsWarps);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -208,6 +222,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Ge
             tc::drain_wait(done, 0);
         }
         __syncwarp();
+    } else if (A8 && warp == 2) {
+        // ---------------- activation scales: one slot per kSaNB blocks ----------------
+        if (lane == 0) {
+            const int nch = (int)((L.KB + kSaNB - 1) / kSaNB);
+            int issued = 0;
+            for (int c = 0; c < nch; ++c) {
+                const int s = c % kSaR;
+                const uint32_t ph = (uint32_t)((c / kSaR) & 1);
+                if (c >= kSaR && !tc::wait_bounded(&sa_free[s], ph ^ 1u, p.status, wl, wh)) {
+                    *abort_v = 1;
+                    break;
+                }
+                if (*abort_v) break;
+                const int nb = (int)imin64(kSaNB, L.KB - (int64_t)c * kSaNB);
+                mbar_arrive_expect_tx(&sa_full[s], (uint32_t)(nb * BT * 4));
+                for (int j = 0; j < nb; ++j) {
+                    const float* src = geo.sa + ((int64_t)c * kSaNB + j) * geo.sa_ld + m0;
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                            smem_u32(sa_ring + (s * kSaNB + j) * BT)),
+                        "l"(src), "r"((uint32_t)(BT * 4)), "r"(smem_u32(&sa_full[s]))
+                        : "memory");
+                }
+                issued = c + 1;
+            }
+            if (*abort_v) {  // let the copies in flight land before the CTA can exit
+                for (int c = issued - kSaR < 0 ? 0 : issued - kSaR; c < issued; ++c)
+                    tc::drain_wait(&sa_full[c % kSaR], (uint32_t)((c / kSaR) & 1));
+            }
+        }
     } else if (warp >= kCtlWarps && warp < kCtlWarps + kDqWarps) {
         // ---------------- A = (q - zp), one W row per thread ----------------
         const int dw = warp - kCtlWarps;
@@ -343,11 +387,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Ge
         bool ok = true;
         for (int64_t b = 0; b < L.KB; ++b) {
             const int pb = (int)(b % NP);
-            float sa_col[A8 ? CW : 1];  // the tokens' activation scales of block b (loaded before the wait)
-            if constexpr (A8) {
-                const int64_t mc = m0 + cs * CW;
-#pragma unroll
-                for (int j = 0; j < CW; ++j) sa_col[j] = mc + j < p.M ? __ldg(geo.sa + (mc + j) * L.KB + b) : 0.f;
+            // accuracy level 4: this warp's CW activation scales of block b, from the ring
+            const int sc_c = (int)(b / kSaNB), sc_j = (int)(b % kSaNB), sc_s = sc_c % kSaR;
+            const uint64_t* sa_b = reinterpret_cast<const uint64_t*>(sa_ring + (sc_s * kSaNB + sc_j) * BT + cs * CW);
+            if (A8 && sc_j == 0 &&
+                !tc::wait_bounded(&sa_full[sc_s], (uint32_t)((sc_c / kSaR) & 1), p.status, wl, wh)) {
+                ok = false;
+                break;
             }
             if (!tc::wait_bounded(&part_full[pb], (uint32_t)((b / NP) & 1), p.status, wl, wh)) {
                 ok = false;
@@ -375,12 +421,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Ge
 #pragma unroll
                 for (int i = 0; i < CH / 2; ++i) {
                     if constexpr (A8) {
-                        const uint64_t sj = pack2(__fmul_rn(sc, sa_col[c0 + 2 * i]), __fmul_rn(sc, sa_col[c0 + 2 * i + 1]));
+                        const uint64_t sj = fmul2(sc2, sa_b[c0 / 2 + i]);  // f32(s_w * s_a) per token
                         y2[c0 / 2 + i] = ffma2(pack2u(P[2 * i], P[2 * i + 1]), sj, y2[c0 / 2 + i]);
                     } else {
                         y2[c0 / 2 + i] = ffma2(pack2u(P[2 * i], P[2 * i + 1]), sc2, y2[c0 / 2 + i]);
                     }
                 }
+            }
+            if (A8 && (sc_j == kSaNB - 1 || b == L.KB - 1)) {  // this warp is done with the slot
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sa_free[sc_s]);
             }
         }
         if (!ok) *abort_v = 1;

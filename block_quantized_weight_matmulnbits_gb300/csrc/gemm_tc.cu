@@ -74,7 +74,7 @@ Geom make_geom(const MatmulParams& p, int max_bt = 128) {
     g.k_stages = (int)((L.Kpad + gbs::kBK - 1) / gbs::kBK);
     g.x_stage = (size_t)g.BT * gbs::kBK * 2;
     g.wp_stage = (size_t)(gbs::kRows / 16) * (gbs::kBK / L.KT) * kTileBytes;
-    const size_t fixed = 1024 + (3 * gbs::kMaxR + 2 * gbs::kMaxNP + 1) * 8 + 16;
+    const size_t fixed = 1024 + gbs::kBarBytes;
     const size_t limit = device_info().smem_optin ? device_info().smem_optin : 232448;
     g.R = gbs::kMaxR;
     while (g.R > 2 && fixed + g.R * (g.x_stage + g.wp_stage) > limit) --g.R;
@@ -211,7 +211,8 @@ bool gemm_a8_supported(const MatmulParams& p) {
     const DeviceInfo& di = device_info();
     if (di.major != 10 || !encode_fn()) return false;
     const Geom g = make_geom(p, 64);
-    return g.NP >= 2 && g.total_bytes <= di.smem_optin && (int64_t)g.n_tiles * g.m_tiles < (int64_t)1 << 31;
+    const size_t ring = (size_t)gbs::kSaR * gbs::kSaNB * g.BT * sizeof(float);  // activation-scale slots
+    return g.NP >= 2 && g.total_bytes + ring <= di.smem_optin && (int64_t)g.n_tiles * g.m_tiles < (int64_t)1 << 31;
 }
 
 // Accuracy level 4 prefill: quantise X per block into bf16 codes and f32
@@ -228,6 +229,10 @@ cudaError_t launch_gemm_a8(const MatmulParams& p, cudaStream_t s) {
     q.act_dtype = kBF16;
     Geom geo = make_geom(q, 64);
     geo.sa = sa;
+    geo.sa_ld = a8_gemm_sa_ld(p.M);
+    geo.total_bytes += (size_t)gbs::kSaR * gbs::kSaNB * geo.BT * sizeof(float);
+    const size_t limit = device_info().smem_optin ? device_info().smem_optin : 232448;
+    if (geo.total_bytes > limit) return cudaErrorNotSupported;
     Maps m;
     e = make_bs_maps(q, geo, enc, qab, p.L.Kpad, kBF16, &m);
     if (e != cudaSuccess) return e;
