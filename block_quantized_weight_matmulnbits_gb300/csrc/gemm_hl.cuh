@@ -32,6 +32,16 @@
 //                slot and one commit that frees the slot.
 //   warps 4-11   write A_hi, A_lo for one W row per thread (its TMEM lane),
 //                32 depths of every stage each; then the epilogue.
+//
+// TF32 variant (accuracy level 4 above 16 rows): X holds the activations as
+// the per-block int8 codes times their block scales (onnx-runtime-ep-cpu
+// matmul_nbits.rs, fn quantize_activation_signed: x ~ code * s_a), rounded to
+// tf32 by the quantising kernel, and A holds w = (q - zp) * scale rounded to
+// tf32: one kind::tf32 MMA (K = 8) per 8 depths, BT = 128 tokens (the X
+// stage is the same 32 KB), A slots of 64 columns (one per depth).  Each
+// operand carries at most 2^-11 relative error, so a product is within
+// 2^-10 of x * w, inside the library's bound, and no per-block rescale of a
+// partial is needed (the block scales are in the operands).
 // Every mbarrier wait is bounded (MNB_ERR_TIMEOUT, copies and MMAs in flight
 // drained with a fixed bound, tensor memory freed).  Reduction orders are
 // fixed, so results are deterministic.
@@ -44,6 +54,7 @@ namespace ghl {
 
 constexpr int kRows = 128;       // W rows per tile = TMEM lanes = MMA M
 constexpr int kBT = 256;         // tokens per tile = MMA N
+constexpr int kBTtf = 128;       // tokens per tile of the tf32 variant
 constexpr int kBK = 64;          // depths per stage (4 k-steps)
 constexpr int kACols = 64;       // TMEM columns of one A slot: A_hi (32) then A_lo (32)
 constexpr int kCtlWarps = 4;
@@ -84,13 +95,14 @@ __device__ __forceinline__ void split_scale(float s, uint32_t* hi2, uint32_t* lo
     *lo2 = tc::cvt_bf16x2(rest, rest);
 }
 
-template <int BITS>
+template <int BITS, bool TF32>
 __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Geom geo,
                                                                const __grid_constant__ CUtensorMap xmap,
                                                                const __grid_constant__ CUtensorMap wmap) {
     constexpr int KT = 256 / BITS;                  // depths per packed tile
     constexpr int TILES = kBK >= KT ? kBK / KT : 1;  // packed tiles per 16-row tile per stage
     constexpr uint32_t kMag = 0x43004300u;           // bf16 128.0 in both halves
+    constexpr int BT = TF32 ? kBTtf : kBT;            // tokens per tile (MMA N)
     const Layout& L = p.L;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -110,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
     const int rank = geo.splitk == 2 ? (int)cluster_ctarank() : 0;
     const int n_tile = tile % geo.n_tiles, m_tile = tile / geo.n_tiles;
     const int64_t n0 = (int64_t)n_tile * kRows;
-    const int64_t m0 = (int64_t)m_tile * kBT;
+    const int64_t m0 = (int64_t)m_tile * BT;
     // stages of this CTA: all of K, or its half
     const int ks_lo = geo.splitk == 2 ? (rank == 0 ? 0 : geo.k_stages / 2) : 0;
     const int ks_hi = geo.splitk == 2 ? (rank == 0 ? geo.k_stages / 2 : geo.k_stages) : geo.k_stages;
@@ -132,8 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
-    const uint32_t tmem = *tmem_slot;            // accumulator: columns [0, 256)
-    const uint32_t a_base = tmem + (uint32_t)kBT;  // A ring: columns [256, 512)
+    const uint32_t tmem = *tmem_slot;           // accumulator: columns [0, BT)
+    const uint32_t a_base = tmem + (uint32_t)BT;  // A ring: columns [BT, BT + 256)
     volatile int* abort_v = abort_flag;
 
     if (warp == 0) {
@@ -152,7 +164,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
                 if (*abort_v) break;
                 const int ks = ks_lo + i;
                 mbar_arrive_expect_tx(&tma_full[s], bytes);
-                tc::tma_load_2d(xs + s * kXStage, &xmap, ks * kBK, (int)m0, &tma_full[s]);
+                if constexpr (TF32) {  // 64 depths of f32: two 128-byte boxes
+                    tc::tma_load_2d(xs + s * kXStage, &xmap, ks * kBK, (int)m0, &tma_full[s]);
+                    tc::tma_load_2d(xs + s * kXStage + BT * 128, &xmap, ks * kBK + 32, (int)m0, &tma_full[s]);
+                } else {
+                    tc::tma_load_2d(xs + s * kXStage, &xmap, ks * kBK, (int)m0, &tma_full[s]);
+                }
                 // packed tiles of this stage: KT >= 64 tiles span whole stages (one load per tile)
                 if constexpr (KT > kBK) {
                     tc::tma_load_5d(wp + s * geo.wp_stage, &wmap, 0, 0, 0, (ks * kBK) / KT, nrt, &tma_full[s]);
@@ -168,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
-        const uint32_t idesc = tc::idesc_f16(true, kRows, kBT);
+        const uint32_t idesc = TF32 ? tc::idesc_tf32(kRows, BT) : tc::idesc_f16(true, kRows, kBT);
         const uint64_t dx0 = tc::sdesc_sw128(smem_u32(xs));
         constexpr uint64_t x_step = (uint64_t)kXStage >> 4;
         bool ok = true;
@@ -184,13 +201,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
                 const uint64_t dxs = dx0 + (uint64_t)s * x_step;
                 const uint32_t as = a_base + (uint32_t)(s * kACols);
                 const int64_t gk0 = (int64_t)(ks_lo + i) * 4;
+                if constexpr (TF32) {
+                    // 8 MMAs of 8 depths: 32 bytes along K each, the second box from the 5th on
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    if (gk0 + kk < n_ksteps) {
-                        const uint64_t bd = dxs + (uint64_t)kk * 2;  // 32 bytes along K per k-step
-                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                        tc::mma_ta(tmem, as + (uint32_t)(kk * 8), bd, idesc, acc);
-                        tc::mma_ta(tmem, as + 32u + (uint32_t)(kk * 8), bd, idesc, 1u);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        if (gk0 + (kk >> 1) < n_ksteps) {
+                            const uint64_t bd = dxs + (uint64_t)(kk >> 2) * ((uint64_t)(BT * 128) >> 4) + (uint64_t)(kk & 3) * 2;
+                            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                            tc::mma_ta_tf32(tmem, as + (uint32_t)(kk * 8), bd, idesc, acc);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if (gk0 + kk < n_ksteps) {
+                            const uint64_t bd = dxs + (uint64_t)kk * 2;  // 32 bytes along K per k-step
+                            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                            tc::mma_ta(tmem, as + (uint32_t)(kk * 8), bd, idesc, acc);
+                            tc::mma_ta(tmem, as + 32u + (uint32_t)(kk * 8), bd, idesc, 1u);
+                        }
                     }
                 }
                 tc::commit(&mma_done[s]);
@@ -326,6 +355,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
                     qz[8 * kk + t + 4] = v1;
                 }
             }
+            if constexpr (TF32) {
+                // w = (q - zp) * scale in f32, rounded to tf32: one column per depth
+                static_assert(kKK == 1, "the tf32 variant writes one k-step per warp");
+                uint32_t av[16];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t v0 = qz[t], v1 = qz[t + 4];  // depths 2t, 2t+1 and 2t+8, 2t+9
+                    av[2 * t] = tc::cvt_tf32(__fmul_rn(__uint_as_float(v0 << 16), sc0));
+                    av[2 * t + 1] = tc::cvt_tf32(__fmul_rn(__uint_as_float(v0 & 0xFFFF0000u), sc0));
+                    av[2 * t + 8] = tc::cvt_tf32(__fmul_rn(__uint_as_float(v1 << 16), sc0));
+                    av[2 * t + 9] = tc::cvt_tf32(__fmul_rn(__uint_as_float(v1 & 0xFFFF0000u), sc0));
+                }
+                tc::st_32x32b_x16(a_base + (uint32_t)(s * kACols + 16 * jh) + lane_addr, av);
+                tc::wait_st();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[s]);
+                return true;
+            }
             uint32_t ah[8 * kKK], al[8 * kKK];
 #pragma unroll
             for (int c = 0; c < 8 * kKK; ++c) {
@@ -361,9 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
         bool fine = ok && !*abort_v && tc::wait_bounded(done, 0, p.status, wl, wh);
         tc::fence_after();
         const float bias = (p.bias && row_ok) ? load_f32(p.bias, n, p.bias_dtype) : 0.f;
-        if (geo.splitk == 1) {
+        if (TF32 || geo.splitk == 1) {
             // columns kEpi jh .. kEpi jh + kEpi - 1 of this thread's row
-            constexpr int kEpi = kBT / (kDqWarps / 4);
+            constexpr int kEpi = BT / (kDqWarps / 4);
             for (int c0 = kEpi * jh; c0 < kEpi * jh + kEpi && fine; c0 += 32) {
                 uint32_t v[32];
                 tc::ld_32x32b<32>(tmem + (uint32_t)c0 + lane_addr, v);
@@ -438,9 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
     if (blockIdx.x == 0 && tid == 0) verify_header(p.packed_hdr, L, p.status);
 }
 
-template <int BITS>
+template <int BITS, bool TF32 = false>
 cudaError_t launch(const MatmulParams& p, const Geom& geo, const Maps& m, cudaStream_t s) {
-    auto kern = gemm_hl_kernel<BITS>;
+    auto kern = gemm_hl_kernel<BITS, TF32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.total_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

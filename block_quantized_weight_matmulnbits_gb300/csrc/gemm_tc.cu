@@ -15,9 +15,9 @@ namespace mnb {
 cudaError_t launch_gemm_tc_b2(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s);
 cudaError_t launch_gemm_tc_b4(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s);
 cudaError_t launch_gemm_tc_b8(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s);
-cudaError_t launch_gemm_a8_b2(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s);
-cudaError_t launch_gemm_a8_b4(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s);
-cudaError_t launch_gemm_a8_b8(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s);
+cudaError_t launch_gemm_a8_b2(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s);
+cudaError_t launch_gemm_a8_b4(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s);
+cudaError_t launch_gemm_a8_b8(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s);
 cudaError_t launch_gemm_hl_b2(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s);
 cudaError_t launch_gemm_hl_b4(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s);
 cudaError_t launch_gemm_hl_b8(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s);
@@ -125,21 +125,37 @@ bool use_hl(const MatmulParams& p) {
 
 // hi/lo kernel: 128 W rows x 256 tokens per tile; the two CTAs of a cluster
 // split K when one tile per CTA would leave more than half the SMs idle.
-ghl::Geom make_geom_hl(const MatmulParams& p) {
+// tf32: the accuracy level 4 variant (128-token tiles, never split along K).
+ghl::Geom make_geom_hl(const MatmulParams& p, bool tf32 = false) {
     ghl::Geom g{};
     const Layout& L = p.L;
     const int sms = device_info().sm_count > 0 ? device_info().sm_count : 148;
+    const int bt = tf32 ? ghl::kBTtf : ghl::kBT;
     g.n_tiles = (int)((L.N + ghl::kRows - 1) / ghl::kRows);
-    g.m_tiles = (int)((p.M + ghl::kBT - 1) / ghl::kBT);
+    g.m_tiles = (int)((p.M + bt - 1) / bt);
     g.k_stages = (int)((L.Kpad + ghl::kBK - 1) / ghl::kBK);
     const int64_t tiles = (int64_t)g.n_tiles * g.m_tiles;
     g.splitk = (2 * tiles <= sms && g.k_stages >= 2) ? 2 : 1;
     const char* env = std::getenv("MNB_TC_SPLITK");
     if (env && (env[0] == '1' || env[0] == '2')) g.splitk = (env[0] == '2' && g.k_stages >= 2) ? 2 : 1;
+    if (tf32) g.splitk = 1;
     const int tiles_per_stage = L.KT >= ghl::kBK ? 1 : (int)(ghl::kBK / L.KT);
     g.wp_stage = (size_t)(ghl::kRows / 16) * tiles_per_stage * kTileBytes;
     g.total_bytes = 1024 + ghl::kR * (ghl::kXStage + g.wp_stage) + (3 * ghl::kR + 1) * 8 + 16;
     return g;
+}
+
+// The packed codes of the hi/lo and tf32 kernels: each 512-byte tile as [chunk
+// t][row group g][16 B], one stage's tiles of 128 rows per box.
+CUresult hl_wmap(const MatmulParams& p, EncodeTiledFn enc, CUtensorMap* w) {
+    const cuuint64_t tdims[5] = {8, 8, 4, (cuuint64_t)p.L.KTILES, (cuuint64_t)p.L.NT};
+    const cuuint64_t tstrides[4] = {64, 16, (cuuint64_t)kTileBytes, (cuuint64_t)p.L.KTILES * kTileBytes};
+    const cuuint32_t tbox[5] = {8, 8, 4, (cuuint32_t)(p.L.KT >= ghl::kBK ? 1 : ghl::kBK / p.L.KT),
+                                (cuuint32_t)(ghl::kRows / 16)};
+    const cuuint32_t testr[5] = {1, 1, 1, 1, 1};
+    return enc(w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<uint8_t*>(p.packed), tdims, tstrides, tbox, testr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 cudaError_t launch_hl(const MatmulParams& p, EncodeTiledFn enc, cudaStream_t s) {
@@ -154,15 +170,7 @@ cudaError_t launch_hl(const MatmulParams& p, EncodeTiledFn enc, cudaStream_t s) 
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    const cuuint64_t tdims[5] = {8, 8, 4, (cuuint64_t)p.L.KTILES, (cuuint64_t)p.L.NT};
-    const cuuint64_t tstrides[4] = {64, 16, (cuuint64_t)kTileBytes, (cuuint64_t)p.L.KTILES * kTileBytes};
-    const cuuint32_t tbox[5] = {8, 8, 4, (cuuint32_t)(p.L.KT >= ghl::kBK ? 1 : ghl::kBK / p.L.KT),
-                                (cuuint32_t)(ghl::kRows / 16)};
-    const cuuint32_t testr[5] = {1, 1, 1, 1, 1};
-    r = enc(&m.w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<uint8_t*>(p.packed), tdims, tstrides, tbox, testr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (hl_wmap(p, enc, &m.w) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     switch (p.L.bits) {
         case 2: return launch_gemm_hl_b2(p, geo, m, s);
         case 4: return launch_gemm_hl_b4(p, geo, m, s);
@@ -210,32 +218,32 @@ bool gemm_a8_supported(const MatmulParams& p) {
     if (p.g_idx != nullptr || p.M < 1 || p.M > (int64_t)1 << 31 || p.L.Kpad > (int64_t)1 << 31) return false;
     const DeviceInfo& di = device_info();
     if (di.major != 10 || !encode_fn()) return false;
-    const Geom g = make_geom(p, 64);
-    const size_t ring = (size_t)gbs::kSaR * gbs::kSaNB * g.BT * sizeof(float);  // activation-scale slots
-    return g.NP >= 2 && g.total_bytes + ring <= di.smem_optin && (int64_t)g.n_tiles * g.m_tiles < (int64_t)1 << 31;
+    const ghl::Geom g = make_geom_hl(p, true);
+    return g.total_bytes <= di.smem_optin && (int64_t)g.n_tiles * g.m_tiles < (int64_t)1 << 31;
 }
 
-// Accuracy level 4 prefill: quantise X per block into bf16 codes and f32
-// scales in the workspace, then the block-scaled GEMM over the codes.
+// Accuracy level 4 prefill: quantise X per block and write code * s_a as
+// tf32 into the workspace, then the tf32 variant of the hi/lo kernel.
 cudaError_t launch_gemm_a8(const MatmulParams& p, cudaStream_t s) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    uint16_t* qab = static_cast<uint16_t*>(p.workspace);
-    float* sa = reinterpret_cast<float*>(static_cast<uint8_t*>(p.workspace) + a8_gemm_codes_bytes(p.M, p.L));
-    cudaError_t e = launch_quant_act_bf16(p.x, p.act_dtype, qab, sa, p.M, p.L, (p.flags & kFlagPDL) != 0, s);
+    float* xq = static_cast<float*>(p.workspace);
+    cudaError_t e = launch_quant_act_tf32(p.x, p.act_dtype, xq, p.M, p.L, (p.flags & kFlagPDL) != 0, s);
     if (e != cudaSuccess) return e;
     MatmulParams q = p;
-    q.x = qab;
-    q.act_dtype = kBF16;
-    Geom geo = make_geom(q, 64);
-    geo.sa = sa;
-    geo.sa_ld = a8_gemm_sa_ld(p.M);
-    geo.total_bytes += (size_t)gbs::kSaR * gbs::kSaNB * geo.BT * sizeof(float);
-    const size_t limit = device_info().smem_optin ? device_info().smem_optin : 232448;
-    if (geo.total_bytes > limit) return cudaErrorNotSupported;
-    Maps m;
-    e = make_bs_maps(q, geo, enc, qab, p.L.Kpad, kBF16, &m);
-    if (e != cudaSuccess) return e;
+    q.x = xq;
+    q.act_dtype = kF32;
+    const ghl::Geom geo = make_geom_hl(q, true);
+    ghl::Maps m;
+    std::memset(&m, 0, sizeof(m));
+    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t dims[2] = {(cuuint64_t)p.L.Kpad, (cuuint64_t)p.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.L.Kpad * 4};
+    const cuuint32_t box[2] = {32, ghl::kBTtf};  // 128 bytes of depth x 128 tokens
+    CUresult r = enc(&m.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, xq, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS || hl_wmap(q, enc, &m.w) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     switch (p.L.bits) {
         case 2: return launch_gemm_a8_b2(q, geo, m, s);
         case 4: return launch_gemm_a8_b4(q, geo, m, s);

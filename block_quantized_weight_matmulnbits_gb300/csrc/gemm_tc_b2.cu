@@ -8,8 +8,8 @@ cudaError_t launch_gemm_tc_b2(const MatmulParams& p, const gbs::Geom& geo, const
     const bool bf = p.act_dtype == kBF16;
     return bf ? gbs::launch<2, true>(p, geo, m, s) : gbs::launch<2, false>(p, geo, m, s);
 }
-cudaError_t launch_gemm_a8_b2(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s) {
-    return gbs::launch<2, true, true>(p, geo, m, s);
+cudaError_t launch_gemm_a8_b2(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s) {
+    return ghl::launch<2, true>(p, geo, m, s);
 }
 cudaError_t launch_gemm_hl_b2(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s) {
     return ghl::launch<2>(p, geo, m, s);

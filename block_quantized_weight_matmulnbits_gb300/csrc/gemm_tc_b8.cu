@@ -8,8 +8,8 @@ cudaError_t launch_gemm_tc_b8(const MatmulParams& p, const gbs::Geom& geo, const
     const bool bf = p.act_dtype == kBF16;
     return bf ? gbs::launch<8, true>(p, geo, m, s) : gbs::launch<8, false>(p, geo, m, s);
 }
-cudaError_t launch_gemm_a8_b8(const MatmulParams& p, const gbs::Geom& geo, const gbs::Maps& m, cudaStream_t s) {
-    return gbs::launch<8, true, true>(p, geo, m, s);
+cudaError_t launch_gemm_a8_b8(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s) {
+    return ghl::launch<8, true>(p, geo, m, s);
 }
 cudaError_t launch_gemm_hl_b8(const MatmulParams& p, const ghl::Geom& geo, const ghl::Maps& m, cudaStream_t s) {
     return ghl::launch<8>(p, geo, m, s);

@@ -5,27 +5,19 @@ namespace mnb {
 namespace gi8 {
 
 // ---- 1. activation quantisation: one warp per (m, kb) ----
-// Codes go to qa (int8) or, for the prefill GEMM, to qab as bf16 values
-// (|code| <= 127: exact); rows are Kpad long either way.
-// sa_ld == 0: s_a as [M][KB]; sa_ld >= M: s_a transposed, [KB][sa_ld], with
-// zeros for the padding tokens M <= m < sa_ld (the prefill GEMM reads whole
-// token tiles of one block's scales).
-__global__ void __launch_bounds__(256) quant_act_kernel(const void* x, int dt, int8_t* qa, uint16_t* qab, float* sa,
-                                                        int64_t M, Layout L, int64_t sa_ld) {
+// Codes go to qa (int8, with the block scales to sa [M][KB]) or, for the
+// prefill GEMM, to xq as code * s_a rounded to tf32 (f32 containers, the
+// activation the GEMM's tf32 MMA multiplies); rows are Kpad long either way.
+__global__ void __launch_bounds__(256) quant_act_kernel(const void* x, int dt, int8_t* qa, float* xq, float* sa,
+                                                        int64_t M, Layout L) {
     // The previous kernel on the stream may have written x, or may still be
     // reading this workspace; no-op when not launched as a dependent.
     griddep_wait();
-    griddep_launch_dependents();  // the GEMV may start streaming its weights
+    griddep_launch_dependents();  // the next kernel may start streaming its weights
     const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t rows = sa_ld ? sa_ld : M;
-    if (w >= rows * L.KB) return;
+    if (w >= M * L.KB) return;
     const int64_t m = w / L.KB, kb = w - m * L.KB;
-    float* sa_at = sa_ld ? sa + kb * sa_ld + m : sa + m * L.KB + kb;
-    if (m >= M) {  // padding token of the transposed layout
-        if (lane == 0) *sa_at = 0.f;
-        return;
-    }
     const int64_t k0 = kb * L.bs;
     const int64_t k1 = imin64(k0 + L.bs, L.K);
     float amax = 0.f;
@@ -33,15 +25,20 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const void* x, int dt, i
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
     const float s = __fdiv_rn(amax, 127.0f);
-    if (lane == 0) *sa_at = s;
+    if (sa && lane == 0) sa[m * L.KB + kb] = s;
     for (int64_t k = k0 + lane; k < k0 + L.bs; k += 32) {
         int code = 0;
         if (k < L.K && amax > 0.f) {
             const float r = roundf(__fdiv_rn(load_f32(x, m * L.K + k, dt), s));  // half away from zero
             code = (int)fminf(fmaxf(r, -127.f), 127.f);
         }
-        if (qab) qab[m * L.Kpad + k] = (uint16_t)(__float_as_uint((float)code) >> 16);  // exact in bf16
-        else qa[m * L.Kpad + k] = (int8_t)code;
+        if (xq) {
+            uint32_t t;  // code * s_a, rounded to tf32 (nearest, ties away)
+            asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(t) : "f"(__fmul_rn((float)code, s)));
+            xq[m * L.Kpad + k] = __uint_as_float(t);
+        } else {
+            qa[m * L.Kpad + k] = (int8_t)code;
+        }
     }
 }
 
@@ -67,9 +64,9 @@ bool gemv_i8_supported(const MatmulParams& p) {
     return g.total_bytes <= device_info().smem_optin && p.L.NT * g.C <= 0x7FFFFFFF;
 }
 
-static cudaError_t quant_launch(const void* x, int act_dtype, int8_t* qa, uint16_t* qab, float* sa, int64_t M,
-                                const Layout& L, bool pdl, cudaStream_t s, int64_t sa_ld = 0) {
-    const int64_t warps = (sa_ld ? sa_ld : M) * L.KB;
+static cudaError_t quant_launch(const void* x, int act_dtype, int8_t* qa, float* xq, float* sa, int64_t M,
+                                const Layout& L, bool pdl, cudaStream_t s) {
+    const int64_t warps = M * L.KB;
     const int64_t blocks = (warps + 7) / 8;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
@@ -82,7 +79,7 @@ static cudaError_t quant_launch(const void* x, int act_dtype, int8_t* qa, uint16
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gi8::quant_act_kernel, x, act_dtype, qa, qab, sa, M, L, sa_ld);
+    return cudaLaunchKernelEx(&cfg, gi8::quant_act_kernel, x, act_dtype, qa, xq, sa, M, L);
 }
 
 cudaError_t launch_quant_act(const void* x, int act_dtype, int8_t* qa, float* sa, int64_t M, const Layout& L,
@@ -90,9 +87,9 @@ cudaError_t launch_quant_act(const void* x, int act_dtype, int8_t* qa, float* sa
     return quant_launch(x, act_dtype, qa, nullptr, sa, M, L, false, s);
 }
 
-cudaError_t launch_quant_act_bf16(const void* x, int act_dtype, uint16_t* qab, float* sa, int64_t M, const Layout& L,
-                                  bool pdl, cudaStream_t s) {
-    return quant_launch(x, act_dtype, nullptr, qab, sa, M, L, pdl, s, a8_gemm_sa_ld(M));
+cudaError_t launch_quant_act_tf32(const void* x, int act_dtype, float* xq, int64_t M, const Layout& L, bool pdl,
+                                  cudaStream_t s) {
+    return quant_launch(x, act_dtype, nullptr, xq, nullptr, M, L, pdl, s);
 }
 
 cudaError_t launch_gemv_i8(const MatmulParams& p, cudaStream_t s) {

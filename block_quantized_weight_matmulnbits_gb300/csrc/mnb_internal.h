@@ -67,19 +67,13 @@ cudaError_t launch_fp_generic(const FpParams& p, cudaStream_t s);
 bool gemv_fp_supported(const FpParams& p);
 cudaError_t launch_gemv_fp(const FpParams& p, cudaStream_t s);
 
-// Accuracy level 4 on the prefill GEMM: workspace = activation codes as bf16
-// [M, Kpad] (256-byte aligned size) followed by the f32 scales s_a
-// transposed, [KB][sa_ld] with sa_ld = M rounded up to 64 tokens (zeros past
-// M), so that one block's scales of a token tile are contiguous.
-inline int64_t a8_gemm_sa_ld(int64_t M) { return (M + 63) / 64 * 64; }
-inline size_t a8_gemm_codes_bytes(int64_t M, const Layout& L) {
-    return ((size_t)M * (size_t)L.Kpad * 2 + 255) & ~size_t(255);
-}
+// Accuracy level 4 on the prefill GEMM: workspace = the quantised
+// activations code * s_a rounded to tf32, f32 [M, Kpad] (zeros past K).
 inline size_t a8_gemm_workspace_bytes(int64_t M, const Layout& L) {
-    return a8_gemm_codes_bytes(M, L) + (size_t)a8_gemm_sa_ld(M) * (size_t)L.KB * sizeof(float);
+    return ((size_t)M * (size_t)L.Kpad * 4 + 255) & ~size_t(255);
 }
-cudaError_t launch_quant_act_bf16(const void* x, int act_dtype, uint16_t* qab, float* sa, int64_t M, const Layout& L,
-                                  bool pdl, cudaStream_t s);
+cudaError_t launch_quant_act_tf32(const void* x, int act_dtype, float* xq, int64_t M, const Layout& L, bool pdl,
+                                  cudaStream_t s);
 bool gemm_a8_supported(const MatmulParams& p);
 cudaError_t launch_gemm_a8(const MatmulParams& p, cudaStream_t s);
 

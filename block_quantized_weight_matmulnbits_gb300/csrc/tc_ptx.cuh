@@ -43,6 +43,17 @@ __device__ __forceinline__ void mma_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] . B[smem]^T, kind::tf32 (A and B tf32 in 32-bit
+// containers, K = 8 per instruction), f32 accumulator.
+__device__ __forceinline__ void mma_ta_tf32(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D[tmem] (+)= A[tmem] . B[smem]^T, kind::i8 (A and B signed 8-bit), s32 accumulator.
 __device__ __forceinline__ void mma_ta_i8(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
@@ -158,6 +169,18 @@ __host__ __device__ inline uint32_t idesc_f16(bool bf16, int m, int n) {
     return d;
 }
 
+// Instruction descriptor of kind::tf32: f32 accumulator, A and B tf32 (format
+// code 2), both K-major, M = m, N = n.
+__host__ __device__ inline uint32_t idesc_tf32(int m, int n) {
+    uint32_t d = 0;
+    d |= 1u << 4;                    // D format: f32
+    d |= 2u << 7;                    // A format: tf32
+    d |= 2u << 10;                   // B format: tf32
+    d |= (uint32_t)(n >> 3) << 17;   // N / 8
+    d |= (uint32_t)(m >> 4) << 24;   // M / 16
+    return d;
+}
+
 // Instruction descriptor of kind::i8: s32 accumulator, A and B signed 8-bit,
 // both K-major, M = m, N = n.
 __host__ __device__ inline uint32_t idesc_i8(int m, int n) {
@@ -174,6 +197,14 @@ __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b, bool bf16) {
     uint32_t d;
     if (bf16) asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     else asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// f32 -> tf32, round to nearest (ties away from zero); the low 13 bits of the
+// result are zero.
+__device__ __forceinline__ uint32_t cvt_tf32(float v) {
+    uint32_t d;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(d) : "f"(v));
     return d;
 }
 

@@ -82,11 +82,10 @@ def test_fp_matmul_rejects_invalid_before_cuda():
 
 @pytest.mark.parametrize("M,K,bs", [(17, 4096, 32), (512, 4096, 32), (64, 1000, 128)])
 def test_a8_prefill_workspace_size(M, K, bs):
-    """Accuracy level 4 above 16 rows: bf16 activation codes [M, Kpad] (256-byte aligned) then
-    f32 block scales transposed, [KB, M rounded up to 64]."""
+    """Accuracy level 4 above 16 rows: the quantised activations code * s_a as tf32 in f32
+    containers, [M, Kpad], 256-byte aligned size."""
     kb = -(-K // bs)
-    codes = -(-(M * kb * bs * 2) // 256) * 256
-    assert mnb.mnb_workspace_size(M, 4096, K, 4, bs, 4) == codes + -(-M // 64) * 64 * kb * 4
+    assert mnb.mnb_workspace_size(M, 4096, K, 4, bs, 4) == -(-(M * kb * bs * 4) // 256) * 256
 
 
 def test_kernel_selection():

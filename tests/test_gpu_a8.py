@@ -216,7 +216,7 @@ def test_matmul_a8_prefill_forced_at_small_m(G, mnb, oracle_mod):
     w = _w(5, 150, 1024, 4, 32, (BF16, F16, BF16), True, 61)
     P = G.Problem(w)
     kb = -(-w.K // w.bs)
-    need = -(-(w.M * kb * w.bs * 2) // 256) * 256 + -(-w.M // 64) * 64 * kb * 4  # scales [KB, M up to 64]
+    need = -(-(w.M * kb * w.bs * 4) // 256) * 256  # code * s_a as tf32, [M, Kpad]
     y = P.run(kernel="gemm_tc", accuracy_level=4, workspace=G.aligned_empty(need))
     ref, mag = _oracle_a8(oracle_mod, P)
     G.assert_within(P.y64(y), ref, mag, w.out_dtype, "a8 prefill forced")
