@@ -56,11 +56,8 @@ constexpr int kRsWarps = 16;      // rescale + epilogue
 constexpr int kThreads = (kCtlWarps + kDqWarps + kRsWarps) * 32;
 constexpr int kMaxR = 4;
 constexpr int kMaxNP = 4;
-constexpr int kSaR = 4;           // accuracy level 4: ring slots of activation scales
-constexpr int kSaNB = 8;          // blocks per slot
-// mbarriers, the tensor-memory address and the abort flag (rounded to 256 B:
-// the activation-scale ring after them takes 16-byte aligned bulk copies)
-constexpr size_t kBarBytes = ((3 * kMaxR + 2 * kMaxNP + 1 + 2 * kSaR) * 8 + 16 + 255) / 256 * 256;
+// mbarriers, the tensor-memory address and the abort flag
+constexpr size_t kBarBytes = (3 * kMaxR + 2 * kMaxNP + 1) * 8 + 16;
 
 struct Geom {
     int BT;             // tokens per tile (MMA N): 32, 64 or 128
@@ -71,19 +68,13 @@ struct Geom {
     int tmem_cols;      // allocated columns (power of two)
     int a_col0;         // first column of the A ring (= NP * BT)
     size_t x_stage, wp_stage, total_bytes;
-    const float* sa;    // accuracy level 4: activation scales s_a, [KB][sa_ld] (X holds the int8 codes as bf16)
-    int64_t sa_ld;      // tokens per row of s_a (a multiple of BT; zeros past M)
 };
 
 struct Maps {
     CUtensorMap x, w;
 };
 
-// A8: accuracy level 4 (onnx-runtime-ep-cpu matmul_nbits.rs, int8_row /
-// int8_matmul_amx): X is the per-block int8 activation codes widened to bf16,
-// so a block's partial is the exact integer dot (|sum| < 2^24), and the
-// rescale multiplies it by f32(s_w[n, kb] * s_a[m, kb]).
-template <int BITS, bool BF16X, int BT, bool A8>
+template <int BITS, bool BF16X, int BT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Geom geo,
                                                                const __grid_constant__ CUtensorMap xmap,
                                                                const __grid_constant__ CUtensorMap wmap) {
@@ -104,12 +95,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Ge
     uint64_t* part_full = bars + 3 * kMaxR;                // partial of a block complete
     uint64_t* part_free = part_full + kMaxNP;              // partial read out (kRsWarps arrivals)
     uint64_t* done = part_free + kMaxNP;                   // every MMA finished
-    uint64_t* sa_full = done + 1;                          // [kSaR] activation scales of a slot landed
-    uint64_t* sa_free = sa_full + kSaR;                    // [kSaR] slot read out (kRsWarps arrivals)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sa_free + kSaR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-    // [kSaR][kSaNB][BT] f32 (accuracy level 4 only)
-    float* sa_ring = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kBarBytes);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -133,10 +120,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Ge
             mbar_init(&part_free[b], kRsWarps);
         }
         mbar_init(done, 1);
-        for (int s = 0; s < kSaR; ++s) {
-            mbar_init(&sa_full[s], 1);
-            mbar_init(&sa_free[s], kRsWarps);
-        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -222,36 +205,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Ge
             tc::drain_wait(done, 0);
         }
         __syncwarp();
-    } else if (A8 && warp == 2) {
-        // ---------------- activation scales: one slot per kSaNB blocks ----------------
-        if (lane == 0) {
-            const int nch = (int)((L.KB + kSaNB - 1) / kSaNB);
-            int issued = 0;
-            for (int c = 0; c < nch; ++c) {
-                const int s = c % kSaR;
-                const uint32_t ph = (uint32_t)((c / kSaR) & 1);
-                if (c >= kSaR && !tc::wait_bounded(&sa_free[s], ph ^ 1u, p.status, wl, wh)) {
-                    *abort_v = 1;
-                    break;
-                }
-                if (*abort_v) break;
-                const int nb = (int)imin64(kSaNB, L.KB - (int64_t)c * kSaNB);
-                mbar_arrive_expect_tx(&sa_full[s], (uint32_t)(nb * BT * 4));
-                for (int j = 0; j < nb; ++j) {
-                    const float* src = geo.sa + ((int64_t)c * kSaNB + j) * geo.sa_ld + m0;
-                    asm volatile(
-                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                            smem_u32(sa_ring + (s * kSaNB + j) * BT)),
-                        "l"(src), "r"((uint32_t)(BT * 4)), "r"(smem_u32(&sa_full[s]))
-                        : "memory");
-                }
-                issued = c + 1;
-            }
-            if (*abort_v) {  // let the copies in flight land before the CTA can exit
-                for (int c = issued - kSaR < 0 ? 0 : issued - kSaR; c < issued; ++c)
-                    tc::drain_wait(&sa_full[c % kSaR], (uint32_t)((c / kSaR) & 1));
-            }
-        }
     } else if (warp >= kCtlWarps && warp < kCtlWarps + kDqWarps) {
         // ---------------- A = (q - zp), one W row per thread ----------------
         const int dw = warp - kCtlWarps;
@@ -387,14 +340,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Ge
         bool ok = true;
         for (int64_t b = 0; b < L.KB; ++b) {
             const int pb = (int)(b % NP);
-            // accuracy level 4: this warp's CW activation scales of block b, from the ring
-            const int sc_c = (int)(b / kSaNB), sc_j = (int)(b % kSaNB), sc_s = sc_c % kSaR;
-            const uint64_t* sa_b = reinterpret_cast<const uint64_t*>(sa_ring + (sc_s * kSaNB + sc_j) * BT + cs * CW);
-            if (A8 && sc_j == 0 &&
-                !tc::wait_bounded(&sa_full[sc_s], (uint32_t)((sc_c / kSaR) & 1), p.status, wl, wh)) {
-                ok = false;
-                break;
-            }
             if (!tc::wait_bounded(&part_full[pb], (uint32_t)((b / NP) & 1), p.status, wl, wh)) {
                 ok = false;
                 break;
@@ -420,17 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Ge
                 }
 #pragma unroll
                 for (int i = 0; i < CH / 2; ++i) {
-                    if constexpr (A8) {
-                        const uint64_t sj = fmul2(sc2, sa_b[c0 / 2 + i]);  // f32(s_w * s_a) per token
-                        y2[c0 / 2 + i] = ffma2(pack2u(P[2 * i], P[2 * i + 1]), sj, y2[c0 / 2 + i]);
-                    } else {
-                        y2[c0 / 2 + i] = ffma2(pack2u(P[2 * i], P[2 * i + 1]), sc2, y2[c0 / 2 + i]);
-                    }
+                    y2[c0 / 2 + i] = ffma2(pack2u(P[2 * i], P[2 * i + 1]), sc2, y2[c0 / 2 + i]);
                 }
-            }
-            if (A8 && (sc_j == kSaNB - 1 || b == L.KB - 1)) {  // this warp is done with the slot
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sa_free[sc_s]);
             }
         }
         if (!ok) *abort_v = 1;
@@ -455,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Ge
     if (blockIdx.x == 0 && tid == 0) verify_header(p.packed_hdr, L, p.status);
 }
 
-template <int BITS, bool BF16X, bool A8 = false>
+template <int BITS, bool BF16X>
 cudaError_t launch(const MatmulParams& p, const Geom& geo, const Maps& m, cudaStream_t s) {
     auto go = [&](auto kern) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.total_bytes);
@@ -463,18 +399,10 @@ cudaError_t launch(const MatmulParams& p, const Geom& geo, const Maps& m, cudaSt
         kern<<<(unsigned)(geo.n_tiles * geo.m_tiles), kThreads, geo.total_bytes, s>>>(p, geo, m.x, m.w);
         return cudaGetLastError();
     };
-    if constexpr (A8) {  // at most 64 tokens per tile: a rescale thread holds CW activation scales
-        switch (geo.BT) {
-            case 32: return go(gemm_bs_kernel<BITS, true, 32, true>);
-            case 64: return go(gemm_bs_kernel<BITS, true, 64, true>);
-            default: return cudaErrorInvalidValue;
-        }
-    } else {
-        switch (geo.BT) {
-            case 32: return go(gemm_bs_kernel<BITS, BF16X, 32, false>);
-            case 64: return go(gemm_bs_kernel<BITS, BF16X, 64, false>);
-            default: return go(gemm_bs_kernel<BITS, BF16X, 128, false>);
-        }
+    switch (geo.BT) {
+        case 32: return go(gemm_bs_kernel<BITS, BF16X, 32>);
+        case 64: return go(gemm_bs_kernel<BITS, BF16X, 64>);
+        default: return go(gemm_bs_kernel<BITS, BF16X, 128>);
     }
 }
 

@@ -37,8 +37,9 @@
 // the per-block int8 codes times their block scales (onnx-runtime-ep-cpu
 // matmul_nbits.rs, fn quantize_activation_signed: x ~ code * s_a), rounded to
 // tf32 by the quantising kernel, and A holds w = (q - zp) * scale rounded to
-// tf32: one kind::tf32 MMA (K = 8) per 8 depths, BT = 128 tokens (the X
-// stage is the same 32 KB), A slots of 64 columns (one per depth).  Each
+// tf32: one kind::tf32 MMA (K = 8) per 8 depths, BT = 256 tokens, a 64 KB X
+// stage (f32) and a ring of three stages, A slots of 64 columns (one per
+// depth).  Each
 // operand carries at most 2^-11 relative error, so a product is within
 // 2^-10 of x * w, inside the library's bound, and no per-block rescale of a
 // partial is needed (the block scales are in the operands).
@@ -54,7 +55,6 @@ namespace ghl {
 
 constexpr int kRows = 128;       // W rows per tile = TMEM lanes = MMA M
 constexpr int kBT = 256;         // tokens per tile = MMA N
-constexpr int kBTtf = 128;       // tokens per tile of the tf32 variant
 constexpr int kBK = 64;          // depths per stage (4 k-steps)
 constexpr int kACols = 64;       // TMEM columns of one A slot: A_hi (32) then A_lo (32)
 constexpr int kCtlWarps = 4;
@@ -102,17 +102,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
     constexpr int KT = 256 / BITS;                  // depths per packed tile
     constexpr int TILES = kBK >= KT ? kBK / KT : 1;  // packed tiles per 16-row tile per stage
     constexpr uint32_t kMag = 0x43004300u;           // bf16 128.0 in both halves
-    constexpr int BT = TF32 ? kBTtf : kBT;            // tokens per tile (MMA N)
+    constexpr int BT = kBT;                           // tokens per tile (MMA N)
+    constexpr int R = TF32 ? 3 : kR;                  // ring depth
+    constexpr int XST = TF32 ? 2 * kXStage : kXStage; // X bytes per stage (f32 in the tf32 variant)
     const Layout& L = p.L;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t* xs = smem;                                      // [kR][BT x 128 B] (SW128, TMA)
-    uint8_t* wp = xs + kR * kXStage;                         // [kR][8 row tiles][TILES][512 B]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(wp + kR * geo.wp_stage);
-    uint64_t* tma_full = bars;                               // [kR]
-    uint64_t* a_full = bars + kR;                            // [kR] kDqWarps arrivals
-    uint64_t* mma_done = bars + 2 * kR;                      // [kR]
-    uint64_t* done = bars + 3 * kR;                          // the accumulator is complete
+    uint8_t* xs = smem;                                      // [R][BT x 128 B] (SW128, TMA)
+    uint8_t* wp = xs + R * XST;                         // [R][8 row tiles][TILES][512 B]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(wp + R * geo.wp_stage);
+    uint64_t* tma_full = bars;                               // [R]
+    uint64_t* a_full = bars + R;                            // [R] kDqWarps arrivals
+    uint64_t* mma_done = bars + 2 * R;                      // [R]
+    uint64_t* done = bars + 3 * R;                          // the accumulator is complete
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -131,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
     const uint32_t wl = p.wait_limit, wh = p.wait_hint_ns;
 
     if (tid == 0) {
-        for (int s = 0; s < kR; ++s) {
+        for (int s = 0; s < R; ++s) {
             mbar_init(&tma_full[s], 1);
             mbar_init(&a_full[s], kDqWarps);
             mbar_init(&mma_done[s], 1);
@@ -151,13 +153,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
     if (warp == 0) {
         // ---------------- producer ----------------
         if (lane == 0) {
-            const uint32_t bytes = (uint32_t)(kXStage + geo.wp_stage);
+            const uint32_t bytes = (uint32_t)(XST + geo.wp_stage);
             const int nrt = (int)(n0 / 16);
             int issued = 0;
             for (int i = 0; i < KS; ++i) {
-                const int s = i % kR;
-                const uint32_t ph = (uint32_t)((i / kR) & 1);
-                if (i >= kR && !tc::wait_bounded(&mma_done[s], ph ^ 1u, p.status, wl, wh)) {
+                const int s = i % R;
+                const uint32_t ph = (uint32_t)((i / R) & 1);
+                if (i >= R && !tc::wait_bounded(&mma_done[s], ph ^ 1u, p.status, wl, wh)) {
                     *abort_v = 1;
                     break;
                 }
@@ -165,10 +167,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
                 const int ks = ks_lo + i;
                 mbar_arrive_expect_tx(&tma_full[s], bytes);
                 if constexpr (TF32) {  // 64 depths of f32: two 128-byte boxes
-                    tc::tma_load_2d(xs + s * kXStage, &xmap, ks * kBK, (int)m0, &tma_full[s]);
-                    tc::tma_load_2d(xs + s * kXStage + BT * 128, &xmap, ks * kBK + 32, (int)m0, &tma_full[s]);
+                    tc::tma_load_2d(xs + s * XST, &xmap, ks * kBK, (int)m0, &tma_full[s]);
+                    tc::tma_load_2d(xs + s * XST + BT * 128, &xmap, ks * kBK + 32, (int)m0, &tma_full[s]);
                 } else {
-                    tc::tma_load_2d(xs + s * kXStage, &xmap, ks * kBK, (int)m0, &tma_full[s]);
+                    tc::tma_load_2d(xs + s * XST, &xmap, ks * kBK, (int)m0, &tma_full[s]);
                 }
                 // packed tiles of this stage: KT >= 64 tiles span whole stages (one load per tile)
                 if constexpr (KT > kBK) {
@@ -179,19 +181,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
                 issued = i + 1;
             }
             if (*abort_v) {
-                for (int i = issued - kR < 0 ? 0 : issued - kR; i < issued; ++i)
-                    tc::drain_wait(&tma_full[i % kR], (uint32_t)((i / kR) & 1));
+                for (int i = issued - R < 0 ? 0 : issued - R; i < issued; ++i)
+                    tc::drain_wait(&tma_full[i % R], (uint32_t)((i / R) & 1));
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         const uint32_t idesc = TF32 ? tc::idesc_tf32(kRows, BT) : tc::idesc_f16(true, kRows, kBT);
         const uint64_t dx0 = tc::sdesc_sw128(smem_u32(xs));
-        constexpr uint64_t x_step = (uint64_t)kXStage >> 4;
+        constexpr uint64_t x_step = (uint64_t)XST >> 4;
         bool ok = true;
         for (int i = 0; i < KS; ++i) {
-            const int s = i % kR;
-            const uint32_t ph = (uint32_t)((i / kR) & 1);
+            const int s = i % R;
+            const uint32_t ph = (uint32_t)((i / R) & 1);
             if (!tc::wait_bounded(&a_full[s], ph, p.status, wl, wh)) {
                 ok = false;
                 break;
@@ -296,10 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
         for (int q = 0; q < kPF; ++q)
             if (q < KS) fetch(ks_lo + q, &ps0[q], &ps1[q], &pz0[q], &pz1[q]);
         auto stage = [&](int i, uint32_t& slot_s0, uint32_t& slot_s1, uint32_t& slot_z0, uint32_t& slot_z1) -> bool {
-            const int s = i % kR;
-            const uint32_t ph = (uint32_t)((i / kR) & 1);
+            const int s = i % R;
+            const uint32_t ph = (uint32_t)((i / R) & 1);
             const int ks = ks_lo + i;
-            if (i >= kR && !tc::wait_bounded(&mma_done[s], ph ^ 1u, p.status, wl, wh)) {
+            if (i >= R && !tc::wait_bounded(&mma_done[s], ph ^ 1u, p.status, wl, wh)) {
                 return false;
             }
             if (!tc::wait_bounded(&tma_full[s], ph, p.status, wl, wh)) {
@@ -409,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
         bool fine = ok && !*abort_v && tc::wait_bounded(done, 0, p.status, wl, wh);
         tc::fence_after();
         const float bias = (p.bias && row_ok) ? load_f32(p.bias, n, p.bias_dtype) : 0.f;
-        if (TF32 || geo.splitk == 1) {
+        if (geo.splitk == 1) {
             // columns kEpi jh .. kEpi jh + kEpi - 1 of this thread's row
             constexpr int kEpi = BT / (kDqWarps / 4);
             for (int c0 = kEpi * jh; c0 < kEpi * jh + kEpi && fine; c0 += 32) {

@@ -125,23 +125,23 @@ bool use_hl(const MatmulParams& p) {
 
 // hi/lo kernel: 128 W rows x 256 tokens per tile; the two CTAs of a cluster
 // split K when one tile per CTA would leave more than half the SMs idle.
-// tf32: the accuracy level 4 variant (128-token tiles, never split along K).
+// tf32: the accuracy level 4 variant (f32 X stages of 64 KB, a ring of three).
 ghl::Geom make_geom_hl(const MatmulParams& p, bool tf32 = false) {
     ghl::Geom g{};
     const Layout& L = p.L;
     const int sms = device_info().sm_count > 0 ? device_info().sm_count : 148;
-    const int bt = tf32 ? ghl::kBTtf : ghl::kBT;
     g.n_tiles = (int)((L.N + ghl::kRows - 1) / ghl::kRows);
-    g.m_tiles = (int)((p.M + bt - 1) / bt);
+    g.m_tiles = (int)((p.M + ghl::kBT - 1) / ghl::kBT);
     g.k_stages = (int)((L.Kpad + ghl::kBK - 1) / ghl::kBK);
     const int64_t tiles = (int64_t)g.n_tiles * g.m_tiles;
     g.splitk = (2 * tiles <= sms && g.k_stages >= 2) ? 2 : 1;
     const char* env = std::getenv("MNB_TC_SPLITK");
     if (env && (env[0] == '1' || env[0] == '2')) g.splitk = (env[0] == '2' && g.k_stages >= 2) ? 2 : 1;
-    if (tf32) g.splitk = 1;
     const int tiles_per_stage = L.KT >= ghl::kBK ? 1 : (int)(ghl::kBK / L.KT);
     g.wp_stage = (size_t)(ghl::kRows / 16) * tiles_per_stage * kTileBytes;
-    g.total_bytes = 1024 + ghl::kR * (ghl::kXStage + g.wp_stage) + (3 * ghl::kR + 1) * 8 + 16;
+    const int R = tf32 ? 3 : ghl::kR;
+    const size_t xst = tf32 ? 2 * (size_t)ghl::kXStage : (size_t)ghl::kXStage;
+    g.total_bytes = 1024 + R * (xst + g.wp_stage) + (3 * R + 1) * 8 + 16;
     return g;
 }
 
@@ -239,7 +239,7 @@ cudaError_t launch_gemm_a8(const MatmulParams& p, cudaStream_t s) {
     const cuuint32_t estr[2] = {1, 1};
     const cuuint64_t dims[2] = {(cuuint64_t)p.L.Kpad, (cuuint64_t)p.M};
     const cuuint64_t strides[1] = {(cuuint64_t)p.L.Kpad * 4};
-    const cuuint32_t box[2] = {32, ghl::kBTtf};  // 128 bytes of depth x 128 tokens
+    const cuuint32_t box[2] = {32, ghl::kBT};  // 128 bytes of depth x 256 tokens
     CUresult r = enc(&m.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, xq, dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

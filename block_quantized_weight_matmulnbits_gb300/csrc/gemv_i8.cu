@@ -5,15 +5,14 @@ namespace mnb {
 namespace gi8 {
 
 // ---- 1. activation quantisation: one warp per (m, kb) ----
-// Codes go to qa (int8, with the block scales to sa [M][KB]) or, for the
-// prefill GEMM, to xq as code * s_a rounded to tf32 (f32 containers, the
-// activation the GEMM's tf32 MMA multiplies); rows are Kpad long either way.
-__global__ void __launch_bounds__(256) quant_act_kernel(const void* x, int dt, int8_t* qa, float* xq, float* sa,
-                                                        int64_t M, Layout L) {
+// Codes to qa (int8, rows Kpad long, zero past K) and the block scales to
+// sa [M][KB].
+__global__ void __launch_bounds__(256) quant_act_kernel(const void* x, int dt, int8_t* qa, float* sa, int64_t M,
+                                                        Layout L) {
     // The previous kernel on the stream may have written x, or may still be
     // reading this workspace; no-op when not launched as a dependent.
     griddep_wait();
-    griddep_launch_dependents();  // the next kernel may start streaming its weights
+    griddep_launch_dependents();  // the GEMV may start streaming its weights
     const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (w >= M * L.KB) return;
@@ -25,21 +24,73 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const void* x, int dt, i
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
     const float s = __fdiv_rn(amax, 127.0f);
-    if (sa && lane == 0) sa[m * L.KB + kb] = s;
+    if (lane == 0) sa[m * L.KB + kb] = s;
     for (int64_t k = k0 + lane; k < k0 + L.bs; k += 32) {
         int code = 0;
         if (k < L.K && amax > 0.f) {
             const float r = roundf(__fdiv_rn(load_f32(x, m * L.K + k, dt), s));  // half away from zero
             code = (int)fminf(fmaxf(r, -127.f), 127.f);
         }
-        if (xq) {
-            uint32_t t;  // code * s_a, rounded to tf32 (nearest, ties away)
-            asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(t) : "f"(__fmul_rn((float)code, s)));
-            xq[m * L.Kpad + k] = __uint_as_float(t);
-        } else {
-            qa[m * L.Kpad + k] = (int8_t)code;
-        }
+        qa[m * L.Kpad + k] = (int8_t)code;
     }
+}
+
+// The same quantisation for the prefill GEMM, 8 consecutive depths per lane
+// (one 16-byte load of bf16 / f16 X where the row allows it), a block's
+// bs / 8 lanes reducing its |x| max with shuffles: xq[m, k] = code * s_a
+// rounded to tf32 (f32 containers, rows Kpad long, zero past K), the
+// activation the GEMM's tf32 MMA multiplies.  Codes and scales are those of
+// quant_act_kernel (same operations on the same values).
+__global__ void __launch_bounds__(256) quant_act_tf32_kernel(const void* x, int dt, float* xq, int64_t M, Layout L,
+                                                             int64_t lanes_per_row) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int64_t gl = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // global lane
+    const int64_t m = gl / lanes_per_row;
+    const int64_t k0 = (gl - m * lanes_per_row) * 8;
+    const bool live = m < M && k0 < L.Kpad;  // lanes past the row still join the shuffles
+    float v[8];
+    const int64_t xrow = m * L.K;
+    if (live && dt != kF32 && k0 + 8 <= L.K && (L.K & 7) == 0 &&
+        (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + xrow + k0));
+        const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (dt == kBF16) {
+                v[2 * j] = __uint_as_float(wv[j] << 16);
+                v[2 * j + 1] = __uint_as_float(wv[j] & 0xFFFF0000u);
+            } else {
+                v[2 * j] = __half2float(__ushort_as_half((unsigned short)(wv[j] & 0xFFFFu)));
+                v[2 * j + 1] = __half2float(__ushort_as_half((unsigned short)(wv[j] >> 16)));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = (live && k0 + j < L.K) ? load_f32(x, xrow + k0 + j, dt) : 0.f;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+    // the block's lanes are aligned groups of bs / 8 (2 .. 32) lanes
+    for (int o = 1; o < L.bs / 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if (!live) return;
+    const float s = __fdiv_rn(amax, 127.0f);
+    float out[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        int code = 0;
+        if (k0 + j < L.K && amax > 0.f) {
+            const float r = roundf(__fdiv_rn(v[j], s));  // half away from zero
+            code = (int)fminf(fmaxf(r, -127.f), 127.f);
+        }
+        uint32_t t;  // code * s_a, rounded to tf32 (nearest, ties away)
+        asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(t) : "f"(__fmul_rn((float)code, s)));
+        out[j] = __uint_as_float(t);
+    }
+    float4* dst = reinterpret_cast<float4*>(xq + m * L.Kpad + k0);  // Kpad % 8 == 0, workspace 256-B aligned
+    dst[0] = make_float4(out[0], out[1], out[2], out[3]);
+    dst[1] = make_float4(out[4], out[5], out[6], out[7]);
 }
 
 }  // namespace gi8
@@ -64,10 +115,12 @@ bool gemv_i8_supported(const MatmulParams& p) {
     return g.total_bytes <= device_info().smem_optin && p.L.NT * g.C <= 0x7FFFFFFF;
 }
 
+// xq == nullptr: int8 codes and scales (warp per block); else tf32 activations (thread per block).
 static cudaError_t quant_launch(const void* x, int act_dtype, int8_t* qa, float* xq, float* sa, int64_t M,
                                 const Layout& L, bool pdl, cudaStream_t s) {
-    const int64_t warps = M * L.KB;
-    const int64_t blocks = (warps + 7) / 8;
+    // tf32: lanes of 8 depths, a row rounded up to whole warps (a block's lanes never straddle rows)
+    const int64_t lanes_per_row = (L.Kpad / 8 + 31) / 32 * 32;
+    const int64_t blocks = xq ? (M * lanes_per_row + 255) / 256 : (M * L.KB + 7) / 8;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
@@ -79,7 +132,8 @@ static cudaError_t quant_launch(const void* x, int act_dtype, int8_t* qa, float*
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gi8::quant_act_kernel, x, act_dtype, qa, xq, sa, M, L);
+    if (xq) return cudaLaunchKernelEx(&cfg, gi8::quant_act_tf32_kernel, x, act_dtype, xq, M, L, lanes_per_row);
+    return cudaLaunchKernelEx(&cfg, gi8::quant_act_kernel, x, act_dtype, qa, sa, M, L);
 }
 
 cudaError_t launch_quant_act(const void* x, int act_dtype, int8_t* qa, float* sa, int64_t M, const Layout& L,
