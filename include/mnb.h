@@ -158,9 +158,11 @@ MNB_API mnb_status mnb_matmul(const void* x, const void* packed_b, const void* s
  *                  int8 (scale = max|x|/127, round half away from zero), exact
  *                  integer block dot, then one f32 rescale by
  *                  f32(scale * s_a) (fn quantize_activation_signed, fn int8_row,
- *                  int8_matmul_amx).  M <= 16 runs the int8 GEMV; larger M the
- *                  tensor-core GEMM over the codes widened to bf16 (each block's
- *                  dot stays an exact integer in its f32 partial).  Needs workspace.
+ *                  int8_matmul_amx).  M <= 16 runs the int8 GEMV (exact integer
+ *                  block dots); larger M the tensor-core GEMM in tf32 over the
+ *                  quantised activations code * s_a and the weights (q - zp) *
+ *                  scale, each rounded to tf32 (relative error <= 2^-11 per
+ *                  operand, inside the per-element bound).  Needs workspace.
  *   workspace      device scratch of at least mnb_workspace_size() bytes
  *                  (256-byte aligned) or NULL when that size is 0.
  *   kernel         MNB_KERNEL_AUTO or a forced family.
@@ -344,9 +346,11 @@ MNB_API mnb_status mnb_matmul_fp(const void* x, const void* packed, const void* 
  *   MNB_TC_KERNEL=bs       prefill GEMM for bf16 X with per-block partial sums
  *                          instead of the hi/lo weight split
  *   MNB_TC_BT=32|64|128    token tile of the block-scaled prefill GEMM
- *   MNB_TC_SPLITK=0|1      K split over a 2-CTA cluster in the hi/lo GEMM
+ *   MNB_TC_SPLITK=1|2      K split over a 2-CTA cluster in the hi/lo GEMM
+ *                          (1: never, 2: always)
  *   MNB_WAIT_MODE=0|1|2    bounded mbarrier waits: suspend with a time hint,
- *                          try_wait without a hint, or test_wait polling
+ *                          try_wait without a hint (the default), or
+ *                          test_wait polling
  *   MNB_WAIT_LIMIT=n       test hook: n tries per bounded wait (then
  *                          MNB_ERR_TIMEOUT in the status word)
  *   MNB_GEMV_STAGE_BUFS, MNB_GEMV_MAX_SLOTS  ring shape of the f32 GEMV
