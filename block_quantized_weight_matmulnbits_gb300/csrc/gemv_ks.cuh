@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     const Layout& L = p.L;
     extern __shared__ __align__(128) uint8_t smem[];
     uint4* xs = reinterpret_cast<uint4*>(smem);                  // [M + 1][xrow]: row M is zeros
-    float* red = reinterpret_cast<float*>(smem + geo.x_bytes);   // [max_rt][kW][16][M]
+    float* red = reinterpret_cast<float*>(smem + geo.x_bytes);   // [max_rt][kW][M][16 rows]
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -316,12 +316,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
         // (x[k0 + 2tt..], x[k0 + 8 + 2tt..], x[k0 + 16 + 2tt..], x[k0 + 24 + 2tt..])
         const uint32_t* x32 = static_cast<const uint32_t*>(p.x);  // K even: rows are 4-byte aligned
         const int64_t kw = L.K / 2;
-        for (int m = 0; m < M; ++m) {
-            for (int r = tid; r < pairs * 4; r += kThreads) {
-                const int P = r >> 2, tt = r & 3;
-                const uint32_t* src = x32 + m * kw + P * 16 + tt;
-                xs[(size_t)m * geo.xrow + r] = make_uint4(__ldg(src), __ldg(src + 4), __ldg(src + 8), __ldg(src + 12));
+        // every row's words of a thread are requested before any is stored, so
+        // the M rows cost one round trip, not M
+        for (int r0 = 0; r0 < pairs * 4; r0 += kThreads) {
+            const int r = r0 + tid;
+            const int P = r >> 2, tt = r & 3;
+            uint4 v[M1 ? 1 : 8];
+#pragma unroll
+            for (int m = 0; m < (M1 ? 1 : 8); ++m) {
+                if (m < M && r < pairs * 4) {
+                    const uint32_t* src = x32 + m * kw + P * 16 + tt;
+                    v[m] = make_uint4(__ldg(src), __ldg(src + 4), __ldg(src + 8), __ldg(src + 12));
+                }
             }
+#pragma unroll
+            for (int m = 0; m < (M1 ? 1 : 8); ++m)
+                if (m < M && r < pairs * 4) xs[(size_t)m * geo.xrow + r] = v[m];
         }
     }
     load(buf[1], nxt);
@@ -334,12 +344,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
         float* r = red + (size_t)(rt_l * kW + warp) * 16 * M;
         const int m0 = 2 * t, m1 = 2 * t + 1;
         if (m0 < M) {
-            r[g * M + m0] = y[0];
-            r[(g + 8) * M + m0] = y[2];
+            r[m0 * 16 + g] = y[0];
+            r[m0 * 16 + g + 8] = y[2];
         }
         if (!M1 && m1 < M) {
-            r[g * M + m1] = y[1];
-            r[(g + 8) * M + m1] = y[3];
+            r[m1 * 16 + g] = y[1];
+            r[m1 * 16 + g + 8] = y[3];
         }
         y[0] = y[1] = y[2] = y[3] = 0.f;
     };
@@ -361,13 +371,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     __syncthreads();
 
     // ---- 4. rows: the 16 warps' partials in a fixed order ----
+    // consecutive threads take consecutive rows of one token (coalesced stores,
+    // conflict-free reads); q = rt_l * M + m is split with a float reciprocal
+    // (q < 2^16: exact after truncation of (q + 0.5) / M)
+    const float inv_m = M1 ? 1.f : 1.f / (float)M;
     for (int o = tid; o < nrt * 16 * M; o += kThreads) {
-        const int rt_l = o / (16 * M), rem = o - rt_l * 16 * M;
-        const int row = rem / M, m = rem - row * M;
-        const float* src = red + (size_t)rt_l * kW * 16 * M + row * M + m;
-        float v = 0.f;
+        const int row = o & 15, q = o >> 4;
+        const int rt_l = M1 ? q : __float2int_rz(((float)q + 0.5f) * inv_m);
+        const int m = M1 ? 0 : q - rt_l * M;
+        const float* src = red + (size_t)rt_l * kW * 16 * M + m * 16 + row;
+        // the 16 warps' partials as a fixed pairwise tree (independent loads, depth 4)
+        float t8[kW / 2];
 #pragma unroll
-        for (int w2 = 0; w2 < kW; ++w2) v += src[(size_t)w2 * 16 * M];
+        for (int w2 = 0; w2 < kW / 2; ++w2) t8[w2] = src[(size_t)(2 * w2) * 16 * M] + src[(size_t)(2 * w2 + 1) * 16 * M];
+#pragma unroll
+        for (int h = kW / 4; h >= 1; h >>= 1) {
+#pragma unroll
+            for (int w2 = 0; w2 < h; ++w2) t8[w2] = t8[2 * w2] + t8[2 * w2 + 1];
+        }
+        float v = t8[0];
         const int64_t n = (rt0 + rt_l) * 16 + row;
         if (n < L.N) {
             if (p.bias) v += load_f32(p.bias, n, p.bias_dtype);
