@@ -63,8 +63,11 @@ constexpr int kKK = 16 / kDqWarps;  // k-steps a dequant warp writes per stage
 constexpr int kThreads = (kCtlWarps + kDqWarps) * 32;
 constexpr int kR = 4;            // ring depth (shared-memory stages and TMEM A slots)
 constexpr int kXStage = kBT * kBK * 2;  // 32 KB
+// mbarriers, tensor-memory address and abort flag
+__host__ __device__ constexpr size_t hl_bar_bytes(int r) { return (3 * r + 1) * 8 + 16; }
 
 struct Geom {
+    int ystore;         // 1: Y written by TMA from a shared-memory stage (Maps::y valid)
     int n_tiles, m_tiles;
     int splitk;         // 1, or 2: the two CTAs of a cluster take halves of K
     int k_stages;       // stages of the whole K (ceil(Kpad / 64))
@@ -72,7 +75,7 @@ struct Geom {
 };
 
 struct Maps {
-    CUtensorMap x, w;
+    CUtensorMap x, w, y;
 };
 
 __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
@@ -98,7 +101,8 @@ __device__ __forceinline__ void split_scale(float s, uint32_t* hi2, uint32_t* lo
 template <int BITS, bool TF32>
 __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Geom geo,
                                                                const __grid_constant__ CUtensorMap xmap,
-                                                               const __grid_constant__ CUtensorMap wmap) {
+                                                               const __grid_constant__ CUtensorMap wmap,
+                                                               const __grid_constant__ CUtensorMap ymap) {
     constexpr int KT = 256 / BITS;                  // depths per packed tile
     constexpr int TILES = kBK >= KT ? kBK / KT : 1;  // packed tiles per 16-row tile per stage
     constexpr uint32_t kMag = 0x43004300u;           // bf16 128.0 in both halves
@@ -411,6 +415,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
         bool fine = ok && !*abort_v && tc::wait_bounded(done, 0, p.status, wl, wh);
         tc::fence_after();
         const float bias = (p.bias && row_ok) ? load_f32(p.bias, n, p.bias_dtype) : 0.f;
+        // Y: this CTA's tokens [tok0, tok0 + T) of its 128 rows, staged in the idle X ring as
+        // [128-byte row chunk][token][row] and written by TMA (out-of-range rows and tokens are
+        // clipped), or stored element by element
+        const int T = geo.splitk == 2 ? kBT / 2 : BT;
+        const int64_t tok0 = m0 + (geo.splitk == 2 ? (int64_t)(kBT / 2) * rank : 0);
+        const int es = p.out_dtype == kF32 ? 4 : 2;
+        const int rowc = 128 / es;
+        uint8_t* ystage = smem + (geo.splitk == 2 ? 65536 : 0);  // past the split-K exchange buffer
+        auto put = [&](int t, float v) {
+            if (geo.ystore) {
+                uint8_t* d = ystage + (size_t)(r / rowc) * (size_t)(T * 128) + (size_t)t * 128 + (size_t)(r % rowc) * es;
+                if (es == 4) {
+                    *reinterpret_cast<float*>(d) = v;
+                } else if (p.out_dtype == kF16) {
+                    *reinterpret_cast<__half*>(d) = __float2half_rn(v);
+                } else {
+                    *reinterpret_cast<__nv_bfloat16*>(d) = __float2bfloat16_rn(v);
+                }
+            } else {
+                const int64_t m = tok0 + t;
+                if (row_ok && m < p.M) store_f32(p.y, m * L.N + n, v, p.out_dtype);
+            }
+        };
         if (geo.splitk == 1) {
             // columns kEpi jh .. kEpi jh + kEpi - 1 of this thread's row
             constexpr int kEpi = BT / (kDqWarps / 4);
@@ -418,13 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
                 uint32_t v[32];
                 tc::ld_32x32b<32>(tmem + (uint32_t)c0 + lane_addr, v);
                 tc::wait_ld();
-                if (row_ok) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int64_t m = m0 + c0 + j;
-                        if (m < p.M) store_f32(p.y, m * L.N + n, __uint_as_float(v[j]) + bias, p.out_dtype);
-                    }
-                }
+                for (int j = 0; j < 32; ++j) put(c0 + j, __uint_as_float(v[j]) + bias);
             }
         } else {
             // rank r outputs tokens 128 r .. 128 r + 127; it hands the partner its half
@@ -463,13 +485,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
                         const float ov[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int64_t m = m0 + c0 + j + e;
                             // D_rank0 + D_rank1 in either CTA (f32 addition of two terms commutes)
-                            const float yv = __uint_as_float(v[j + e]) + ov[e];
-                            if (row_ok && m < p.M) store_f32(p.y, m * L.N + n, yv + bias, p.out_dtype);
+                            put(c0 - mine + j + e, __uint_as_float(v[j + e]) + ov[e] + bias);
                         }
                     }
                 }
+            }
+        }
+        if (geo.ystore) {
+            fence_proxy_async_smem();  // the stage's generic writes, before the TMA reads them
+            asm volatile("bar.sync 1, %0;" ::"n"(kDqWarps * 32) : "memory");
+            if (warp == kCtlWarps && lane == 0 && fine) {
+                for (int c = 0; c < 128 / rowc; ++c)
+                    tc::tma_store_2d(&ymap, ystage + (size_t)c * (size_t)(T * 128), (int)(n0 + c * rowc), (int)tok0);
+                tc::bulk_commit();
+                tc::bulk_wait_read0();
             }
         }
     }
@@ -505,7 +535,7 @@ cudaError_t launch(const MatmulParams& p, const Geom& geo, const Maps& m, cudaSt
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, p, geo, m.x, m.w);
+    return cudaLaunchKernelEx(&cfg, kern, p, geo, m.x, m.w, m.y);
 }
 
 }  // namespace ghl

@@ -141,7 +141,7 @@ ghl::Geom make_geom_hl(const MatmulParams& p, bool tf32 = false) {
     g.wp_stage = (size_t)(ghl::kRows / 16) * tiles_per_stage * kTileBytes;
     const int R = tf32 ? 3 : ghl::kR;
     const size_t xst = tf32 ? 2 * (size_t)ghl::kXStage : (size_t)ghl::kXStage;
-    g.total_bytes = 1024 + R * (xst + g.wp_stage) + (3 * R + 1) * 8 + 16;
+    g.total_bytes = 1024 + R * (xst + g.wp_stage) + ghl::hl_bar_bytes(R);
     return g;
 }
 
@@ -158,10 +158,28 @@ CUresult hl_wmap(const MatmulParams& p, EncodeTiledFn enc, CUtensorMap* w) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// Y for the TMA store of the hi/lo and tf32 kernels: [M][N] of out_dtype, boxes of
+// 128 bytes of rows x the CTA's tokens (256, or 128 with a K split).  False
+// (element stores instead) when Y's base or row stride is not 16-byte aligned.
+bool hl_ymap(const MatmulParams& p, const ghl::Geom& geo, EncodeTiledFn enc, CUtensorMap* y) {
+    const int es = p.out_dtype == kF32 ? 4 : 2;
+    if ((reinterpret_cast<uintptr_t>(p.y) & 15) != 0 || (p.L.N * es) % 16 != 0) return false;
+    const CUtensorMapDataType dt = p.out_dtype == kF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : p.out_dtype == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint64_t dims[2] = {(cuuint64_t)p.L.N, (cuuint64_t)p.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.L.N * es};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)(geo.splitk == 2 ? ghl::kBT / 2 : ghl::kBT)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(y, dt, 2, p.y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_hl(const MatmulParams& p, EncodeTiledFn enc, cudaStream_t s) {
-    const ghl::Geom geo = make_geom_hl(p);
+    ghl::Geom geo = make_geom_hl(p);
     ghl::Maps m;
     std::memset(&m, 0, sizeof(m));
+    geo.ystore = hl_ymap(p, geo, enc, &m.y) ? 1 : 0;
     const cuuint32_t estr[2] = {1, 1};
     const cuuint64_t dims[2] = {(cuuint64_t)p.L.K, (cuuint64_t)p.M};
     const cuuint64_t strides[1] = {(cuuint64_t)p.L.K * 2};
@@ -233,9 +251,10 @@ cudaError_t launch_gemm_a8(const MatmulParams& p, cudaStream_t s) {
     MatmulParams q = p;
     q.x = xq;
     q.act_dtype = kF32;
-    const ghl::Geom geo = make_geom_hl(q, true);
+    ghl::Geom geo = make_geom_hl(q, true);
     ghl::Maps m;
     std::memset(&m, 0, sizeof(m));
+    geo.ystore = hl_ymap(q, geo, enc, &m.y) ? 1 : 0;
     const cuuint32_t estr[2] = {1, 1};
     const cuuint64_t dims[2] = {(cuuint64_t)p.L.Kpad, (cuuint64_t)p.M};
     const cuuint64_t strides[1] = {(cuuint64_t)p.L.Kpad * 4};
