@@ -373,14 +373,14 @@ def run_ours(args):
             peak = pk["hbm_gbs"]
             out["roofline"] = {"bound": "hbm", "achieved": per_step / per_launch_s, "peak": peak, "unit": "GB/s",
                                "frac": per_step / per_launch_s / peak,
-                               "traffic": traffic_for(f"{chosen}:{w.name}"),
+                               "traffic": traffic_for(f"{chosen}:{w.name}" + (":acc4" if acc == 4 else "")),
                                "algorithmic_bytes": w.algorithmic_bytes(),
                                "peak_source": f"{pk_src} hbm_gbs"}
         else:
             peak = pk["bf16_tflops"]
             out["roofline"] = {"bound": "tensor", "achieved": per_step / per_launch_s, "peak": peak,
                                "unit": "TFLOP/s", "frac": per_step / per_launch_s / peak,
-                               "traffic": traffic_for(f"{chosen}:{w.name}"),
+                               "traffic": traffic_for(f"{chosen}:{w.name}" + (":acc4" if acc == 4 else "")),
                                "algorithmic_bytes": w.algorithmic_bytes(), "flops": w.flops(),
                                "peak_source": f"{pk_src} bf16_tflops (burst)"}
         if want_e2e:
