@@ -439,10 +439,10 @@ def run_ours(args):
         per_launch_s = t / steps
         achieved = per_step / per_launch_s
         return {"workload": w.name, "value": whole_job_value(world, steps, per_step, t), "unit": "GB/s",
-                "kernel": "gemv_moe", "ms_per_step": per_launch_s * 1e3, "steps": steps,
+                "kernel": "gemv_ks (grouped: pairs <= 8)", "ms_per_step": per_launch_s * 1e3, "steps": steps,
                 "experts_active": int(len(np.unique(d["ids"]))), "experts": w.E, "tokens": w.T, "top_k": w.S,
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                             "frac": achieved / pk["hbm_gbs"], "traffic": traffic_for(f"gemv_moe:{w.name}"),
+                             "frac": achieved / pk["hbm_gbs"], "traffic": traffic_for(f"gemv_ks_moe:{w.name}"),
                              "algorithmic_bytes": step_bytes, "peak_source": f"{pk_src} hbm_gbs"},
                 "clocks": ck, "weight_copies": R}, steps
 

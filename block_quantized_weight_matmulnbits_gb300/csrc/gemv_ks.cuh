@@ -244,6 +244,19 @@ struct Item {
 };
 
 // Position of a warp in its CTA's item list.
+// Grouped (mixture-of-experts) calls with at most 8 (token, slot) pairs: grid
+// row y runs the schedule on the y-th smallest expert id present in ids, over
+// that expert's pairs (ascending token-then-slot order, one MMA column each).
+// This is ggml's MUL_MAT_ID grouping as the SpacemiT backend computes it (toy
+// 0.8.0, data/vendor/ggml/src/ggml-cpu/spacemit/ime.cpp, forward_mul_mat_id).
+constexpr int kMoeMaxPairs = 8;
+struct MoeKs {
+    const int32_t* ids;        // [T, S] expert of each (token, slot); nullptr: a plain call
+    int pairs, S, E, x_per_slot;
+    size_t expert_bytes;       // packed bytes per expert (header included)
+    size_t expert_scale_bytes, expert_zp_bytes;
+};
+
 // Position of a warp in its CTA's item list: item i = (local row tile rt,
 // chunk c); a step of kW items moves q16 row tiles and r16 chunks.
 struct Cursor {
@@ -259,8 +272,8 @@ struct Cursor {
     }
 };
 
-template <int BITS, bool BF16X, int SPB_LOG, int SDT, bool M1>
-__global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KGeom geo, int pdl) {
+template <int BITS, bool BF16X, int SPB_LOG, int SDT, bool M1, bool MOE>
+__global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KGeom geo, int pdl, MoeKs moe) {
     using It = Item<BITS, BF16X, SPB_LOG, SDT>;
     constexpr int CH = It::CH;
     const Layout& L = p.L;
@@ -271,7 +284,54 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int M = M1 ? 1 : (int)p.M;
+    int M = M1 ? 1 : (int)p.M;
+    // grouped call: this grid row's expert, its pairs (registers) and their Y rows (shared)
+    int pl[MOE ? kMoeMaxPairs : 1] = {};
+    __shared__ int moe_yrow[MOE ? kMoeMaxPairs : 1];
+    if constexpr (MOE) {
+        int id[kMoeMaxPairs];
+#pragma unroll
+        for (int q = 0; q < kMoeMaxPairs; ++q) id[q] = q < moe.pairs ? __ldg(moe.ids + q) : -1;
+        // the expert whose rank among the distinct valid ids is blockIdx.y
+        bool valid[kMoeMaxPairs], first[kMoeMaxPairs];
+        bool bad = false;
+#pragma unroll
+        for (int q = 0; q < kMoeMaxPairs; ++q) {
+            valid[q] = q < moe.pairs && id[q] >= 0 && id[q] < moe.E;
+            bad = bad || (q < moe.pairs && !valid[q]);
+            first[q] = valid[q];
+#pragma unroll
+            for (int q2 = 0; q2 < q; ++q2)
+                if (id[q2] == id[q]) first[q] = false;
+        }
+        int e = -1;
+#pragma unroll
+        for (int q = 0; q < kMoeMaxPairs; ++q) {
+            int rank = 0;  // distinct valid ids below id[q]
+#pragma unroll
+            for (int q2 = 0; q2 < kMoeMaxPairs; ++q2)
+                if (first[q2] && id[q2] < id[q]) ++rank;
+            if (first[q] && rank == (int)blockIdx.y) e = id[q];
+        }
+        if (bad && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) set_status(p.status, 1 /* MNB_ERR_INVALID_ARG */);
+        if (e < 0) return;  // fewer distinct experts than grid rows (every thread agrees)
+        M = 0;  // the expert's pairs in ascending order (static indices: pl stays in registers)
+#pragma unroll
+        for (int q = 0; q < kMoeMaxPairs; ++q) {
+            const bool hit = q < moe.pairs && id[q] == e;
+#pragma unroll
+            for (int m = 0; m < kMoeMaxPairs; ++m)
+                if (hit && m == M) pl[m] = q;
+            M += hit ? 1 : 0;
+        }
+#pragma unroll
+        for (int m = 0; m < kMoeMaxPairs; ++m)
+            if (tid == m && m < M) moe_yrow[m] = pl[m];
+        p.packed += (size_t)e * moe.expert_bytes;
+        p.packed_hdr = static_cast<const uint8_t*>(p.packed_hdr) + (size_t)e * moe.expert_bytes;
+        p.scales = static_cast<const uint8_t*>(p.scales) + (size_t)e * moe.expert_scale_bytes;
+        if (p.zp) p.zp += (size_t)e * moe.expert_zp_bytes;
+    }
     const int KC = geo.KC;
     const uint32_t NT32 = (uint32_t)L.NT;
     const int64_t rt0 = (int64_t)(blockIdx.x * NT32 / (uint32_t)geo.G);
@@ -325,7 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
 #pragma unroll
             for (int m = 0; m < (M1 ? 1 : 8); ++m) {
                 if (m < M && r < pairs * 4) {
-                    const uint32_t* src = x32 + m * kw + P * 16 + tt;
+                    // grouped call: column m is pair pl[m] = t * S + s, row t of X (or row t * S + s)
+                    const int xr = MOE ? (moe.x_per_slot ? pl[MOE ? m : 0] : pl[MOE ? m : 0] / moe.S) : m;
+                    const uint32_t* src = x32 + (int64_t)xr * kw + P * 16 + tt;
                     v[m] = make_uint4(__ldg(src), __ldg(src + 4), __ldg(src + 8), __ldg(src + 12));
                 }
             }
@@ -393,20 +455,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
         const int64_t n = (rt0 + rt_l) * 16 + row;
         if (n < L.N) {
             if (p.bias) v += load_f32(p.bias, n, p.bias_dtype);
-            store_f32(p.y, (int64_t)m * L.N + n, v, p.out_dtype);
+            store_f32(p.y, (int64_t)(MOE ? moe_yrow[MOE ? m : 0] : m) * L.N + n, v, p.out_dtype);
         }
     }
     if (blockIdx.x == 0 && tid == 0) verify_header(p.packed_hdr, L, p.status);
 }
 
 template <int BITS, bool BF16X, int SPB_LOG, int SDT>
-cudaError_t launch_k(const MatmulParams& p, const KGeom& geo, cudaStream_t s) {
+cudaError_t launch_k(const MatmulParams& p, const KGeom& geo, cudaStream_t s, const MoeKs* moe) {
     const int pdl = (p.flags & kFlagPDL) ? 1 : 0;
-    auto kern = p.M == 1 ? gemv_ks_kernel<BITS, BF16X, SPB_LOG, SDT, true> : gemv_ks_kernel<BITS, BF16X, SPB_LOG, SDT, false>;
+    auto kern = moe ? gemv_ks_kernel<BITS, BF16X, SPB_LOG, SDT, false, true>
+                : p.M == 1 ? gemv_ks_kernel<BITS, BF16X, SPB_LOG, SDT, true, false>
+                           : gemv_ks_kernel<BITS, BF16X, SPB_LOG, SDT, false, false>;
+    const MoeKs none{};
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.total_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)geo.G);
+    // grouped: one grid row per expert that can be present (at most min(pairs, E))
+    cfg.gridDim = dim3((unsigned)geo.G, moe ? (unsigned)(moe->pairs < moe->E ? moe->pairs : moe->E) : 1u);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = geo.total_bytes;
     cfg.stream = s;
@@ -415,35 +481,35 @@ cudaError_t launch_k(const MatmulParams& p, const KGeom& geo, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, p, geo, pdl);
+    return cudaLaunchKernelEx(&cfg, kern, p, geo, pdl, moe ? *moe : none);
 }
 
 template <int BITS, bool BF16X, int SPB_LOG>
-cudaError_t launch_sdt(const MatmulParams& p, const KGeom& geo, cudaStream_t s) {
+cudaError_t launch_sdt(const MatmulParams& p, const KGeom& geo, cudaStream_t s, const MoeKs* moe) {
     constexpr int BPC = chunk_steps(BITS) >> SPB_LOG;
     switch (p.scale_dtype) {
         case kF32:
-            if constexpr (BPC * 4 <= 32) return launch_k<BITS, BF16X, SPB_LOG, kF32>(p, geo, s);
+            if constexpr (BPC * 4 <= 32) return launch_k<BITS, BF16X, SPB_LOG, kF32>(p, geo, s, moe);
             break;
-        case kF16: return launch_k<BITS, BF16X, SPB_LOG, kF16>(p, geo, s);
-        case kBF16: return launch_k<BITS, BF16X, SPB_LOG, kBF16>(p, geo, s);
+        case kF16: return launch_k<BITS, BF16X, SPB_LOG, kF16>(p, geo, s, moe);
+        case kBF16: return launch_k<BITS, BF16X, SPB_LOG, kBF16>(p, geo, s, moe);
         default: break;
     }
     return cudaErrorNotSupported;
 }
 
 template <int BITS, bool BF16X>
-cudaError_t launch_bs(const MatmulParams& p, const KGeom& geo, cudaStream_t s) {
+cudaError_t launch_bs(const MatmulParams& p, const KGeom& geo, cudaStream_t s, const MoeKs* moe) {
     constexpr int CH = chunk_steps(BITS);
     switch (p.L.bs) {
         case 16:
-            if constexpr (CH <= 16) return launch_sdt<BITS, BF16X, 0>(p, geo, s);
+            if constexpr (CH <= 16) return launch_sdt<BITS, BF16X, 0>(p, geo, s, moe);
             break;
-        case 32: return launch_sdt<BITS, BF16X, 1>(p, geo, s);
-        case 64: return launch_sdt<BITS, BF16X, 2>(p, geo, s);
-        case 128: return launch_sdt<BITS, BF16X, 3>(p, geo, s);
+        case 32: return launch_sdt<BITS, BF16X, 1>(p, geo, s, moe);
+        case 64: return launch_sdt<BITS, BF16X, 2>(p, geo, s, moe);
+        case 128: return launch_sdt<BITS, BF16X, 3>(p, geo, s, moe);
         case 256:
-            if constexpr (CH >= 16) return launch_sdt<BITS, BF16X, 4>(p, geo, s);
+            if constexpr (CH >= 16) return launch_sdt<BITS, BF16X, 4>(p, geo, s, moe);
             break;
         default: break;
     }
@@ -451,8 +517,8 @@ cudaError_t launch_bs(const MatmulParams& p, const KGeom& geo, cudaStream_t s) {
 }
 
 template <int BITS>
-cudaError_t launch_bits(const MatmulParams& p, const KGeom& geo, cudaStream_t s) {
-    return p.act_dtype == kBF16 ? launch_bs<BITS, true>(p, geo, s) : launch_bs<BITS, false>(p, geo, s);
+cudaError_t launch_bits(const MatmulParams& p, const KGeom& geo, cudaStream_t s, const MoeKs* moe = nullptr) {
+    return p.act_dtype == kBF16 ? launch_bs<BITS, true>(p, geo, s, moe) : launch_bs<BITS, false>(p, geo, s, moe);
 }
 
 }  // namespace gks

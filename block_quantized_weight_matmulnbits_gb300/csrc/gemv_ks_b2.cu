@@ -2,7 +2,8 @@
 #include "gemv_ks.cuh"
 
 namespace mnb {
-cudaError_t launch_gemv_ks_b2(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s) {
-    return gks::launch_bits<2>(p, geo, s);
+cudaError_t launch_gemv_ks_b2(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s,
+                             const gks::MoeKs* moe) {
+    return gks::launch_bits<2>(p, geo, s, moe);
 }
 }  // namespace mnb

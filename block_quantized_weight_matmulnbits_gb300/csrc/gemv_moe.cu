@@ -1,7 +1,9 @@
 // Host side of the grouped (mixture-of-experts) GEMV (kernel in gemv_moe.cuh):
 // validation, geometry and the C entry point mnb_matmul_grouped.
 #include <cstdlib>
+#include <cstring>
 
+#include "gemv_ks.cuh"
 #include "gemv_moe.cuh"
 #include "mnb.h"
 
@@ -13,6 +15,9 @@ cudaError_t launch_gemv_moe_b4(const MatmulParams& p, const gmma::Geom& geo, con
                                unsigned groups, size_t smem_bytes, cudaStream_t s);
 cudaError_t launch_gemv_moe_b8(const MatmulParams& p, const gmma::Geom& geo, const gmoe::MoeArgs& g,
                                unsigned groups, size_t smem_bytes, cudaStream_t s);
+cudaError_t launch_gemv_ks_b2(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe);
+cudaError_t launch_gemv_ks_b4(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe);
+cudaError_t launch_gemv_ks_b8(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe);
 
 }  // namespace mnb
 
@@ -50,6 +55,56 @@ mnb_status mnb_matmul_grouped(const void* x, const int32_t* ids, const void* pac
         return MNB_ERR_UNSUPPORTED;  // (T and S bounded first: T * S cannot overflow)
     const int pairs = (int)(T * S);
     const int MT = pairs <= 8 ? 8 : 16;
+
+    // Decode-sized calls (at most 8 pairs) run the K-chunk schedule, one grid row per expert
+    // present (MNB_MOE_SCHED=tile keeps the per-tile kernel below)
+    const char* sched = std::getenv("MNB_MOE_SCHED");
+    if (pairs <= gks::kMoeMaxPairs && !(sched && std::strcmp(sched, "tile") == 0)) {
+        MatmulParams q{};
+        q.x = x;
+        q.packed_hdr = packed_b;
+        q.packed = static_cast<const uint8_t*>(packed_b) + kHeaderBytes;
+        q.scales = scales;
+        q.zp = zero_points;
+        q.y = y;
+        q.M = pairs;
+        q.L.init(N, K, bits, block_size);
+        q.act_dtype = act_dtype;
+        q.out_dtype = out_dtype;
+        q.scale_dtype = scale_dtype;
+        q.bias_dtype = kF32;
+        q.status = device_status_word();
+        if (!q.status) return MNB_ERR_CUDA;
+        gks::MoeKs mk{};
+        mk.ids = ids;
+        mk.pairs = pairs;
+        mk.S = (int)S;
+        mk.E = (int)E;
+        mk.x_per_slot = x_per_slot;
+        mk.expert_bytes = expert_bytes;
+        mk.expert_scale_bytes = (size_t)N * (size_t)q.L.KB * dt_bytes(scale_dtype);
+        mk.expert_zp_bytes = (size_t)N * (size_t)q.L.zp_row;
+        const int sms = device_info().sm_count > 0 ? device_info().sm_count : 148;
+        gks::KGeom kg;
+        const bool fits = aligned_to(scales, 16) && mk.expert_scale_bytes % 16 == 0 &&
+                          (!zero_points || (aligned_to(zero_points, 16) && mk.expert_zp_bytes % 16 == 0)) &&
+                          gks::make_kgeom(q.L, pairs, sms, device_info().smem_optin, (int)dt_bytes(scale_dtype), &kg);
+        if (fits) {
+            if (inject_launch_failure()) return MNB_ERR_CUDA;
+            cudaStream_t st = (cudaStream_t)stream;
+            cudaError_t e;
+            switch (bits) {
+                case 2: e = launch_gemv_ks_b2(q, kg, st, &mk); break;
+                case 4: e = launch_gemv_ks_b4(q, kg, st, &mk); break;
+                case 8: e = launch_gemv_ks_b8(q, kg, st, &mk); break;
+                default: return MNB_ERR_INVALID_ARG;
+            }
+            if (e == cudaSuccess) return MNB_OK;
+            cudaGetLastError();
+            if (e != cudaErrorNotSupported) return MNB_ERR_CUDA;
+            // not instantiated for this block size / scale type (nothing launched): the per-tile kernel
+        }
+    }
 
     MatmulParams p{};
     p.x = x;
