@@ -244,11 +244,14 @@ struct Item {
 };
 
 // Position of a warp in its CTA's item list.
-// Grouped (mixture-of-experts) calls with at most 8 (token, slot) pairs: grid
-// row y runs the schedule on the y-th smallest expert id present in ids, over
-// that expert's pairs (ascending token-then-slot order, one MMA column each).
-// This is ggml's MUL_MAT_ID grouping as the SpacemiT backend computes it (toy
-// 0.8.0, data/vendor/ggml/src/ggml-cpu/spacemit/ime.cpp, forward_mul_mat_id).
+// Grouped (mixture-of-experts) calls with at most 8 (token, slot) pairs: the
+// experts present in ids, in ascending order, are laid end to end as one
+// matrix of n_active x NT row tiles, and the CTAs split that range as they
+// split a plain matrix.  Row tile R belongs to active expert R / NT; its MMA
+// columns are that expert's pairs (ascending token-then-slot order), the
+// other columns read a zero X row.  This is ggml's MUL_MAT_ID grouping as the
+// SpacemiT backend computes it (toy 0.8.0, data/vendor/ggml/src/ggml-cpu/
+// spacemit/ime.cpp, forward_mul_mat_id).
 constexpr int kMoeMaxPairs = 8;
 struct MoeKs {
     const int32_t* ids;        // [T, S] expert of each (token, slot); nullptr: a plain call
@@ -284,56 +287,63 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
-    int M = M1 ? 1 : (int)p.M;
-    // grouped call: this grid row's expert, its pairs (registers) and their Y rows (shared)
-    int pl[MOE ? kMoeMaxPairs : 1] = {};
-    __shared__ int moe_yrow[MOE ? kMoeMaxPairs : 1];
+    const int M = M1 ? 1 : (int)p.M;  // grouped: the pairs (every X row staged, one per pair)
+    const int KC = geo.KC;
+    uint32_t NT32 = (uint32_t)L.NT;
+    // grouped call: the active experts (ascending), each one's X row and Y row per MMA column
+    __shared__ int moe_ak[MOE ? kMoeMaxPairs : 1];                      // expert id of active index k
+    __shared__ int moe_col[MOE ? kMoeMaxPairs * 8 : 1];                 // [k][column g]: X row (M: zero row)
+    __shared__ int moe_yrow[MOE ? kMoeMaxPairs * kMoeMaxPairs : 1];     // [k][column m]: Y row, -1: none
+    int n_active = 1;
+    float inv_nt = 0.f;
     if constexpr (MOE) {
         int id[kMoeMaxPairs];
 #pragma unroll
         for (int q = 0; q < kMoeMaxPairs; ++q) id[q] = q < moe.pairs ? __ldg(moe.ids + q) : -1;
-        // the expert whose rank among the distinct valid ids is blockIdx.y
-        bool valid[kMoeMaxPairs], first[kMoeMaxPairs];
+        bool first[kMoeMaxPairs];
+        int rank[kMoeMaxPairs];
         bool bad = false;
+        n_active = 0;
 #pragma unroll
         for (int q = 0; q < kMoeMaxPairs; ++q) {
-            valid[q] = q < moe.pairs && id[q] >= 0 && id[q] < moe.E;
-            bad = bad || (q < moe.pairs && !valid[q]);
-            first[q] = valid[q];
+            const bool valid = q < moe.pairs && id[q] >= 0 && id[q] < moe.E;
+            bad = bad || (q < moe.pairs && !valid);
+            first[q] = valid;
 #pragma unroll
             for (int q2 = 0; q2 < q; ++q2)
                 if (id[q2] == id[q]) first[q] = false;
+            n_active += first[q] ? 1 : 0;
         }
-        int e = -1;
 #pragma unroll
         for (int q = 0; q < kMoeMaxPairs; ++q) {
-            int rank = 0;  // distinct valid ids below id[q]
+            rank[q] = 0;  // distinct valid ids below id[q]
 #pragma unroll
             for (int q2 = 0; q2 < kMoeMaxPairs; ++q2)
-                if (first[q2] && id[q2] < id[q]) ++rank;
-            if (first[q] && rank == (int)blockIdx.y) e = id[q];
+                if (first[q2] && id[q2] < id[q]) ++rank[q];
         }
-        if (bad && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) set_status(p.status, 1 /* MNB_ERR_INVALID_ARG */);
-        if (e < 0) return;  // fewer distinct experts than grid rows (every thread agrees)
-        M = 0;  // the expert's pairs in ascending order (static indices: pl stays in registers)
+        if (bad && blockIdx.x == 0 && tid == 0) set_status(p.status, 1 /* MNB_ERR_INVALID_ARG */);
+        if (tid < kMoeMaxPairs * 8) {  // entry (k, c) of the tables, c a column
+            const int k = tid >> 3, c = tid & 7;
+            int e = -1;
 #pragma unroll
-        for (int q = 0; q < kMoeMaxPairs; ++q) {
-            const bool hit = q < moe.pairs && id[q] == e;
+            for (int q = 0; q < kMoeMaxPairs; ++q)
+                if (first[q] && rank[q] == k) e = id[q];
+            int pos = 0, xr = M, yr = -1;  // the c-th pair of expert e
 #pragma unroll
-            for (int m = 0; m < kMoeMaxPairs; ++m)
-                if (hit && m == M) pl[m] = q;
-            M += hit ? 1 : 0;
+            for (int q = 0; q < kMoeMaxPairs; ++q) {
+                if (e >= 0 && q < moe.pairs && id[q] == e) {
+                    if (pos == c) xr = yr = q;
+                    ++pos;
+                }
+            }
+            if (c == 0) moe_ak[k] = e;
+            moe_col[k * 8 + c] = xr;
+            moe_yrow[k * kMoeMaxPairs + c] = yr;
         }
-#pragma unroll
-        for (int m = 0; m < kMoeMaxPairs; ++m)
-            if (tid == m && m < M) moe_yrow[m] = pl[m];
-        p.packed += (size_t)e * moe.expert_bytes;
-        p.packed_hdr = static_cast<const uint8_t*>(p.packed_hdr) + (size_t)e * moe.expert_bytes;
-        p.scales = static_cast<const uint8_t*>(p.scales) + (size_t)e * moe.expert_scale_bytes;
-        if (p.zp) p.zp += (size_t)e * moe.expert_zp_bytes;
+        inv_nt = 1.f / (float)NT32;
+        NT32 *= (uint32_t)n_active;  // the experts' row tiles end to end
+        __syncthreads();             // the tables, before the first item's loads read them
     }
-    const int KC = geo.KC;
-    const uint32_t NT32 = (uint32_t)L.NT;
     const int64_t rt0 = (int64_t)(blockIdx.x * NT32 / (uint32_t)geo.G);
     const int nrt = (int)((blockIdx.x + 1) * NT32 / (uint32_t)geo.G - (uint32_t)rt0);
     const int n_items = nrt * KC;
@@ -344,11 +354,43 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     const uint8_t* zb = p.zp != nullptr ? p.zp + (size_t)rt0 * 16 * zrow : nullptr;
     const uint32_t nlast = (uint32_t)(L.N - 1 - rt0 * 16);  // last row, local
     const int q16 = geo.q16, r16 = geo.r16;
+    // grouped: active expert k of a CTA-local row tile, and its row tile within the expert
+    auto expert_of = [&](int rt_l, int* rt_e) -> int {
+        const int R = (int)rt0 + rt_l;
+        const int k = __float2int_rz(((float)R + 0.5f) * inv_nt);  // R < 2^24: exact
+        *rt_e = R - k * (int)L.NT;
+        return k;
+    };
+    // grouped: warp w takes whole row tiles w, w + kW, ... (every chunk in order), so a row's
+    // sum stays in one warp's registers and is stored when the row tile ends
+    auto valid = [&](const Cursor& it) { return MOE ? it.rt < nrt : it.i < n_items; };
+    auto advance = [&](Cursor& it) {
+        if constexpr (MOE) {
+            if (++it.c == KC) {
+                it.c = 0;
+                it.rt += kW;
+            }
+        } else {
+            it.advance(KC, q16, r16);
+        }
+    };
     auto load = [&](It& b, const Cursor& it) {
-        if (it.i < n_items) {
-            const uint32_t nl = (uint32_t)it.rt * 16u + (uint32_t)g;
-            const uint32_t r0 = min(nl, nlast), r8 = min(nl + 8u, nlast);
-            b.load(wbase + (uint32_t)it.i * (uint32_t)kItemBytes, sb, zb, srow, zrow, r0, r8, (uint32_t)it.c);
+        if (valid(it)) {
+            if constexpr (MOE) {
+                int rt_e;
+                const int e = moe_ak[expert_of(it.rt, &rt_e)];
+                const uint32_t nl = (uint32_t)rt_e * 16u + (uint32_t)g, nmax = (uint32_t)L.N - 1u;
+                const uint32_t r0 = min(nl, nmax), r8 = min(nl + 8u, nmax);
+                const uint8_t* wp = p.packed + (size_t)e * moe.expert_bytes +
+                                    ((size_t)rt_e * (size_t)KC + (size_t)it.c) * kItemBytes + lane * 16;
+                const uint8_t* se = static_cast<const uint8_t*>(p.scales) + (size_t)e * moe.expert_scale_bytes;
+                const uint8_t* ze = p.zp != nullptr ? p.zp + (size_t)e * moe.expert_zp_bytes : nullptr;
+                b.load(wp, se, ze, srow, zrow, r0, r8, (uint32_t)it.c);
+            } else {
+                const uint32_t nl = (uint32_t)it.rt * 16u + (uint32_t)g;
+                const uint32_t r0 = min(nl, nlast), r8 = min(nl + 8u, nlast);
+                b.load(wbase + (uint32_t)it.i * (uint32_t)kItemBytes, sb, zb, srow, zrow, r0, r8, (uint32_t)it.c);
+            }
         }
     };
 
@@ -356,15 +398,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     //         wait), X staged in B-fragment order, then the second item: X
     //         queues behind one item of weights, not two ----
     It buf[2];
-    Cursor cur = Cursor{warp, 0, warp};
+    Cursor cur = MOE ? Cursor{0, warp, 0} : Cursor{warp, 0, warp};
     while (cur.c >= KC) {  // at most kW - 1 times
         cur.c -= KC;
         ++cur.rt;
     }
     Cursor nxt = cur;
-    nxt.advance(KC, q16, r16);
+    advance(nxt);
     load(buf[0], cur);
-    for (int o = tid; o < nrt * kW * 16 * M; o += kThreads) red[o] = 0.f;
+    if constexpr (!MOE)
+        for (int o = tid; o < nrt * kW * 16 * M; o += kThreads) red[o] = 0.f;
     const int pairs = (int)(L.K / 32);
     for (int o = tid; o < pairs * 4; o += kThreads) xs[(size_t)M * geo.xrow + o] = make_uint4(0, 0, 0, 0);
     if (pdl) {
@@ -385,8 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
 #pragma unroll
             for (int m = 0; m < (M1 ? 1 : 8); ++m) {
                 if (m < M && r < pairs * 4) {
-                    // grouped call: column m is pair pl[m] = t * S + s, row t of X (or row t * S + s)
-                    const int xr = MOE ? (moe.x_per_slot ? pl[MOE ? m : 0] : pl[MOE ? m : 0] / moe.S) : m;
+                    // grouped call: row m is pair m = t * S + s: row t of X (or row t * S + s)
+                    const int xr = MOE ? (moe.x_per_slot ? m : m / moe.S) : m;
                     const uint32_t* src = x32 + (int64_t)xr * kw + P * 16 + tt;
                     v[m] = make_uint4(__ldg(src), __ldg(src + 4), __ldg(src + 8), __ldg(src + 12));
                 }
@@ -402,7 +445,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     // ---- 2. items, two buffers: compute one while the next is in flight ----
     const uint32_t xa_lane = smem_u32(xs + (size_t)(g < M ? g : M) * geo.xrow + t);
     float y[4] = {0.f, 0.f, 0.f, 0.f};
+    const float bias_none = 0.f;
     auto flush = [&](int rt_l) {
+        if constexpr (MOE) {  // the row tile's sums are complete: store them (bias added here)
+            int rt_e;
+            const int k = expert_of(rt_l, &rt_e);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int m = 2 * t + (j & 1);
+                const int64_t n = (int64_t)rt_e * 16 + g + ((j >> 1) << 3);
+                const int yr = m < M ? moe_yrow[k * kMoeMaxPairs + m] : -1;
+                if (yr >= 0 && n < L.N) {
+                    const float b = p.bias ? load_f32(p.bias, n, p.bias_dtype) : bias_none;
+                    store_f32(p.y, (int64_t)yr * L.N + n, y[j] + b, p.out_dtype);
+                }
+            }
+            y[0] = y[1] = y[2] = y[3] = 0.f;
+            return;
+        }
         float* r = red + (size_t)(rt_l * kW + warp) * 16 * M;
         const int m0 = 2 * t, m1 = 2 * t + 1;
         if (m0 < M) {
@@ -417,18 +477,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     };
     // step: compute `cur` from b, refill b with the item after `nxt`, move on
     auto step = [&](It& b) {
-        b.template compute<M1>(xa_lane + (uint32_t)cur.c * (uint32_t)(CH / 2) * 64u, y);
+        uint32_t xa = xa_lane;
+        if constexpr (MOE) {  // this item's expert: its columns' X rows
+            int rt_e;
+            const int k = expert_of(cur.rt, &rt_e);
+            xa = smem_u32(xs + (size_t)moe_col[k * 8 + g] * geo.xrow + t);
+        }
+        b.template compute<M1>(xa + (uint32_t)cur.c * (uint32_t)(CH / 2) * 64u, y);
         Cursor after = nxt;
-        after.advance(KC, q16, r16);
+        advance(after);
         load(b, after);
-        if (nxt.i >= n_items || nxt.rt != cur.rt) flush(cur.rt);
+        if (!valid(nxt) || nxt.rt != cur.rt) flush(cur.rt);
         cur = nxt;
         nxt = after;
-        return cur.i < n_items;
+        return valid(cur);
     };
-    if (cur.i < n_items) {
+    if (valid(cur)) {
         while (step(buf[0]) && step(buf[1])) {
         }
+    }
+    if constexpr (MOE) {  // rows already stored
+        if (blockIdx.x == 0 && tid == 0)
+            for (int k = 0; k < n_active; ++k)
+                verify_header(static_cast<const uint8_t*>(p.packed_hdr) + (size_t)moe_ak[k] * moe.expert_bytes, L, p.status);
+        return;
     }
     __syncthreads();
 
@@ -455,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
         const int64_t n = (rt0 + rt_l) * 16 + row;
         if (n < L.N) {
             if (p.bias) v += load_f32(p.bias, n, p.bias_dtype);
-            store_f32(p.y, (int64_t)(MOE ? moe_yrow[MOE ? m : 0] : m) * L.N + n, v, p.out_dtype);
+            store_f32(p.y, (int64_t)m * L.N + n, v, p.out_dtype);
         }
     }
     if (blockIdx.x == 0 && tid == 0) verify_header(p.packed_hdr, L, p.status);
@@ -471,8 +543,7 @@ cudaError_t launch_k(const MatmulParams& p, const KGeom& geo, cudaStream_t s, co
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.total_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    // grouped: one grid row per expert that can be present (at most min(pairs, E))
-    cfg.gridDim = dim3((unsigned)geo.G, moe ? (unsigned)(moe->pairs < moe->E ? moe->pairs : moe->E) : 1u);
+    cfg.gridDim = dim3((unsigned)geo.G);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = geo.total_bytes;
     cfg.stream = s;

@@ -86,9 +86,21 @@ mnb_status mnb_matmul_grouped(const void* x, const int32_t* ids, const void* pac
         mk.expert_zp_bytes = (size_t)N * (size_t)q.L.zp_row;
         const int sms = device_info().sm_count > 0 ? device_info().sm_count : 148;
         gks::KGeom kg;
-        const bool fits = aligned_to(scales, 16) && mk.expert_scale_bytes % 16 == 0 &&
-                          (!zero_points || (aligned_to(zero_points, 16) && mk.expert_zp_bytes % 16 == 0)) &&
-                          gks::make_kgeom(q.L, pairs, sms, device_info().smem_optin, (int)dt_bytes(scale_dtype), &kg);
+        bool fits = aligned_to(scales, 16) && mk.expert_scale_bytes % 16 == 0 &&
+                    (!zero_points || (aligned_to(zero_points, 16) && mk.expert_zp_bytes % 16 == 0)) &&
+                    gks::make_kgeom(q.L, pairs, sms, device_info().smem_optin, (int)dt_bytes(scale_dtype), &kg);
+        // the active experts' row tiles end to end: at most min(pairs, E) x NT, split over the SMs
+        const int64_t u_max = (pairs < E ? pairs : E) * q.L.NT;
+        // (the kernel finds a row tile's expert with a float reciprocal of NT: exact for NT < 2^16)
+        if (fits && q.L.NT < 65536 && u_max * (sms + 1) < (int64_t)1 << 31) {
+            kg.G = (int)(u_max < sms ? u_max : sms);
+            kg.max_rt = (int)((u_max + kg.G - 1) / kg.G);
+            kg.red_bytes = 0;  // grouped: each warp stores its whole row tiles' sums itself
+            kg.total_bytes = kg.x_bytes;
+            fits = kg.total_bytes <= device_info().smem_optin;
+        } else {
+            fits = false;
+        }
         if (fits) {
             if (inject_launch_failure()) return MNB_ERR_CUDA;
             cudaStream_t st = (cudaStream_t)stream;
