@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--only", default=None, choices=["moe", "fp8", "nvfp4"],
+                    help="diagnostic: time only this secondary object (for profiling its kernel alone)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--accuracy-level", type=int, default=0, choices=[0, 4],
                     help="4: int8-activation path for the main workload")
@@ -491,6 +493,15 @@ def run_ours(args):
                 "clocks": ck, "weight_copies": R}, steps
 
     w = wl.config(args.config)
+    if args.only:
+        if args.only == "moe":
+            obj, n = measure_moe(wl.MOE_CONFIGS[0], args.steps, args.warmup)
+        else:
+            obj, n = measure_fp(mnb.MNB_WF_E4M3 if args.only == "fp8" else mnb.MNB_WF_NVFP4, 1, 11008, 4096,
+                                args.steps, args.warmup)
+        if rank == 0:
+            print(json.dumps({"only": args.only, args.only: obj, "gpu_launches": n}), flush=True)
+        return
     main, data = measure(w, args.steps, args.warmup, args.kernel, True, args.accuracy_level)
     res = {
         "metric": "int4 MatMulNBits GB/s at M=1, TFLOP/s at M=512; % of roofline",
