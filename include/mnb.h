@@ -246,6 +246,8 @@ MNB_API mnb_status mnb_matmul_a8_static(const void* x, const void* packed_b, con
  *   zero_points device uint8 [E, N, ceil(KB*bits/8)] or NULL (default
  *               2^(bits-1) for every expert).
  *   y           device [T, S, N] of out_dtype, 16-byte aligned.
+ * Calls with T*S <= 8 run the K-chunk decode schedule over the selected
+ * experts' row tiles end to end; larger calls the per-tile kernel.
  * The weights of experts that no pair selects are not read.  Limits:
  * E <= 1024 and T*S <= 4096 (MNB_ERR_UNSUPPORTED beyond).  An id outside
  * [0, E) is not checked on the host (ids live on the device): its Y row is
@@ -354,7 +356,9 @@ MNB_API mnb_status mnb_matmul_fp(const void* x, const void* packed, const void* 
  *   MNB_WAIT_LIMIT=n       test hook: n tries per bounded wait (then
  *                          MNB_ERR_TIMEOUT in the status word)
  *   MNB_GEMV_STAGE_BUFS, MNB_GEMV_MAX_SLOTS  ring shape of the f32 GEMV
- *   MNB_MOE_SETS           expert sets per row tile of mnb_matmul_grouped
+ *   MNB_MOE_SCHED=tile     mnb_matmul_grouped with at most 8 pairs on the
+ *                          per-tile kernel instead of the K-chunk schedule
+ *   MNB_MOE_SETS           expert sets per row tile of the per-tile grouped kernel
  *   MNB_FAIL_LAUNCH=1      test hook: every launch reports MNB_ERR_CUDA
  *                          without launching */
 

@@ -71,7 +71,11 @@ CASES = [
 
 
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
-def test_grouped_matches_oracle(mnb, oracle_mod, w):
+@pytest.mark.parametrize("sched", ["auto", "tile"])
+def test_grouped_matches_oracle(mnb, oracle_mod, monkeypatch, w, sched):
+    """Both schedules: the K-chunk grouped mode (at most 8 pairs, the default) and the per-tile kernel."""
+    if sched == "tile":
+        monkeypatch.setenv("MNB_MOE_SCHED", "tile")
     P = Grouped(mnb, w)
     y = P.run()
     y_ref, mag = P.oracle(oracle_mod)
