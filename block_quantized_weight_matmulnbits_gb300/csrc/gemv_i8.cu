@@ -1,5 +1,6 @@
 // Host side of the int8-activation path (kernels in gemv_i8.cuh).
 #include "gemv_i8.cuh"
+#include "gemv_ks.cuh"
 
 namespace mnb {
 namespace gi8 {
@@ -32,6 +33,39 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const void* x, int dt, i
             code = (int)fminf(fmaxf(r, -127.f), 127.f);
         }
         qa[m * L.Kpad + k] = (int8_t)code;
+    }
+}
+
+// The same quantisation for the decode GEMV on the bf16 K-chunk schedule:
+// x' = code * s_a in f32, written as two bf16 rows, hi = RN(x') and
+// lo = RN(x' - hi) (|x' - hi - lo| <= 2^-16 |x'|), rows 2m and 2m + 1 of xq
+// [2M][Kpad] (zero past K).
+__global__ void __launch_bounds__(256) quant_act_hilo_kernel(const void* x, int dt, uint16_t* xq, int64_t M,
+                                                             Layout L) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= M * L.KB) return;
+    const int64_t m = w / L.KB, kb = w - m * L.KB;
+    const int64_t k0 = kb * L.bs;
+    const int64_t k1 = imin64(k0 + L.bs, L.K);
+    float amax = 0.f;
+    for (int64_t k = k0 + lane; k < k1; k += 32) amax = fmaxf(amax, fabsf(load_f32(x, m * L.K + k, dt)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float s = __fdiv_rn(amax, 127.0f);
+    for (int64_t k = k0 + lane; k < k0 + L.bs; k += 32) {
+        int code = 0;
+        if (k < L.K && amax > 0.f) {
+            const float r = roundf(__fdiv_rn(load_f32(x, m * L.K + k, dt), s));  // half away from zero
+            code = (int)fminf(fmaxf(r, -127.f), 127.f);
+        }
+        const float v = __fmul_rn((float)code, s);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));  // v - hi is exact in f32
+        xq[(2 * m) * L.Kpad + k] = __bfloat16_as_ushort(hi);
+        xq[(2 * m + 1) * L.Kpad + k] = __bfloat16_as_ushort(lo);
     }
 }
 
@@ -102,10 +136,20 @@ cudaError_t launch_gemv_i8_b4(const MatmulParams& p, const gi8::Geom& geo, const
                               cudaStream_t s);
 cudaError_t launch_gemv_i8_b8(const MatmulParams& p, const gi8::Geom& geo, const int8_t* qa, const float* sa,
                               cudaStream_t s);
+cudaError_t launch_gemv_ks_b2(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe);
+cudaError_t launch_gemv_ks_b4(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe);
+cudaError_t launch_gemv_ks_b8(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe);
 
 static gi8::Geom geom_for(const MatmulParams& p) { return gi8::make_geom(p.L, p.M, p.M == 1 ? 1 : 16); }
 
-size_t i8_workspace_bytes(int64_t M, const Layout& L) { return gi8::workspace_bytes(M, L); }
+// M <= 4 may run on the bf16 K-chunk schedule over hi / lo activation rows: [2M][Kpad] bf16.
+static size_t hilo_bytes(int64_t M, const Layout& L) { return ((size_t)4 * M * (size_t)L.Kpad + 255) & ~size_t(255); }
+
+size_t i8_workspace_bytes(int64_t M, const Layout& L) {
+    const size_t a = gi8::workspace_bytes(M, L);
+    const size_t b = M <= 4 ? hilo_bytes(M, L) : 0;
+    return a > b ? a : b;
+}
 
 bool gemv_i8_supported(const MatmulParams& p) {
     if (p.M < 1 || p.M > 16 || p.g_idx != nullptr) return false;
@@ -146,7 +190,49 @@ cudaError_t launch_quant_act_tf32(const void* x, int act_dtype, float* xq, int64
     return quant_launch(x, act_dtype, nullptr, xq, nullptr, M, L, pdl, s);
 }
 
+// Accuracy level 4 with M <= 4: the quantised activations as hi + lo bf16 rows, then the bf16
+// K-chunk decode GEMV over them with each token's two columns summed (exact up to 2^-16 of
+// code * s_a per element, and f32 accumulation).  False when that schedule declines the shape.
+static bool hilo_ok(const MatmulParams& p, gks::KGeom* kg) {
+    const char* ev = std::getenv("MNB_A8_HILO");  // 0: always the int8 kernel (tests, tuning)
+    if (p.M > 4 || (ev && ev[0] == '0')) return false;
+    if ((reinterpret_cast<uintptr_t>(p.scales) & 15) != 0) return false;
+    if (p.zp && (reinterpret_cast<uintptr_t>(p.zp) & 15) != 0) return false;
+    const int sms = device_info().sm_count > 0 ? device_info().sm_count : 148;
+    if (!gks::make_kgeom(p.L, 2 * p.M, sms, device_info().smem_optin, p.scale_dtype == kF32 ? 4 : 2, kg)) return false;
+    kg->pairx = 1;
+    return true;
+}
+
 cudaError_t launch_gemv_i8(const MatmulParams& p, cudaStream_t s) {
+    gks::KGeom kg;
+    if (hilo_ok(p, &kg)) {
+        uint16_t* xq = static_cast<uint16_t*>(p.workspace);
+        cudaLaunchConfig_t cfg = {};
+        const int64_t blocks = (p.M * p.L.KB + 7) / 8;
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(256);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = (p.flags & kFlagPDL) ? 1 : 0;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, gi8::quant_act_hilo_kernel, p.x, p.act_dtype, xq, p.M, p.L);
+        if (e != cudaSuccess) return e;
+        MatmulParams q = p;
+        q.x = xq;
+        q.act_dtype = kBF16;
+        q.M = 2 * p.M;
+        switch (p.L.bits) {
+            case 2: e = launch_gemv_ks_b2(q, kg, s, nullptr); break;
+            case 4: e = launch_gemv_ks_b4(q, kg, s, nullptr); break;
+            case 8: e = launch_gemv_ks_b8(q, kg, s, nullptr); break;
+            default: return cudaErrorInvalidValue;
+        }
+        if (e != cudaErrorNotSupported) return e;
+        cudaGetLastError();  // not instantiated for this block size and scale type: the int8 kernel below
+    }
     const gi8::Geom geo = geom_for(p);
     if (geo.total_bytes > device_info().smem_optin) return cudaErrorNotSupported;
     int8_t* qa = static_cast<int8_t*>(p.workspace);

@@ -46,6 +46,8 @@ struct KGeom {
     int q16, r16; // a step of kW items: q16 row tiles and r16 chunks
     int max_rt;   // most row tiles of one CTA
     int xrow;     // X row stride in 16-byte units (K / 8 + 4: padded against bank conflicts)
+    int pairx;    // 1: X rows 2m, 2m + 1 are the hi and lo bf16 parts of one activation row m
+                  // (accuracy level 4); Y row m is the sum of their two columns
     size_t x_bytes, red_bytes, total_bytes;
 };
 
@@ -463,6 +465,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
             y[0] = y[1] = y[2] = y[3] = 0.f;
             return;
         }
+        if (!M1 && geo.pairx) {  // columns 2t, 2t + 1 are the hi and lo parts of token t
+            float* r = red + (size_t)(rt_l * kW + warp) * 16 * (M >> 1);
+            if (2 * t < M) {
+                r[t * 16 + g] = y[0] + y[1];
+                r[t * 16 + g + 8] = y[2] + y[3];
+            }
+            y[0] = y[1] = y[2] = y[3] = 0.f;
+            return;
+        }
         float* r = red + (size_t)(rt_l * kW + warp) * 16 * M;
         const int m0 = 2 * t, m1 = 2 * t + 1;
         if (m0 < M) {
@@ -508,16 +519,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     // consecutive threads take consecutive rows of one token (coalesced stores,
     // conflict-free reads); q = rt_l * M + m is split with a float reciprocal
     // (q < 2^16: exact after truncation of (q + 0.5) / M)
-    const float inv_m = M1 ? 1.f : 1.f / (float)M;
-    for (int o = tid; o < nrt * 16 * M; o += kThreads) {
+    const int MO = (!M1 && geo.pairx) ? M >> 1 : M;  // output columns
+    const float inv_m = M1 ? 1.f : 1.f / (float)MO;
+    for (int o = tid; o < nrt * 16 * MO; o += kThreads) {
         const int row = o & 15, q = o >> 4;
         const int rt_l = M1 ? q : __float2int_rz(((float)q + 0.5f) * inv_m);
-        const int m = M1 ? 0 : q - rt_l * M;
-        const float* src = red + (size_t)rt_l * kW * 16 * M + m * 16 + row;
+        const int m = M1 ? 0 : q - rt_l * MO;
+        const float* src = red + (size_t)rt_l * kW * 16 * MO + m * 16 + row;
         // the 16 warps' partials as a fixed pairwise tree (independent loads, depth 4)
         float t8[kW / 2];
 #pragma unroll
-        for (int w2 = 0; w2 < kW / 2; ++w2) t8[w2] = src[(size_t)(2 * w2) * 16 * M] + src[(size_t)(2 * w2 + 1) * 16 * M];
+        for (int w2 = 0; w2 < kW / 2; ++w2) t8[w2] = src[(size_t)(2 * w2) * 16 * MO] + src[(size_t)(2 * w2 + 1) * 16 * MO];
 #pragma unroll
         for (int h = kW / 4; h >= 1; h >>= 1) {
 #pragma unroll

@@ -114,7 +114,11 @@ A8_CASES = [
 
 
 @pytest.mark.parametrize("M,bits,bs,dt,asym,N,K", A8_CASES)
-def test_matmul_a8(G, mnb, oracle_mod, M, bits, bs, dt, asym, N, K):
+@pytest.mark.parametrize("hilo", ["1", "0"])
+def test_matmul_a8(G, mnb, oracle_mod, monkeypatch, M, bits, bs, dt, asym, N, K, hilo):
+    """M <= 4 runs the bf16 K-chunk GEMV over hi / lo activation rows where its shape limits
+    allow (hilo=1), else and with MNB_A8_HILO=0 the int8 dp4a kernel."""
+    monkeypatch.setenv("MNB_A8_HILO", hilo)
     w = _w(M, N, K, bits, bs, dt, asym, 40 + M + bits + bs)
     P = G.Problem(w)
     assert mnb.mnb_select_kernel(M, N, K, bits, bs, dt[0], 4) == "gemv_i8"
