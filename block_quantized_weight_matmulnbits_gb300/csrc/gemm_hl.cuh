@@ -68,6 +68,7 @@ __host__ __device__ constexpr size_t hl_bar_bytes(int r) { return (3 * r + 1) * 
 
 struct Geom {
     int ystore;         // 1: Y written by TMA from a shared-memory stage (Maps::y valid)
+    int pdl;            // launched as a programmatic dependent: X is read only after the dependency wait
     int n_tiles, m_tiles;
     int splitk;         // 1, or 2: the two CTAs of a cluster take halves of K
     int k_stages;       // stages of the whole K (ceil(Kpad / 64))
@@ -160,28 +161,48 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_hl_kernel(MatmulParams p, Ge
             const uint32_t bytes = (uint32_t)(XST + geo.wp_stage);
             const int nrt = (int)(n0 / 16);
             int issued = 0;
-            for (int i = 0; i < KS; ++i) {
-                const int s = i % R;
-                const uint32_t ph = (uint32_t)((i / R) & 1);
-                if (i >= R && !tc::wait_bounded(&mma_done[s], ph ^ 1u, p.status, wl, wh)) {
-                    *abort_v = 1;
-                    break;
-                }
-                if (*abort_v) break;
-                const int ks = ks_lo + i;
-                mbar_arrive_expect_tx(&tma_full[s], bytes);
+            auto load_x = [&](int i) {
+                const int s = i % R, ks = ks_lo + i;
                 if constexpr (TF32) {  // 64 depths of f32: two 128-byte boxes
                     tc::tma_load_2d(xs + s * XST, &xmap, ks * kBK, (int)m0, &tma_full[s]);
                     tc::tma_load_2d(xs + s * XST + BT * 128, &xmap, ks * kBK + 32, (int)m0, &tma_full[s]);
                 } else {
                     tc::tma_load_2d(xs + s * XST, &xmap, ks * kBK, (int)m0, &tma_full[s]);
                 }
+            };
+            auto load_w = [&](int i) {
+                const int s = i % R, ks = ks_lo + i;
                 // packed tiles of this stage: KT >= 64 tiles span whole stages (one load per tile)
                 if constexpr (KT > kBK) {
                     tc::tma_load_5d(wp + s * geo.wp_stage, &wmap, 0, 0, 0, (ks * kBK) / KT, nrt, &tma_full[s]);
                 } else {
                     tc::tma_load_5d(wp + s * geo.wp_stage, &wmap, 0, 0, 0, ks * TILES, nrt, &tma_full[s]);
                 }
+            };
+            // the first ring fill's weights do not depend on the previous kernel: they are
+            // requested before the dependency wait, X after it
+            const int pre = KS < R ? KS : R;
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&tma_full[i], bytes);
+                load_w(i);
+            }
+            if (geo.pdl) {
+                griddep_wait();               // X (and Y) may belong to the previous kernel on the stream
+                griddep_launch_dependents();  // after the wait: at most two chained kernels overlap
+            }
+            for (int i = 0; i < pre; ++i) load_x(i);
+            issued = pre;
+            for (int i = pre; i < KS; ++i) {
+                const int s = i % R;
+                const uint32_t ph = (uint32_t)((i / R) & 1);
+                if (!tc::wait_bounded(&mma_done[s], ph ^ 1u, p.status, wl, wh)) {
+                    *abort_v = 1;
+                    break;
+                }
+                if (*abort_v) break;
+                mbar_arrive_expect_tx(&tma_full[s], bytes);
+                load_x(i);
+                load_w(i);
                 issued = i + 1;
             }
             if (*abort_v) {
@@ -528,13 +549,15 @@ cudaError_t launch(const MatmulParams& p, const Geom& geo, const Maps& m, cudaSt
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = geo.total_bytes;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)geo.splitk;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = geo.pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, p, geo, m.x, m.w, m.y);
 }
 

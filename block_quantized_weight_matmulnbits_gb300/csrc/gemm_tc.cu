@@ -180,6 +180,7 @@ cudaError_t launch_hl(const MatmulParams& p, EncodeTiledFn enc, cudaStream_t s) 
     ghl::Maps m;
     std::memset(&m, 0, sizeof(m));
     geo.ystore = hl_ymap(p, geo, enc, &m.y) ? 1 : 0;
+    geo.pdl = (p.flags & kFlagPDL) ? 1 : 0;
     const cuuint32_t estr[2] = {1, 1};
     const cuuint64_t dims[2] = {(cuuint64_t)p.L.K, (cuuint64_t)p.M};
     const cuuint64_t strides[1] = {(cuuint64_t)p.L.K * 2};
@@ -255,6 +256,7 @@ cudaError_t launch_gemm_a8(const MatmulParams& p, cudaStream_t s) {
     ghl::Maps m;
     std::memset(&m, 0, sizeof(m));
     geo.ystore = hl_ymap(q, geo, enc, &m.y) ? 1 : 0;
+    geo.pdl = (p.flags & kFlagPDL) ? 1 : 0;
     const cuuint32_t estr[2] = {1, 1};
     const cuuint64_t dims[2] = {(cuuint64_t)p.L.Kpad, (cuuint64_t)p.M};
     const cuuint64_t strides[1] = {(cuuint64_t)p.L.Kpad * 4};
