@@ -376,18 +376,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
             it.advance(KC, q16, r16);
         }
     };
+    // grouped: a warp's items are the chunks of one row tile in a row, so the row tile's expert,
+    // bases and rows are worked out once per row tile (for the loads and for the X fragments)
+    int lc_rt = -1, cc_rt = -1;
+    const uint8_t *lc_w = nullptr, *lc_s = nullptr, *lc_z = nullptr;
+    uint32_t lc_r0 = 0, lc_r8 = 0, cc_xa = 0;
     auto load = [&](It& b, const Cursor& it) {
         if (valid(it)) {
             if constexpr (MOE) {
-                int rt_e;
-                const int e = moe_ak[expert_of(it.rt, &rt_e)];
-                const uint32_t nl = (uint32_t)rt_e * 16u + (uint32_t)g, nmax = (uint32_t)L.N - 1u;
-                const uint32_t r0 = min(nl, nmax), r8 = min(nl + 8u, nmax);
-                const uint8_t* wp = p.packed + (size_t)e * moe.expert_bytes +
-                                    ((size_t)rt_e * (size_t)KC + (size_t)it.c) * kItemBytes + lane * 16;
-                const uint8_t* se = static_cast<const uint8_t*>(p.scales) + (size_t)e * moe.expert_scale_bytes;
-                const uint8_t* ze = p.zp != nullptr ? p.zp + (size_t)e * moe.expert_zp_bytes : nullptr;
-                b.load(wp, se, ze, srow, zrow, r0, r8, (uint32_t)it.c);
+                if (it.rt != lc_rt) {
+                    lc_rt = it.rt;
+                    int rt_e;
+                    const int e = moe_ak[expert_of(it.rt, &rt_e)];
+                    const uint32_t nl = (uint32_t)rt_e * 16u + (uint32_t)g, nmax = (uint32_t)L.N - 1u;
+                    lc_r0 = min(nl, nmax);
+                    lc_r8 = min(nl + 8u, nmax);
+                    lc_w = p.packed + (size_t)e * moe.expert_bytes + (size_t)rt_e * (size_t)KC * kItemBytes + lane * 16;
+                    lc_s = static_cast<const uint8_t*>(p.scales) + (size_t)e * moe.expert_scale_bytes;
+                    lc_z = p.zp != nullptr ? p.zp + (size_t)e * moe.expert_zp_bytes : nullptr;
+                }
+                b.load(lc_w + (uint32_t)it.c * (uint32_t)kItemBytes, lc_s, lc_z, srow, zrow, lc_r0, lc_r8,
+                       (uint32_t)it.c);
             } else {
                 const uint32_t nl = (uint32_t)it.rt * 16u + (uint32_t)g;
                 const uint32_t r0 = min(nl, nlast), r8 = min(nl + 8u, nlast);
@@ -490,9 +499,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     auto step = [&](It& b) {
         uint32_t xa = xa_lane;
         if constexpr (MOE) {  // this item's expert: its columns' X rows
-            int rt_e;
-            const int k = expert_of(cur.rt, &rt_e);
-            xa = smem_u32(xs + (size_t)moe_col[k * 8 + g] * geo.xrow + t);
+            if (cur.rt != cc_rt) {
+                cc_rt = cur.rt;
+                int rt_e;
+                const int k = expert_of(cur.rt, &rt_e);
+                cc_xa = smem_u32(xs + (size_t)moe_col[k * 8 + g] * geo.xrow + t);
+            }
+            xa = cc_xa;
         }
         b.template compute<M1>(xa + (uint32_t)cur.c * (uint32_t)(CH / 2) * 64u, y);
         Cursor after = nxt;
