@@ -482,13 +482,16 @@ def run_ours(args):
             mnb.mnb_matmul_fp(x, pb, s, 0.05, yb, M, N, K, fmt, act, out, stream=stream)
 
         t, ck = replay_timed(call, steps, warmup, stream)
+        # NVFP4 decodes on the tensor-core GEMV unless MNB_FP_KERNEL picks another
+        fpk = os.environ.get("MNB_FP_KERNEL", "")
+        kern = "fp_generic" if fpk == "generic" else "gemv_nv" if fmt == mnb.MNB_WF_NVFP4 and fpk != "lut" else "gemv_fp"
         per_step = (wbytes + sbytes + M * K * 2 + M * N * 2) / 1e9
         per_launch_s = t / steps
         achieved = per_step / per_launch_s
         return {"workload": name, "value": whole_job_value(world, steps, per_step, t), "unit": "GB/s",
-                "kernel": "gemv_fp", "ms_per_step": per_launch_s * 1e3, "steps": steps,
+                "kernel": kern, "ms_per_step": per_launch_s * 1e3, "steps": steps,
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                             "frac": achieved / pk["hbm_gbs"], "traffic": traffic_for(f"gemv_fp:{name}"),
+                             "frac": achieved / pk["hbm_gbs"], "traffic": traffic_for(f"{kern}:{name}"),
                              "algorithmic_bytes": int(per_step * 1e9), "peak_source": f"{pk_src} hbm_gbs"},
                 "clocks": ck, "weight_copies": R}, steps
 

@@ -315,7 +315,7 @@ mnb_status mnb_matmul_fp(const void* x, const void* packed, const void* scales, 
     const bool fast = gemv_fp_supported(p);
     if (log_enabled())
         std::fprintf(stderr, "[mnb] matmul_fp M=%lld N=%lld K=%lld format=%d kernel=%s\n", (long long)M,
-                     (long long)N, (long long)K, (int)format, fast ? "gemv_fp" : "fp_generic");
+                     (long long)N, (long long)K, (int)format, fast ? (gemv_nv_selected(p) ? "gemv_nv" : "gemv_fp") : "fp_generic");
     return from_cuda(fast ? launch_gemv_fp(p, (cudaStream_t)stream) : launch_fp_generic(p, (cudaStream_t)stream));
 }
 

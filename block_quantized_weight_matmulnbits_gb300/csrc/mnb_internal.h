@@ -65,6 +65,7 @@ inline void fp_layout(Layout* L, int64_t N, int64_t K, int fmt) {
 
 cudaError_t launch_fp_generic(const FpParams& p, cudaStream_t s);
 bool gemv_fp_supported(const FpParams& p);
+bool gemv_nv_selected(const FpParams& p);
 cudaError_t launch_gemv_fp(const FpParams& p, cudaStream_t s);
 
 // Accuracy level 4 on the prefill GEMM: workspace = the quantised

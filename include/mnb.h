@@ -359,6 +359,8 @@ MNB_API mnb_status mnb_matmul_fp(const void* x, const void* packed, const void* 
  *   MNB_A8_HILO=0          accuracy level 4 with M <= 4: the int8 dp4a GEMV
  *                          instead of hi / lo bf16 activation rows
  *   MNB_FP_KERNEL=generic  FP8 / NVFP4: the exact generic kernel
+ *   MNB_FP_KERNEL=lut      NVFP4 decode: the CUDA-core table GEMV instead
+ *                          of the tensor-core one
  *   MNB_MOE_SCHED=tile     mnb_matmul_grouped with at most 8 pairs on the
  *                          per-tile kernel instead of the K-chunk schedule
  *   MNB_MOE_SETS           expert sets per row tile of the per-tile grouped kernel

@@ -248,6 +248,35 @@ def test_fp_decode_gemv(G, monkeypatch, M, N, K, act, out, fmt):
     monkeypatch.setenv("MNB_FP_KERNEL", "generic")
     y2 = _run(G, xs, act, packed, st, gs, M, N, K, fmt, out)
     G.assert_within(y2, ref, mag, out, f"fp generic fmt={fmt} {M}x{N}x{K}")
+    if fmt == mnb.MNB_WF_NVFP4:
+        # the table kernel, which the tensor-core kernel replaces for these shapes
+        monkeypatch.setenv("MNB_FP_KERNEL", "lut")
+        y3 = _run(G, xs, act, packed, st, gs, M, N, K, fmt, out)
+        G.assert_within(y3, ref, mag, out, f"fp lut fmt={fmt} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("act", [BF16, F16])
+def test_nvfp4_decode_gemv_every_nibble_and_scale_code(G, act):
+    """The tensor-core NVFP4 GEMV on one-hot rows: every E2M1 nibble (the subnormal 0.5 and both zeros
+    included) under every E4M3 block-scale code equals the page's f32(f32(e2m1 * e4m3) * global) bit for
+    bit, and only the NaN scale codes give NaN."""
+    N, K, M = 256, 512, 4
+    rng = np.random.default_rng(405 + act)
+    w4 = rng.integers(0, 16, size=(K, N)).astype(np.uint8)
+    w4[:16, :] = np.arange(16, dtype=np.uint8)[:, None]  # block 0: nibble k at depth k, every column
+    s8 = rng.choice([c for c in range(256) if (c & 0x7F) != 0x7F], size=(K // 16, N)).astype(np.uint8)
+    s8[0, :] = np.arange(256, dtype=np.uint8)  # block 0: every scale code, one per column
+    gs = np.float32(0.7351)
+    packed = _pack(G, _nibbles(w4), N, K, mnb.MNB_WF_NVFP4)
+    st = torch.from_numpy(s8).cuda()
+    for d0 in range(0, 16, M):
+        x = np.zeros((M, K))
+        x[np.arange(M), d0 + np.arange(M)] = 1.0
+        y = _run(G, wl.to_storage(x, act), act, packed, st, float(gs), M, N, K, mnb.MNB_WF_NVFP4, F32)
+        ref, _ = oracle.matmul_nvfp4(x, _nibbles(w4), s8, float(gs), K, N)
+        fin = _same_class(y, ref)
+        assert np.array_equal(y[fin], ref[fin]), f"depths {d0}..{d0 + M - 1}"
+        assert set(np.nonzero(~fin)[1].tolist()) == {0x7F, 0xFF}
 
 
 @pytest.mark.parametrize("fmt", [mnb.MNB_WF_E4M3, mnb.MNB_WF_E5M2])
