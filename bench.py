@@ -479,7 +479,7 @@ def run_ours(args):
 
         def call(i):
             pb, s = copies[i % R]
-            mnb.mnb_matmul_fp(x, pb, s, 0.05, yb, M, N, K, fmt, act, out, stream=stream)
+            mnb.mnb_matmul_fp(x, pb, s, 0.05, yb, M, N, K, fmt, act, out, stream=stream, flags=flags)
 
         t, ck = replay_timed(call, steps, warmup, stream)
         # NVFP4 decodes on the tensor-core GEMV unless MNB_FP_KERNEL picks another

@@ -28,6 +28,7 @@ EXPORTS = [
     "mnb_matmul_ex", "mnb_workspace_size", "mnb_quantize_activations", "mnb_select_kernel",
     "mnb_get_device_error", "mnb_status_string", "mnb_kernel_name", "mnb_abi_version", "mnb_matmul_a8_static",
     "mnb_matmul_host_io", "mnb_matmul_grouped", "mnb_fp_packed_size", "mnb_pack_fp_weights", "mnb_matmul_fp",
+    "mnb_matmul_fp_ex",
 ]
 MNB_A8_STATIC_SCRATCH_BYTES = 1 << 20
 MNB_HOST_IO_X_BYTES = 8 << 20
@@ -89,6 +90,7 @@ def load(build: bool = True):
             "mnb_fp_packed_size": (sz, [i64, i64, ci]),
             "mnb_pack_fp_weights": (ci, [vp, vp, sz, i64, i64, ci, vp]),
             "mnb_matmul_fp": (ci, [vp, vp, vp, ctypes.c_float, vp, i64, i64, i64, ci, ci, ci, vp]),
+            "mnb_matmul_fp_ex": (ci, [vp, vp, vp, ctypes.c_float, vp, i64, i64, i64, ci, ci, ci, vp, ci]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -214,8 +216,13 @@ def mnb_pack_fp_weights(w_kn, packed, N, K, fmt, stream=None):
                                       _stream(stream)), "mnb_pack_fp_weights")
 
 
-def mnb_matmul_fp(x, packed, scales, global_scale, y, M, N, K, fmt, act_dtype, out_dtype, stream=None):
-    """Y = X . W for an FP8 (scales f32 [N] or None) or NVFP4 (e4m3 [ceil(K/16), N] scales) weight."""
+def mnb_matmul_fp(x, packed, scales, global_scale, y, M, N, K, fmt, act_dtype, out_dtype, stream=None, flags=0):
+    """Y = X . W for an FP8 (scales f32 [N] or None) or NVFP4 (e4m3 [ceil(K/16), N] scales) weight;
+    flags (MNB_FLAG_*) go through mnb_matmul_fp_ex."""
+    if flags:
+        _check(load().mnb_matmul_fp_ex(_ptr(x), _ptr(packed), _ptr(scales), float(global_scale), _ptr(y), M, N, K,
+                                       fmt, act_dtype, out_dtype, _stream(stream), int(flags)), "mnb_matmul_fp_ex")
+        return
     _check(load().mnb_matmul_fp(_ptr(x), _ptr(packed), _ptr(scales), float(global_scale), _ptr(y), M, N, K, fmt,
                                 act_dtype, out_dtype, _stream(stream)), "mnb_matmul_fp")
 

@@ -289,7 +289,14 @@ mnb_status mnb_pack_fp_weights(const uint8_t* w_kn, void* packed, size_t packed_
 mnb_status mnb_matmul_fp(const void* x, const void* packed, const void* scales, float global_scale, void* y,
                          int64_t M, int64_t N, int64_t K, mnb_wformat format, mnb_dtype act_dtype,
                          mnb_dtype out_dtype, mnb_stream_t stream) {
-    if (!valid_fp(N, K, format) || M < 0 || !valid_dtype(act_dtype) || !valid_dtype(out_dtype))
+    return mnb_matmul_fp_ex(x, packed, scales, global_scale, y, M, N, K, format, act_dtype, out_dtype, stream, 0);
+}
+
+mnb_status mnb_matmul_fp_ex(const void* x, const void* packed, const void* scales, float global_scale, void* y,
+                            int64_t M, int64_t N, int64_t K, mnb_wformat format, mnb_dtype act_dtype,
+                            mnb_dtype out_dtype, mnb_stream_t stream, int flags) {
+    if (!valid_fp(N, K, format) || M < 0 || !valid_dtype(act_dtype) || !valid_dtype(out_dtype) ||
+        (flags & ~MNB_FLAG_PDL) != 0)
         return MNB_ERR_INVALID_ARG;
     if (M == 0) return MNB_OK;
     if (!x || !packed || !y || (format == MNB_WF_NVFP4 && !scales)) return MNB_ERR_INVALID_ARG;
@@ -311,6 +318,7 @@ mnb_status mnb_matmul_fp(const void* x, const void* packed, const void* scales, 
     p.act_dtype = act_dtype;
     p.out_dtype = out_dtype;
     p.status = pd->status;
+    p.flags = flags;
     if (inject_launch_failure()) return MNB_ERR_CUDA;
     const bool fast = gemv_fp_supported(p);
     if (log_enabled())

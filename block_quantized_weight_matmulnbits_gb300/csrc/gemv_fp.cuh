@@ -93,7 +93,7 @@ __device__ __forceinline__ float x_hi(uint32_t v) {
 }
 
 template <int FMT, bool BF16X, int MT>
-__global__ void __launch_bounds__(kThreads, 1) gemv_fp_kernel(FpParams p, FGeom geo) {
+__global__ void __launch_bounds__(kThreads, 1) gemv_fp_kernel(FpParams p, FGeom geo, int pdl) {
     constexpr bool NV = FMT == kWfNVFP4;
     constexpr int SPT = NV ? 4 : 2;            // k-steps per packed tile
     constexpr int CH = kTilesPerChunk * SPT;   // k-steps per chunk
@@ -154,6 +154,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fp_kernel(FpParams p, FGeom 
         }
     }
     for (int o = tid; o < nrt * kW * 16 * M; o += kThreads) red[o] = 0.f;
+    if (pdl) {
+        griddep_wait();               // X (and Y) may belong to the previous kernel on the stream
+        griddep_launch_dependents();  // after the wait: at most two chained kernels overlap
+    }
     {
         const uint32_t* x32 = static_cast<const uint32_t*>(p.x);  // K even: rows are 4-byte aligned
         const int64_t kw = L.K / 2;
@@ -309,11 +313,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fp_kernel(FpParams p, FGeom 
 template <int FMT>
 cudaError_t launch_fmt(const FpParams& p, const FGeom& geo, cudaStream_t s) {
     const bool bf = p.act_dtype == kBF16;
+    const int pdl = (p.flags & kFlagPDL) ? 1 : 0;
     auto go = [&](auto kern) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.total_bytes);
         if (e != cudaSuccess) return e;
-        kern<<<(unsigned)geo.G, kThreads, geo.total_bytes, s>>>(p, geo);
-        return cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)geo.G);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = geo.total_bytes;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+        return cudaLaunchKernelEx(&cfg, kern, p, geo, pdl);
     };
     if (p.M == 1) return bf ? go(gemv_fp_kernel<FMT, true, 1>) : go(gemv_fp_kernel<FMT, false, 1>);
     return bf ? go(gemv_fp_kernel<FMT, true, 4>) : go(gemv_fp_kernel<FMT, false, 4>);

@@ -122,7 +122,7 @@ __device__ __forceinline__ void kstep_a(uint32_t w, uint32_t (&a)[4]) {
 }
 
 template <bool BF16X, bool M1>
-__global__ void __launch_bounds__(kThreads, 1) gemv_nv_kernel(FpParams p, NGeom geo) {
+__global__ void __launch_bounds__(kThreads, 1) gemv_nv_kernel(FpParams p, NGeom geo, int pdl) {
     const Layout& L = p.L;
     extern __shared__ __align__(128) uint8_t smem[];
     uint4* xs = reinterpret_cast<uint4*>(smem);                                 // [M + 1][xrow]: row M is zeros
@@ -224,6 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_nv_kernel(FpParams p, NGeom 
     for (int o = tid; o < nrt * kW * 16 * M; o += kThreads) red[o] = 0.f;
     const int pairs = (int)(L.K / 32);
     for (int o = tid; o < pairs * 4; o += kThreads) xs[(size_t)M * geo.xrow + o] = make_uint4(0, 0, 0, 0);
+    if (pdl) {
+        griddep_wait();               // X (and Y) may belong to the previous kernel on the stream
+        griddep_launch_dependents();  // after the wait: at most two chained kernels overlap
+    }
     {
         // X in B-fragment order: entry (m, pair P, lane class tt) holds depths
         // 32P + 2tt + {0, 1}, + 8, + 16, + 24 of row m
@@ -328,11 +332,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_nv_kernel(FpParams p, NGeom 
 
 inline cudaError_t launch(const FpParams& p, const NGeom& geo, cudaStream_t s) {
     const bool bf = p.act_dtype == kBF16;
+    const int pdl = (p.flags & kFlagPDL) ? 1 : 0;
     auto go = [&](auto kern) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.total_bytes);
         if (e != cudaSuccess) return e;
-        kern<<<(unsigned)geo.G, kThreads, geo.total_bytes, s>>>(p, geo);
-        return cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)geo.G);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = geo.total_bytes;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+        return cudaLaunchKernelEx(&cfg, kern, p, geo, pdl);
     };
     if (p.M == 1) return bf ? go(gemv_nv_kernel<true, true>) : go(gemv_nv_kernel<false, true>);
     return bf ? go(gemv_nv_kernel<true, false>) : go(gemv_nv_kernel<false, false>);

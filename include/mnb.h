@@ -92,8 +92,9 @@ typedef enum mnb_kernel {
  * kernel on the stream has finished (its X and Y accesses still wait for it),
  * and lets the next kernel start as its own blocks retire.  Use it only when
  * the preceding kernel does not write packed_b, scales, zero_points or bias
- * (true for constant model weights).  Honoured by MNB_KERNEL_GEMV_MMA and
- * MNB_KERNEL_GEMV_I8; other kernels ignore it. */
+ * (true for constant model weights).  Honoured by MNB_KERNEL_GEMV_MMA,
+ * MNB_KERNEL_GEMV_I8 and the FP8 / NVFP4 decode GEMVs (mnb_matmul_fp_ex);
+ * other kernels ignore it. */
 #define MNB_FLAG_PDL 1
 
 /* ---- weight layout (one-time re-tiling) -------------------------------- */
@@ -331,6 +332,14 @@ MNB_API mnb_status mnb_pack_fp_weights(const uint8_t* w_kn, void* packed, size_t
 MNB_API mnb_status mnb_matmul_fp(const void* x, const void* packed, const void* scales, float global_scale,
                          void* y, int64_t M, int64_t N, int64_t K, mnb_wformat format, mnb_dtype act_dtype,
                          mnb_dtype out_dtype, mnb_stream_t stream);
+
+/* mnb_matmul_fp with MNB_FLAG_* flags (0 for none; an unknown bit is
+ * MNB_ERR_INVALID_ARG).  With MNB_FLAG_PDL the decode GEMVs read the weights
+ * and the NVFP4 block scales before the preceding kernel on the stream has
+ * finished; X and Y wait for it. */
+MNB_API mnb_status mnb_matmul_fp_ex(const void* x, const void* packed, const void* scales, float global_scale,
+                            void* y, int64_t M, int64_t N, int64_t K, mnb_wformat format,
+                            mnb_dtype act_dtype, mnb_dtype out_dtype, mnb_stream_t stream, int flags);
 
 /* ---- diagnostics ------------------------------------------------------- */
 

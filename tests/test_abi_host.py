@@ -78,6 +78,9 @@ def test_fp_matmul_rejects_invalid_before_cuda():
     assert lib.mnb_matmul_fp(None, None, None, 1.0, None, 0, 8, 8, 1, 0, 0, None) == mnb.MNB_OK  # M == 0
     assert lib.mnb_matmul_fp(None, None, None, 1.0, None, 1, 8, 8, 9, 0, 0, None) == mnb.MNB_ERR_INVALID_ARG
     assert lib.mnb_pack_fp_weights(None, None, 0, 8, 8, 1, None) == mnb.MNB_ERR_INVALID_ARG
+    # the flags form: an unknown flag bit is an argument error; MNB_FLAG_PDL alone is not
+    assert lib.mnb_matmul_fp_ex(None, None, None, 1.0, None, 0, 8, 8, 1, 0, 0, None, 2) == mnb.MNB_ERR_INVALID_ARG
+    assert lib.mnb_matmul_fp_ex(None, None, None, 1.0, None, 0, 8, 8, 1, 0, 0, None, mnb.MNB_FLAG_PDL) == mnb.MNB_OK
 
 
 @pytest.mark.parametrize("M,K,bs", [(17, 4096, 32), (512, 4096, 32), (64, 1000, 128)])

@@ -316,3 +316,34 @@ def test_nvfp4_decode_gemv_nan_scale_codes(G):
     fin = _same_class(y, ref)
     assert set(np.nonzero(~fin)[1].tolist()) == {10, 41}
     G.assert_within(np.where(fin, y, 0), np.where(fin, ref, 0), np.where(fin, mag, 0), F32, "nvfp4 gemv finite")
+
+
+@pytest.mark.parametrize("fmt,kern", [(mnb.MNB_WF_NVFP4, ""), (mnb.MNB_WF_NVFP4, "lut"), (mnb.MNB_WF_E4M3, "")])
+def test_fp_pdl_chain_matches_plain_launches(G, monkeypatch, fmt, kern):
+    """y1 = f(x), y2 = f(y1), y3 = f(y2) launched with MNB_FLAG_PDL equals the plain chain bit for bit: each
+    call stages its X only after the previous call has finished."""
+    if kern:
+        monkeypatch.setenv("MNB_FP_KERNEL", kern)
+    N = K = 1024
+    rng = np.random.default_rng(911 + fmt)
+    if fmt == mnb.MNB_WF_NVFP4:
+        w4 = rng.integers(0, 16, size=(K, N)).astype(np.uint8)
+        s8 = rng.choice(np.arange(0x20, 0x38), size=(K // 16, N)).astype(np.uint8)
+        src, st, gs = _nibbles(w4), torch.from_numpy(s8).cuda(), 0.03
+    else:
+        src = rng.choice(_finite_fp8_codes(False), size=(K, N)).astype(np.uint8)
+        st, gs = torch.from_numpy(rng.uniform(1e-3, 1e-2, size=N).astype(np.float32)).cuda(), 0.0
+    packed = _pack(G, src, N, K, fmt)
+    x0 = G.to_dev(wl.to_storage(rng.standard_normal((1, K)), BF16), BF16)
+    outs = {}
+    for flags in (0, mnb.MNB_FLAG_PDL):
+        ys = [torch.empty((1, N), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+        xin = x0
+        for y in ys:
+            mnb.mnb_matmul_fp(xin, packed, st, gs, y, 1, N, K, fmt, BF16, BF16, flags=flags)
+            xin = y
+        torch.cuda.synchronize()
+        assert mnb.mnb_get_device_error() == mnb.MNB_OK
+        outs[flags] = [y.clone() for y in ys]
+    for a, b in zip(outs[0], outs[mnb.MNB_FLAG_PDL]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
