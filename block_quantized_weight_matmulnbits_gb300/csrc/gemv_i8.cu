@@ -136,9 +136,12 @@ cudaError_t launch_gemv_i8_b4(const MatmulParams& p, const gi8::Geom& geo, const
                               cudaStream_t s);
 cudaError_t launch_gemv_i8_b8(const MatmulParams& p, const gi8::Geom& geo, const int8_t* qa, const float* sa,
                               cudaStream_t s);
-cudaError_t launch_gemv_ks_b2(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe);
-cudaError_t launch_gemv_ks_b4(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe);
-cudaError_t launch_gemv_ks_b8(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe);
+cudaError_t launch_gemv_ks_b2(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe,
+                              bool a8 = false);
+cudaError_t launch_gemv_ks_b4(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe,
+                              bool a8 = false);
+cudaError_t launch_gemv_ks_b8(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe,
+                              bool a8 = false);
 
 static gi8::Geom geom_for(const MatmulParams& p) { return gi8::make_geom(p.L, p.M, p.M == 1 ? 1 : 16); }
 
@@ -207,6 +210,22 @@ static bool hilo_ok(const MatmulParams& p, gks::KGeom* kg) {
 cudaError_t launch_gemv_i8(const MatmulParams& p, cudaStream_t s) {
     gks::KGeom kg;
     if (hilo_ok(p, &kg)) {
+        // one launch: the decode GEMV quantises X while staging it (block sizes 32 .. 256);
+        // MNB_A8_HILO=2 takes the two-launch form below (the same bits, for tests)
+        const char* ev = std::getenv("MNB_A8_HILO");
+        const bool fused = !(ev && ev[0] == '2');
+        MatmulParams f = p;
+        f.M = 2 * p.M;  // hi / lo rows; X stays p.x in its own type
+        cudaError_t e = cudaErrorNotSupported;
+        if (fused) switch (p.L.bits) {
+            case 2: e = launch_gemv_ks_b2(f, kg, s, nullptr, true); break;
+            case 4: e = launch_gemv_ks_b4(f, kg, s, nullptr, true); break;
+            case 8: e = launch_gemv_ks_b8(f, kg, s, nullptr, true); break;
+            default: return cudaErrorInvalidValue;
+        }
+        if (e != cudaErrorNotSupported) return e;
+        cudaGetLastError();
+        // otherwise the quantised rows through the workspace, then the GEMV over them
         uint16_t* xq = static_cast<uint16_t*>(p.workspace);
         cudaLaunchConfig_t cfg = {};
         const int64_t blocks = (p.M * p.L.KB + 7) / 8;
@@ -218,7 +237,7 @@ cudaError_t launch_gemv_i8(const MatmulParams& p, cudaStream_t s) {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = (p.flags & kFlagPDL) ? 1 : 0;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, gi8::quant_act_hilo_kernel, p.x, p.act_dtype, xq, p.M, p.L);
+        e = cudaLaunchKernelEx(&cfg, gi8::quant_act_hilo_kernel, p.x, p.act_dtype, xq, p.M, p.L);
         if (e != cudaSuccess) return e;
         MatmulParams q = p;
         q.x = xq;

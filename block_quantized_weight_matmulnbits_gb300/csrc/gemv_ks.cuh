@@ -277,8 +277,17 @@ struct Cursor {
     }
 };
 
-template <int BITS, bool BF16X, int SPB_LOG, int SDT, bool M1, bool MOE>
+// A8: accuracy level 4 (bf16 MMAs, M = 2 x the activation rows, pairx): X is read
+// raw (p.act_dtype bf16, f16 or f32) and quantised while it is staged, per (row,
+// block) as quantize_activation_signed of onnx-runtime-ep-cpu 0.1.0-dev.5,
+// src/kernels/matmul_nbits.rs does it (s_a = amax / 127, code = round(x / s_a)
+// half away from zero, clamped to +-127), each x' = code * s_a in f32 staged as
+// its hi = RN_bf16(x') and lo = RN_bf16(x' - hi) in rows 2a and 2a + 1: the same
+// operations on the same values as quant_act_hilo_kernel, so the same bits.
+// Needs 32 <= bs <= 256 (a block's bs / 8 staging lanes reduce its max).
+template <int BITS, bool BF16X, int SPB_LOG, int SDT, bool M1, bool MOE, bool A8 = false>
 __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KGeom geo, int pdl, MoeKs moe) {
+    static_assert(!A8 || (BF16X && !M1 && !MOE), "accuracy level 4 staging: bf16 hi / lo rows");
     using It = Item<BITS, BF16X, SPB_LOG, SDT>;
     constexpr int CH = It::CH;
     const Layout& L = p.L;
@@ -425,7 +434,79 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
         griddep_wait();               // X (and Y) may belong to the previous kernel on the stream
         griddep_launch_dependents();  // after the wait: at most two chained kernels overlap
     }
-    {
+    if constexpr (A8) {
+        // entry (row, pair P, lane class tt) holds depths 32P + 2tt + {0, 1}, + 8, + 16, + 24 (pairs);
+        // a block's entries are bs / 8 consecutive lanes, whose max |x| is reduced with shuffles
+        const int MA = M >> 1;  // activation rows
+        const int G = (int)(L.bs >> 3);
+        for (int r0 = 0; r0 < pairs * 4; r0 += kThreads) {
+            const int r = r0 + tid;
+            const bool live = r < pairs * 4;
+            const int P = r >> 2, tt = r & 3;
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                if (a < MA) {
+                    float v[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[j] = 0.f;
+                    const int64_t k0 = (int64_t)a * L.K + 32 * P + 2 * tt;
+                    if (live) {
+                        if (p.act_dtype == kF32) {
+                            const float* xf = static_cast<const float*>(p.x) + k0;  // 8-byte aligned pairs
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float2 f = __ldg(reinterpret_cast<const float2*>(xf + 8 * j));
+                                v[2 * j] = f.x;
+                                v[2 * j + 1] = f.y;
+                            }
+                        } else {
+                            const uint32_t* xw = static_cast<const uint32_t*>(p.x) + (k0 >> 1);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint32_t wv = __ldg(xw + 4 * j);
+                                if (p.act_dtype == kBF16) {
+                                    v[2 * j] = __uint_as_float(wv << 16);
+                                    v[2 * j + 1] = __uint_as_float(wv & 0xFFFF0000u);
+                                } else {
+                                    v[2 * j] = __half2float(__ushort_as_half((unsigned short)(wv & 0xFFFFu)));
+                                    v[2 * j + 1] = __half2float(__ushort_as_half((unsigned short)(wv >> 16)));
+                                }
+                            }
+                        }
+                    }
+                    float amax = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+                    for (int o = G >> 1; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                    const float sa = __fdiv_rn(amax, 127.0f);
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t h2[2], l2[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            int code = 0;
+                            if (amax > 0.f) {
+                                const float q = roundf(__fdiv_rn(v[2 * j + e], sa));  // half away from zero
+                                code = (int)fminf(fmaxf(q, -127.f), 127.f);
+                            }
+                            const float xq = __fmul_rn((float)code, sa);
+                            const __nv_bfloat16 hi = __float2bfloat16_rn(xq);
+                            const __nv_bfloat16 lo = __float2bfloat16_rn(xq - __bfloat162float(hi));  // exact difference
+                            h2[e] = __bfloat16_as_ushort(hi);
+                            l2[e] = __bfloat16_as_ushort(lo);
+                        }
+                        hw[j] = h2[0] | (h2[1] << 16);
+                        lw[j] = l2[0] | (l2[1] << 16);
+                    }
+                    if (live) {
+                        xs[(size_t)(2 * a) * geo.xrow + r] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        xs[(size_t)(2 * a + 1) * geo.xrow + r] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                }
+            }
+        }
+    } else {
         // item (m, pair P, lane class tt), k0 = 32 P:
         // (x[k0 + 2tt..], x[k0 + 8 + 2tt..], x[k0 + 16 + 2tt..], x[k0 + 24 + 2tt..])
         const uint32_t* x32 = static_cast<const uint32_t*>(p.x);  // K even: rows are 4-byte aligned
@@ -559,11 +640,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
 }
 
 template <int BITS, bool BF16X, int SPB_LOG, int SDT>
-cudaError_t launch_k(const MatmulParams& p, const KGeom& geo, cudaStream_t s, const MoeKs* moe) {
+cudaError_t launch_k(const MatmulParams& p, const KGeom& geo, cudaStream_t s, const MoeKs* moe, bool a8) {
     const int pdl = (p.flags & kFlagPDL) ? 1 : 0;
     auto kern = moe ? gemv_ks_kernel<BITS, BF16X, SPB_LOG, SDT, false, true>
                 : p.M == 1 ? gemv_ks_kernel<BITS, BF16X, SPB_LOG, SDT, true, false>
                            : gemv_ks_kernel<BITS, BF16X, SPB_LOG, SDT, false, false>;
+    if constexpr (BF16X && SPB_LOG >= 1) {
+        if (a8) kern = gemv_ks_kernel<BITS, true, SPB_LOG, SDT, false, false, true>;
+    } else {
+        if (a8) return cudaErrorNotSupported;
+    }
     const MoeKs none{};
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.total_bytes);
     if (e != cudaSuccess) return e;
@@ -581,40 +667,45 @@ cudaError_t launch_k(const MatmulParams& p, const KGeom& geo, cudaStream_t s, co
 }
 
 template <int BITS, bool BF16X, int SPB_LOG>
-cudaError_t launch_sdt(const MatmulParams& p, const KGeom& geo, cudaStream_t s, const MoeKs* moe) {
+cudaError_t launch_sdt(const MatmulParams& p, const KGeom& geo, cudaStream_t s, const MoeKs* moe, bool a8) {
     constexpr int BPC = chunk_steps(BITS) >> SPB_LOG;
     switch (p.scale_dtype) {
         case kF32:
-            if constexpr (BPC * 4 <= 32) return launch_k<BITS, BF16X, SPB_LOG, kF32>(p, geo, s, moe);
+            if constexpr (BPC * 4 <= 32) return launch_k<BITS, BF16X, SPB_LOG, kF32>(p, geo, s, moe, a8);
             break;
-        case kF16: return launch_k<BITS, BF16X, SPB_LOG, kF16>(p, geo, s, moe);
-        case kBF16: return launch_k<BITS, BF16X, SPB_LOG, kBF16>(p, geo, s, moe);
+        case kF16: return launch_k<BITS, BF16X, SPB_LOG, kF16>(p, geo, s, moe, a8);
+        case kBF16: return launch_k<BITS, BF16X, SPB_LOG, kBF16>(p, geo, s, moe, a8);
         default: break;
     }
     return cudaErrorNotSupported;
 }
 
 template <int BITS, bool BF16X>
-cudaError_t launch_bs(const MatmulParams& p, const KGeom& geo, cudaStream_t s, const MoeKs* moe) {
+cudaError_t launch_bs(const MatmulParams& p, const KGeom& geo, cudaStream_t s, const MoeKs* moe, bool a8) {
     constexpr int CH = chunk_steps(BITS);
     switch (p.L.bs) {
         case 16:
-            if constexpr (CH <= 16) return launch_sdt<BITS, BF16X, 0>(p, geo, s, moe);
+            if constexpr (CH <= 16) return launch_sdt<BITS, BF16X, 0>(p, geo, s, moe, a8);
             break;
-        case 32: return launch_sdt<BITS, BF16X, 1>(p, geo, s, moe);
-        case 64: return launch_sdt<BITS, BF16X, 2>(p, geo, s, moe);
-        case 128: return launch_sdt<BITS, BF16X, 3>(p, geo, s, moe);
+        case 32: return launch_sdt<BITS, BF16X, 1>(p, geo, s, moe, a8);
+        case 64: return launch_sdt<BITS, BF16X, 2>(p, geo, s, moe, a8);
+        case 128: return launch_sdt<BITS, BF16X, 3>(p, geo, s, moe, a8);
         case 256:
-            if constexpr (CH >= 16) return launch_sdt<BITS, BF16X, 4>(p, geo, s, moe);
+            if constexpr (CH >= 16) return launch_sdt<BITS, BF16X, 4>(p, geo, s, moe, a8);
             break;
         default: break;
     }
     return cudaErrorNotSupported;
 }
 
+// a8: accuracy level 4 with X quantised in the staging (bf16 MMAs whatever X's type; p.M counts the
+// hi / lo rows, twice the activation rows); cudaErrorNotSupported where that mode is not built.
 template <int BITS>
-cudaError_t launch_bits(const MatmulParams& p, const KGeom& geo, cudaStream_t s, const MoeKs* moe = nullptr) {
-    return p.act_dtype == kBF16 ? launch_bs<BITS, true>(p, geo, s, moe) : launch_bs<BITS, false>(p, geo, s, moe);
+cudaError_t launch_bits(const MatmulParams& p, const KGeom& geo, cudaStream_t s, const MoeKs* moe = nullptr,
+                        bool a8 = false) {
+    if (a8) return launch_bs<BITS, true>(p, geo, s, nullptr, true);
+    return p.act_dtype == kBF16 ? launch_bs<BITS, true>(p, geo, s, moe, false)
+                                : launch_bs<BITS, false>(p, geo, s, moe, false);
 }
 
 }  // namespace gks

@@ -3,7 +3,7 @@
 
 namespace mnb {
 cudaError_t launch_gemv_ks_b8(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s,
-                             const gks::MoeKs* moe) {
-    return gks::launch_bits<8>(p, geo, s, moe);
+                             const gks::MoeKs* moe, bool a8) {
+    return gks::launch_bits<8>(p, geo, s, moe, a8);
 }
 }  // namespace mnb

@@ -26,11 +26,11 @@ cudaError_t launch_gemv_stream_b2(const MatmulParams& p, const gstr::SGeom& geo,
 cudaError_t launch_gemv_stream_b4(const MatmulParams& p, const gstr::SGeom& geo, cudaStream_t s);
 cudaError_t launch_gemv_stream_b8(const MatmulParams& p, const gstr::SGeom& geo, cudaStream_t s);
 cudaError_t launch_gemv_ks_b2(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s,
-                             const gks::MoeKs* moe = nullptr);
+                             const gks::MoeKs* moe = nullptr, bool a8 = false);
 cudaError_t launch_gemv_ks_b4(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s,
-                             const gks::MoeKs* moe = nullptr);
+                             const gks::MoeKs* moe = nullptr, bool a8 = false);
 cudaError_t launch_gemv_ks_b8(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s,
-                             const gks::MoeKs* moe = nullptr);
+                             const gks::MoeKs* moe = nullptr, bool a8 = false);
 cudaError_t launch_gemv_xr_b2(const MatmulParams& p, const gxr::XGeom& geo, cudaStream_t s);
 cudaError_t launch_gemv_xr_b4(const MatmulParams& p, const gxr::XGeom& geo, cudaStream_t s);
 cudaError_t launch_gemv_xr_b8(const MatmulParams& p, const gxr::XGeom& geo, cudaStream_t s);

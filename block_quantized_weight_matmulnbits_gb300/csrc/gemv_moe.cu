@@ -15,9 +15,12 @@ cudaError_t launch_gemv_moe_b4(const MatmulParams& p, const gmma::Geom& geo, con
                                unsigned groups, size_t smem_bytes, cudaStream_t s);
 cudaError_t launch_gemv_moe_b8(const MatmulParams& p, const gmma::Geom& geo, const gmoe::MoeArgs& g,
                                unsigned groups, size_t smem_bytes, cudaStream_t s);
-cudaError_t launch_gemv_ks_b2(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe);
-cudaError_t launch_gemv_ks_b4(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe);
-cudaError_t launch_gemv_ks_b8(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe);
+cudaError_t launch_gemv_ks_b2(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe,
+                              bool a8 = false);
+cudaError_t launch_gemv_ks_b4(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe,
+                              bool a8 = false);
+cudaError_t launch_gemv_ks_b8(const MatmulParams& p, const gks::KGeom& geo, cudaStream_t s, const gks::MoeKs* moe,
+                              bool a8 = false);
 
 }  // namespace mnb
 

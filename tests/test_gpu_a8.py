@@ -127,6 +127,18 @@ def test_matmul_a8(G, mnb, oracle_mod, monkeypatch, M, bits, bs, dt, asym, N, K,
     G.assert_within(P.y64(y), ref, mag, w.out_dtype, f"a8 {w.name}")
 
 
+@pytest.mark.parametrize("M,bits,bs,dt,asym,N,K", [c for c in A8_CASES if c[0] <= 4 and 32 <= c[2] <= 256])
+def test_matmul_a8_fused_quantisation_bit_identical(G, mnb, monkeypatch, M, bits, bs, dt, asym, N, K):
+    """The one-launch form (X quantised while the GEMV stages it) gives the bits of the two-launch form
+    (quantised hi / lo rows through the workspace, MNB_A8_HILO=2)."""
+    w = _w(M, N, K, bits, bs, dt, asym, 40 + M + bits + bs)
+    P = G.Problem(w)
+    y1 = _run_a8(G, mnb, P).clone()
+    monkeypatch.setenv("MNB_A8_HILO", "2")
+    y2 = _run_a8(G, mnb, P)
+    assert torch.equal(y1.view(torch.uint8), y2.view(torch.uint8))
+
+
 def test_matmul_a8_bias_and_pdl(G, mnb, oracle_mod):
     w = _w(4, 111, 2048, 4, 32, (BF16, F16, BF16), True, 50)
     P = G.Problem(w)
