@@ -372,14 +372,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
         *rt_e = R - k * (int)L.NT;
         return k;
     };
-    // grouped: warp w takes whole row tiles w, w + kW, ... (every chunk in order), so a row's
-    // sum stays in one warp's registers and is stored when the row tile ends
+    // grouped: warp w takes whole row tiles w, w + kW, ... below qW (every chunk in order), so a
+    // row's sum stays in one warp's registers and is stored when the row tile ends; the last
+    // nrt - qW (< kW) row tiles are split by chunks over all warps (item j = (row tile - qW) * KC +
+    // chunk, warp w takes j = w, w + kW, ...), their partials summed at the end, so every warp gets
+    // the same number of items to within one (geo.red_bytes == 0: whole row tiles only)
+    const int qW = MOE && geo.red_bytes > 0 ? (nrt / kW) * kW : nrt;
+    const int pb_rt = qW + warp / KC, pb_c = warp % KC;  // this warp's first split item
     auto valid = [&](const Cursor& it) { return MOE ? it.rt < nrt : it.i < n_items; };
     auto advance = [&](Cursor& it) {
         if constexpr (MOE) {
-            if (++it.c == KC) {
-                it.c = 0;
-                it.rt += kW;
+            if (it.rt < qW) {
+                if (++it.c == KC) {
+                    it.c = 0;
+                    it.rt += kW;
+                }
+                if (it.rt >= qW) it = Cursor{warp, pb_rt, pb_c};
+            } else {
+                it.advance(KC, q16, r16);
             }
         } else {
             it.advance(KC, q16, r16);
@@ -418,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     //         wait), X staged in B-fragment order, then the second item: X
     //         queues behind one item of weights, not two ----
     It buf[2];
-    Cursor cur = MOE ? Cursor{0, warp, 0} : Cursor{warp, 0, warp};
+    Cursor cur = !MOE ? Cursor{warp, 0, warp} : warp < qW ? Cursor{0, warp, 0} : Cursor{warp, pb_rt, pb_c};
     while (cur.c >= KC) {  // at most kW - 1 times
         cur.c -= KC;
         ++cur.rt;
@@ -428,6 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     load(buf[0], cur);
     if constexpr (!MOE)
         for (int o = tid; o < nrt * kW * 16 * M; o += kThreads) red[o] = 0.f;
+    else
+        for (int o = tid; o < (nrt - qW) * kW * 16 * M; o += kThreads) red[o] = 0.f;
     const int pairs = (int)(L.K / 32);
     for (int o = tid; o < pairs * 4; o += kThreads) xs[(size_t)M * geo.xrow + o] = make_uint4(0, 0, 0, 0);
     if (pdl) {
@@ -539,6 +551,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     float y[4] = {0.f, 0.f, 0.f, 0.f};
     const float bias_none = 0.f;
     auto flush = [&](int rt_l) {
+        if (MOE && rt_l >= qW) {  // a split row tile: this warp's partial, summed at the end
+            float* r = red + (size_t)((rt_l - qW) * kW + warp) * 16 * M;
+            const int m0 = 2 * t, m1 = 2 * t + 1;
+            if (m0 < M) {
+                r[m0 * 16 + g] = y[0];
+                r[m0 * 16 + g + 8] = y[2];
+            }
+            if (m1 < M) {
+                r[m1 * 16 + g] = y[1];
+                r[m1 * 16 + g + 8] = y[3];
+            }
+            y[0] = y[1] = y[2] = y[3] = 0.f;
+            return;
+        }
         if constexpr (MOE) {  // the row tile's sums are complete: store them (bias added here)
             int rt_e;
             const int k = expert_of(rt_l, &rt_e);
@@ -601,7 +627,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
         while (step(buf[0]) && step(buf[1])) {
         }
     }
-    if constexpr (MOE) {  // rows already stored
+    if constexpr (MOE) {  // whole row tiles already stored; the split ones: their 16 warps' partials
+        if (nrt > qW) {
+            __syncthreads();
+            const float inv_mp = 1.f / (float)M;
+            for (int o = tid; o < (nrt - qW) * 16 * M; o += kThreads) {
+                const int row = o & 15, q = o >> 4;
+                const int rr = __float2int_rz(((float)q + 0.5f) * inv_mp);  // q < 2^16: exact
+                const int m = q - rr * M;
+                const float* src = red + (size_t)rr * kW * 16 * M + m * 16 + row;
+                float t8[kW / 2];
+#pragma unroll
+                for (int w2 = 0; w2 < kW / 2; ++w2)
+                    t8[w2] = src[(size_t)(2 * w2) * 16 * M] + src[(size_t)(2 * w2 + 1) * 16 * M];
+#pragma unroll
+                for (int h = kW / 4; h >= 1; h >>= 1) {
+#pragma unroll
+                    for (int w2 = 0; w2 < h; ++w2) t8[w2] = t8[2 * w2] + t8[2 * w2 + 1];
+                }
+                int rt_e;
+                const int k = expert_of(qW + rr, &rt_e);
+                const int yr = moe_yrow[k * kMoeMaxPairs + m];
+                const int64_t n = (int64_t)rt_e * 16 + row;
+                if (yr >= 0 && n < L.N) {
+                    const float b = p.bias ? load_f32(p.bias, n, p.bias_dtype) : 0.f;
+                    store_f32(p.y, (int64_t)yr * L.N + n, t8[0] + b, p.out_dtype);
+                }
+            }
+        }
         if (blockIdx.x == 0 && tid == 0)
             for (int k = 0; k < n_active; ++k)
                 verify_header(static_cast<const uint8_t*>(p.packed_hdr) + (size_t)moe_ak[k] * moe.expert_bytes, L, p.status);

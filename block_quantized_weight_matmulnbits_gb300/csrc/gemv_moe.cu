@@ -98,8 +98,15 @@ mnb_status mnb_matmul_grouped(const void* x, const int32_t* ids, const void* pac
         if (fits && q.L.NT < 65536 && u_max * (sms + 1) < (int64_t)1 << 31) {
             kg.G = (int)(u_max < sms ? u_max : sms);
             kg.max_rt = (int)((u_max + kg.G - 1) / kg.G);
-            kg.red_bytes = 0;  // grouped: each warp stores its whole row tiles' sums itself
-            kg.total_bytes = kg.x_bytes;
+            // grouped: each warp stores its whole row tiles' sums itself; the CTA's last (at most
+            // kW - 1) row tiles are split over all warps, their partials in shared memory
+            const int64_t rem_cap = kg.max_rt < gks::kW - 1 ? kg.max_rt : gks::kW - 1;
+            kg.red_bytes = (size_t)rem_cap * gks::kW * 16 * (size_t)pairs * 4;
+            kg.total_bytes = kg.x_bytes + kg.red_bytes;
+            if (kg.total_bytes > device_info().smem_optin) {  // whole row tiles only
+                kg.red_bytes = 0;
+                kg.total_bytes = kg.x_bytes;
+            }
             fits = kg.total_bytes <= device_info().smem_optin;
         } else {
             fits = false;
