@@ -367,6 +367,8 @@ MNB_API mnb_status mnb_matmul_fp_ex(const void* x, const void* packed, const voi
  *   MNB_GEMV_STAGE_BUFS, MNB_GEMV_MAX_SLOTS  ring shape of the f32 GEMV
  *   MNB_A8_HILO=0          accuracy level 4 with M <= 4: the int8 dp4a GEMV
  *                          instead of hi / lo bf16 activation rows
+ *   MNB_A8_HILO=2          the same with the hi / lo rows written to the
+ *                          workspace by a separate quantiser (same bits)
  *   MNB_FP_KERNEL=generic  FP8 / NVFP4: the exact generic kernel
  *   MNB_FP_KERNEL=lut      NVFP4 decode: the CUDA-core table GEMV instead
  *                          of the tensor-core one
