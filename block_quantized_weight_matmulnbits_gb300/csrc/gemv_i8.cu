@@ -75,13 +75,12 @@ __global__ void __launch_bounds__(256) quant_act_hilo_kernel(const void* x, int 
 // rounded to tf32 (f32 containers, rows Kpad long, zero past K), the
 // activation the GEMM's tf32 MMA multiplies.  Codes and scales are those of
 // quant_act_kernel (same operations on the same values).
-__global__ void __launch_bounds__(256) quant_act_tf32_kernel(const void* x, int dt, float* xq, int64_t M, Layout L,
-                                                             int64_t lanes_per_row) {
+__global__ void __launch_bounds__(256) quant_act_tf32_kernel(const void* x, int dt, float* xq, int64_t M, Layout L) {
     griddep_wait();
     griddep_launch_dependents();
-    const int64_t gl = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // global lane
-    const int64_t m = gl / lanes_per_row;
-    const int64_t k0 = (gl - m * lanes_per_row) * 8;
+    // grid (lane blocks of a row, rows, row groups of 65535): no division for the lane's row and depth
+    const int64_t m = (int64_t)blockIdx.z * 65535 + blockIdx.y;
+    const int64_t k0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
     const bool live = m < M && k0 < L.Kpad;  // lanes past the row still join the shuffles
     float v[8];
     const int64_t xrow = m * L.K;
@@ -165,12 +164,13 @@ bool gemv_i8_supported(const MatmulParams& p) {
 // xq == nullptr: int8 codes and scales (warp per block); else tf32 activations (thread per block).
 static cudaError_t quant_launch(const void* x, int act_dtype, int8_t* qa, float* xq, float* sa, int64_t M,
                                 const Layout& L, bool pdl, cudaStream_t s) {
-    // tf32: lanes of 8 depths, a row rounded up to whole warps (a block's lanes never straddle rows)
-    const int64_t lanes_per_row = (L.Kpad / 8 + 31) / 32 * 32;
-    const int64_t blocks = xq ? (M * lanes_per_row + 255) / 256 : (M * L.KB + 7) / 8;
-    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    // tf32: lanes of 8 depths, grid (blocks of 256 lanes along the row, rows): a block never straddles rows
+    const int64_t row_blocks = (L.Kpad / 8 + 255) / 256;
+    const int64_t blocks = xq ? row_blocks : (M * L.KB + 7) / 8;
+    const int64_t ry = M < 65535 ? M : 65535, rz = (M + 65534) / 65535;
+    if (blocks > 0x7FFFFFFF || rz > 65535) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.gridDim = xq ? dim3((unsigned)row_blocks, (unsigned)ry, (unsigned)rz) : dim3((unsigned)blocks);
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
@@ -179,7 +179,7 @@ static cudaError_t quant_launch(const void* x, int act_dtype, int8_t* qa, float*
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if (xq) return cudaLaunchKernelEx(&cfg, gi8::quant_act_tf32_kernel, x, act_dtype, xq, M, L, lanes_per_row);
+    if (xq) return cudaLaunchKernelEx(&cfg, gi8::quant_act_tf32_kernel, x, act_dtype, xq, M, L);
     return cudaLaunchKernelEx(&cfg, gi8::quant_act_kernel, x, act_dtype, qa, sa, M, L);
 }
 
