@@ -436,11 +436,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     Cursor nxt = cur;
     advance(nxt);
     load(buf[0], cur);
-    if constexpr (!MOE)
-        for (int o = tid; o < nrt * kW * 16 * M; o += kThreads) red[o] = 0.f;
-    else
-        for (int o = tid; o < (nrt - qW) * kW * 16 * M; o += kThreads) red[o] = 0.f;
     const int pairs = (int)(L.K / 32);
+    // one K-chunk per warp (KC == kW) and one staging pass (K / 8 == kThreads): warp w stages
+    // exactly the X entries of its own chunk (entry r = thread r) and flushes every (row tile,
+    // warp) slot of the partials, so it needs neither a CTA barrier before its items nor zeroed
+    // partials
+    const bool wlocal = !MOE && KC == kW && pairs * 4 == kThreads;
+    if constexpr (!MOE) {
+        if (!wlocal)
+            for (int o = tid; o < nrt * kW * 16 * M; o += kThreads) red[o] = 0.f;
+    } else {
+        for (int o = tid; o < (nrt - qW) * kW * 16 * M; o += kThreads) red[o] = 0.f;
+    }
     for (int o = tid; o < pairs * 4; o += kThreads) xs[(size_t)M * geo.xrow + o] = make_uint4(0, 0, 0, 0);
     if (pdl) {
         griddep_wait();               // X (and Y) may belong to the previous kernel on the stream
@@ -544,7 +551,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
         }
     }
     load(buf[1], nxt);
-    __syncthreads();
+    if (wlocal) __syncwarp();
+    else __syncthreads();
 
     // ---- 2. items, two buffers: compute one while the next is in flight ----
     const uint32_t xa_lane = smem_u32(xs + (size_t)(g < M ? g : M) * geo.xrow + t);
