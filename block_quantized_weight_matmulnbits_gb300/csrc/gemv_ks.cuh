@@ -427,7 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     // ---- 1. this warp's first item (constant data: before the dependency
     //         wait), X staged in B-fragment order, then the second item: X
     //         queues behind one item of weights, not two ----
-    It buf[2];
+    // items in flight per warp: 3 for 8-bit codes in blocks of 32 or more (plain calls: registers
+    // allow a third buffer, and the loop is bound by the bytes in flight, not by issue), else 2
+    constexpr int DEPTH = (BITS == 8 && SPB_LOG >= 1 && !MOE && !A8) ? 3 : 2;
+    It buf[DEPTH];
     Cursor cur = !MOE ? Cursor{warp, 0, warp} : warp < qW ? Cursor{0, warp, 0} : Cursor{warp, pb_rt, pb_c};
     while (cur.c >= KC) {  // at most kW - 1 times
         cur.c -= KC;
@@ -435,6 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
     }
     Cursor nxt = cur;
     advance(nxt);
+    Cursor nxt2 = nxt;  // DEPTH 3: the item after nxt
+    if constexpr (DEPTH == 3) advance(nxt2);
     load(buf[0], cur);
     const int pairs = (int)(L.K / 32);
     // one K-chunk per warp (KC == kW) and one staging pass (K / 8 == kThreads): warp w stages
@@ -551,6 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
         }
     }
     load(buf[1], nxt);
+    if constexpr (DEPTH == 3) load(buf[2], nxt2);
     if (wlocal) __syncwarp();
     else __syncthreads();
 
@@ -610,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
         }
         y[0] = y[1] = y[2] = y[3] = 0.f;
     };
-    // step: compute `cur` from b, refill b with the item after `nxt`, move on
+    // step: compute `cur` from b, refill b with the item DEPTH after it, move on
     auto step = [&](It& b) {
         uint32_t xa = xa_lane;
         if constexpr (MOE) {  // this item's expert: its columns' X rows
@@ -623,16 +629,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
             xa = cc_xa;
         }
         b.template compute<M1>(xa + (uint32_t)cur.c * (uint32_t)(CH / 2) * 64u, y);
-        Cursor after = nxt;
+        Cursor after = DEPTH == 3 ? nxt2 : nxt;
         advance(after);
         load(b, after);
         if (!valid(nxt) || nxt.rt != cur.rt) flush(cur.rt);
         cur = nxt;
-        nxt = after;
+        if constexpr (DEPTH == 3) {
+            nxt = nxt2;
+            nxt2 = after;
+        } else {
+            nxt = after;
+        }
         return valid(cur);
     };
     if (valid(cur)) {
-        while (step(buf[0]) && step(buf[1])) {
+        if constexpr (DEPTH == 3) {
+            while (step(buf[0]) && step(buf[1]) && step(buf[2])) {
+            }
+        } else {
+            while (step(buf[0]) && step(buf[1])) {
+            }
         }
     }
     if constexpr (MOE) {  // whole row tiles already stored; the split ones: their 16 warps' partials
