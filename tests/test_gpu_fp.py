@@ -255,6 +255,26 @@ def test_fp_decode_gemv(G, monkeypatch, M, N, K, act, out, fmt):
         G.assert_within(y3, ref, mag, out, f"fp lut fmt={fmt} {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K,offset", [(4, 64, 256, 0), (1, 4096, 512, 1), (3, 48, 1024, 3)])
+def test_nvfp4_decode_gemv_scale_staging_paths(G, M, N, K, offset):
+    """The tensor-core NVFP4 GEMV's two block-scale staging paths: 16 codes per load (N % 16 == 0 and a 16-byte
+    aligned scale array) and one code per load (a scale array starting `offset` bytes into an allocation), with one
+    K-chunk per row tile (K = 256) among the shapes; both against the oracle."""
+    rng = np.random.default_rng(4242 + N + K + offset)
+    x = rng.standard_normal((M, K))
+    xs = wl.to_storage(x, BF16)
+    w4 = rng.integers(0, 16, size=(K, N)).astype(np.uint8)
+    s8 = rng.choice([c for c in range(256) if (c & 0x7F) != 0x7F], size=(K // 16, N)).astype(np.uint8)
+    gs = float(np.float32(0.0517))
+    packed = _pack(G, _nibbles(w4), N, K, mnb.MNB_WF_NVFP4)
+    buf = torch.zeros(s8.size + 16, dtype=torch.uint8, device="cuda")
+    st = buf[offset:offset + s8.size]
+    st.copy_(torch.from_numpy(s8.ravel()).cuda())
+    y = _run(G, xs, BF16, packed, st, gs, M, N, K, mnb.MNB_WF_NVFP4, F32)
+    ref, mag = oracle.matmul_nvfp4(wl.widen_f64(xs, BF16), _nibbles(w4), s8, gs, K, N)
+    G.assert_within(y, ref, mag, F32, f"nvfp4 gemv staging offset={offset} {M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("act", [BF16, F16])
 def test_nvfp4_decode_gemv_every_nibble_and_scale_code(G, act):
     """The tensor-core NVFP4 GEMV on one-hot rows: every E2M1 nibble (the subnormal 0.5 and both zeros
