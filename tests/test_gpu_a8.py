@@ -139,6 +139,28 @@ def test_matmul_a8_fused_quantisation_bit_identical(G, mnb, monkeypatch, M, bits
     assert torch.equal(y1.view(torch.uint8), y2.view(torch.uint8))
 
 
+@pytest.mark.parametrize("act", [F32, BF16])
+def test_matmul_a8_fused_ties_and_zero_block(G, mnb, oracle_mod, monkeypatch, act):
+    """The one-launch form on exact quantisation ties (amax = 127 gives s_a = 1, so +-2.5 and +-3.5 round away
+    from zero) and an all-zero block (s_a = 0, zero codes): the bits of the two-launch form and the oracle's
+    integer result within the bound."""
+    M, N, K, bs = 2, 64, 512, 32
+    w = _w(M, N, K, 4, bs, (act, F16, F32), True, 77)
+    d = wl.generate(w)
+    x = wl.widen_f64(d["x"], act).copy()
+    x[:, :8] = [127.0, 2.5, -2.5, 3.5, -3.5, 0.5, -0.5, 126.5]
+    x[:, 32:64] = 0.0  # block 1: all zero
+    x[1, 64:96] = -x[1, 64:96]
+    d["x"] = wl.to_storage(x, act)
+    P = G.Problem(w, data=d)
+    y1 = _run_a8(G, mnb, P).clone()
+    monkeypatch.setenv("MNB_A8_HILO", "2")
+    y2 = _run_a8(G, mnb, P)
+    assert torch.equal(y1.view(torch.uint8), y2.view(torch.uint8))
+    ref, mag = _oracle_a8(oracle_mod, P)
+    G.assert_within(P.y64(y1), ref, mag, w.out_dtype, "a8 fused ties")
+
+
 def test_matmul_a8_bias_and_pdl(G, mnb, oracle_mod):
     w = _w(4, 111, 2048, 4, 32, (BF16, F16, BF16), True, 50)
     P = G.Problem(w)
