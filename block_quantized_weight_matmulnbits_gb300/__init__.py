@@ -18,6 +18,7 @@ MNB_OK, MNB_ERR_INVALID_ARG, MNB_ERR_UNSUPPORTED, MNB_ERR_CUDA, MNB_ERR_NO_MEM, 
     MNB_ERR_LAYOUT_MISMATCH = range(7)
 MNB_F32, MNB_F16, MNB_BF16 = 0, 1, 2
 MNB_FLAG_PDL = 1
+MNB_FLAG_KPERM = 2
 MNB_WF_E4M3, MNB_WF_E5M2, MNB_WF_NVFP4 = 1, 2, 3
 KERNELS = {"auto": 0, "gemv": 1, "gemv_mma": 2, "gemm_tc": 3, "generic": 4, "gemv_i8": 5}
 KERNEL_NAMES = {v: k for k, v in KERNELS.items()}
@@ -28,7 +29,7 @@ EXPORTS = [
     "mnb_matmul_ex", "mnb_workspace_size", "mnb_quantize_activations", "mnb_select_kernel",
     "mnb_get_device_error", "mnb_status_string", "mnb_kernel_name", "mnb_abi_version", "mnb_matmul_a8_static",
     "mnb_matmul_host_io", "mnb_matmul_grouped", "mnb_fp_packed_size", "mnb_pack_fp_weights", "mnb_matmul_fp",
-    "mnb_matmul_fp_ex",
+    "mnb_matmul_fp_ex", "mnb_packed_size_gidx", "mnb_pack_weights_gidx",
 ]
 MNB_A8_STATIC_SCRATCH_BYTES = 1 << 20
 MNB_HOST_IO_X_BYTES = 8 << 20
@@ -72,6 +73,8 @@ def load(build: bool = True):
         sig = {
             "mnb_packed_size": (sz, [i64, i64, ci, ci]),
             "mnb_pack_weights": (ci, [vp, vp, sz, i64, i64, ci, ci, vp]),
+            "mnb_packed_size_gidx": (sz, [i64, i64, ci, ci]),
+            "mnb_pack_weights_gidx": (ci, [vp, vp, vp, sz, i64, i64, ci, ci, vp]),
             "mnb_unpack_codes": (ci, [vp, vp, i64, i64, ci, ci, vp]),
             "mnb_dequantize": (ci, [vp, vp, vp, vp, i64, i64, ci, ci, ci, vp]),
             "mnb_matmul": (ci, [vp, vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, ci, ci, vp]),
@@ -140,6 +143,18 @@ def mnb_packed_size(N, K, bits, block_size) -> int:
 def mnb_pack_weights(b_ort, packed_b, N, K, bits, block_size, stream=None):
     _check(load().mnb_pack_weights(_ptr(b_ort), _ptr(packed_b), packed_b.numel() * packed_b.element_size(),
                                    N, K, bits, block_size, _stream(stream)), "mnb_pack_weights")
+
+
+def mnb_packed_size_gidx(N, K, bits, block_size) -> int:
+    return load().mnb_packed_size_gidx(N, K, bits, block_size)
+
+
+def mnb_pack_weights_gidx(b_ort, g_idx, packed_b, N, K, bits, block_size, stream=None):
+    """Act-order pack: depths sorted by their g_idx block, the permutation stored in the buffer
+    (use it with flags=MNB_FLAG_KPERM and no g_idx)."""
+    _check(load().mnb_pack_weights_gidx(_ptr(b_ort), _ptr(g_idx), _ptr(packed_b),
+                                        packed_b.numel() * packed_b.element_size(), N, K, bits, block_size,
+                                        _stream(stream)), "mnb_pack_weights_gidx")
 
 
 def mnb_unpack_codes(packed_b, b_ort, N, K, bits, block_size, stream=None):

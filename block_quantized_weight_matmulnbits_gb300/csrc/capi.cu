@@ -225,6 +225,25 @@ size_t mnb_packed_size(int64_t N, int64_t K, int bits, int block_size) {
     return L.total_bytes();
 }
 
+size_t mnb_packed_size_gidx(int64_t N, int64_t K, int bits, int block_size) {
+    if (!valid_shape(N, K, bits, block_size)) return 0;
+    Layout L;
+    L.init(N, K, bits, block_size);
+    return L.total_bytes() + kperm_bytes(L);
+}
+
+mnb_status mnb_pack_weights_gidx(const uint8_t* b_ort, const int32_t* g_idx, void* packed_b, size_t packed_bytes,
+                                 int64_t N, int64_t K, int bits, int block_size, mnb_stream_t stream) {
+    if (!valid_shape(N, K, bits, block_size) || !b_ort || !g_idx || !packed_b) return MNB_ERR_INVALID_ARG;
+    if (!aligned(packed_b, 256) || !aligned(g_idx, 4)) return MNB_ERR_INVALID_ARG;
+    Layout L;
+    L.init(N, K, bits, block_size);
+    if (packed_bytes < L.total_bytes() + kperm_bytes(L)) return MNB_ERR_NO_MEM;
+    if (!per_device()) return from_cuda(cudaGetLastError());
+    if (inject_launch_failure()) return MNB_ERR_CUDA;
+    return from_cuda(launch_pack_gidx(b_ort, g_idx, static_cast<uint8_t*>(packed_b), L, (cudaStream_t)stream));
+}
+
 mnb_status mnb_pack_weights(const uint8_t* b_ort, void* packed_b, size_t packed_bytes, int64_t N, int64_t K,
                             int bits, int block_size, mnb_stream_t stream) {
     if (!valid_shape(N, K, bits, block_size) || !b_ort || !packed_b) return MNB_ERR_INVALID_ARG;
@@ -387,6 +406,32 @@ mnb_status mnb_matmul_ex(const mnb_matmul_args* a) {
     p.workspace_bytes = a->workspace_bytes;
     p.flags = a->flags;
     wait_limits(&p.wait_limit, &p.wait_hint_ns);
+
+    if (a->flags & kFlagKPerm) {
+        // act-order pack: the buffer's own permutation replaces g_idx; the K-chunk decode GEMV
+        // (X gathered while it is staged) or the generic kernel
+        if (a->g_idx) return MNB_ERR_INVALID_ARG;
+        if (a->accuracy_level == 4) return MNB_ERR_UNSUPPORTED;
+        p.kperm = reinterpret_cast<const int32_t*>(p.packed + p.L.data_bytes());
+        mnb_kernel kk = a->kernel;
+        if (kk == MNB_KERNEL_AUTO) kk = gemv_ks_kperm_supported(p) ? MNB_KERNEL_GEMV_MMA : MNB_KERNEL_GENERIC;
+        cudaError_t ek;
+        if (kk == MNB_KERNEL_GEMV_MMA) {
+            if (!gemv_ks_kperm_supported(p)) return MNB_ERR_UNSUPPORTED;
+            if (inject_launch_failure()) return MNB_ERR_CUDA;
+            ek = launch_gemv_ks_kperm(p, (cudaStream_t)a->stream);
+        } else if (kk == MNB_KERNEL_GENERIC) {
+            if (inject_launch_failure()) return MNB_ERR_CUDA;
+            ek = launch_generic(p, (cudaStream_t)a->stream);
+        } else {
+            return MNB_ERR_UNSUPPORTED;
+        }
+        if (log_enabled())
+            std::fprintf(stderr, "[mnb] matmul M=%lld N=%lld K=%lld bits=%d bs=%d kernel=%s (act-order pack)\n",
+                         (long long)a->M, (long long)a->N, (long long)a->K, a->bits, a->block_size,
+                         mnb_kernel_name(kk));
+        return from_cuda(ek);
+    }
 
     mnb_kernel k = a->kernel;
     if (k == MNB_KERNEL_AUTO && a->accuracy_level == 4) {

@@ -285,9 +285,11 @@ struct Cursor {
 // its hi = RN_bf16(x') and lo = RN_bf16(x' - hi) in rows 2a and 2a + 1: the same
 // operations on the same values as quant_act_hilo_kernel, so the same bits.
 // Needs 32 <= bs <= 256 (a block's bs / 8 staging lanes reduce its max).
-template <int BITS, bool BF16X, int SPB_LOG, int SDT, bool M1, bool MOE, bool A8 = false>
+// KP: act-order pack (p.kperm set): X gathered through the stored permutation while it is staged.
+template <int BITS, bool BF16X, int SPB_LOG, int SDT, bool M1, bool MOE, bool A8 = false, bool KP = false>
 __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KGeom geo, int pdl, MoeKs moe) {
     static_assert(!A8 || (BF16X && !M1 && !MOE), "accuracy level 4 staging: bf16 hi / lo rows");
+    static_assert(!KP || (!MOE && !A8), "act-order pack: plain calls");
     using It = Item<BITS, BF16X, SPB_LOG, SDT>;
     constexpr int CH = It::CH;
     const Layout& L = p.L;
@@ -454,6 +456,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
         for (int o = tid; o < (nrt - qW) * kW * 16 * M; o += kThreads) red[o] = 0.f;
     }
     for (int o = tid; o < pairs * 4; o += kThreads) xs[(size_t)M * geo.xrow + o] = make_uint4(0, 0, 0, 0);
+    // act-order pack: the stored depths of this thread's first staging entry come from these original
+    // depths (constant data, read before the dependency wait)
+    int kk0[KP ? 8 : 1] = {0};
+    if (KP && tid < pairs * 4) {
+        const int j0 = 32 * (tid >> 2) + 2 * (tid & 3);
+#pragma unroll
+        for (int e = 0; e < (KP ? 8 : 1); ++e) kk0[e] = __ldg(p.kperm + j0 + 8 * (e >> 1) + (e & 1));
+    }
     if (pdl) {
         griddep_wait();               // X (and Y) may belong to the previous kernel on the stream
         griddep_launch_dependents();  // after the wait: at most two chained kernels overlap
@@ -540,19 +550,48 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
         for (int r0 = 0; r0 < pairs * 4; r0 += kThreads) {
             const int r = r0 + tid;
             const int P = r >> 2, tt = r & 3;
-            uint4 v[M1 ? 1 : 8];
+            if constexpr (KP) {
+                // act-order pack: stored depth 32P + 2tt + {0, 1, 8, 9, 16, 17, 24, 25} is X's depth kk[e]
+                if (r < pairs * 4) {
+                    int kk[8];
 #pragma unroll
-            for (int m = 0; m < (M1 ? 1 : 8); ++m) {
-                if (m < M && r < pairs * 4) {
-                    // grouped call: row m is pair m = t * S + s: row t of X (or row t * S + s)
-                    const int xr = MOE ? (moe.x_per_slot ? m : m / moe.S) : m;
-                    const uint32_t* src = x32 + (int64_t)xr * kw + P * 16 + tt;
-                    v[m] = make_uint4(__ldg(src), __ldg(src + 4), __ldg(src + 8), __ldg(src + 12));
+                    for (int e = 0; e < 8; ++e) {
+                        const int v = r0 == 0 ? kk0[KP ? e : 0] : __ldg(p.kperm + 32 * P + 2 * tt + 8 * (e >> 1) + (e & 1));
+                        kk[e] = min(max(v, 0), (int)L.K - 1);  // a bad pack's permutation never indexes past X
+                    }
+                    const uint16_t* x16 = static_cast<const uint16_t*>(p.x);
+                    // two rows per round trip (16 gathered values in flight)
+                    for (int m0 = 0; m0 < M; m0 += 2) {
+                        uint32_t hv[2][8];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                hv[h][e] = m0 + h < M ? __ldg(x16 + (int64_t)(m0 + h) * L.K + kk[e]) : 0u;
+                        }
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            if (m0 + h < M)
+                                xs[(size_t)(m0 + h) * geo.xrow + r] =
+                                    make_uint4(hv[h][0] | (hv[h][1] << 16), hv[h][2] | (hv[h][3] << 16),
+                                               hv[h][4] | (hv[h][5] << 16), hv[h][6] | (hv[h][7] << 16));
+                    }
                 }
-            }
+            } else {
+                uint4 v[M1 ? 1 : 8];
 #pragma unroll
-            for (int m = 0; m < (M1 ? 1 : 8); ++m)
-                if (m < M && r < pairs * 4) xs[(size_t)m * geo.xrow + r] = v[m];
+                for (int m = 0; m < (M1 ? 1 : 8); ++m) {
+                    if (m < M && r < pairs * 4) {
+                        // grouped call: row m is pair m = t * S + s: row t of X (or row t * S + s)
+                        const int xr = MOE ? (moe.x_per_slot ? m : m / moe.S) : m;
+                        const uint32_t* src = x32 + (int64_t)xr * kw + P * 16 + tt;
+                        v[m] = make_uint4(__ldg(src), __ldg(src + 4), __ldg(src + 8), __ldg(src + 12));
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < (M1 ? 1 : 8); ++m)
+                    if (m < M && r < pairs * 4) xs[(size_t)m * geo.xrow + r] = v[m];
+            }
         }
     }
     load(buf[1], nxt);
@@ -713,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
             store_f32(p.y, (int64_t)m * L.N + n, v, p.out_dtype);
         }
     }
-    if (blockIdx.x == 0 && tid == 0) verify_header(p.packed_hdr, L, p.status);
+    if (blockIdx.x == 0 && tid == 0) verify_header(p.packed_hdr, L, p.status, kWfInt, KP ? 1 : 0);
 }
 
 template <int BITS, bool BF16X, int SPB_LOG, int SDT>
@@ -726,6 +765,11 @@ cudaError_t launch_k(const MatmulParams& p, const KGeom& geo, cudaStream_t s, co
         if (a8) kern = gemv_ks_kernel<BITS, true, SPB_LOG, SDT, false, false, true>;
     } else {
         if (a8) return cudaErrorNotSupported;
+    }
+    if (p.kperm != nullptr) {
+        if (moe || a8) return cudaErrorNotSupported;
+        kern = p.M == 1 ? gemv_ks_kernel<BITS, BF16X, SPB_LOG, SDT, true, false, false, true>
+                        : gemv_ks_kernel<BITS, BF16X, SPB_LOG, SDT, false, false, false, true>;
     }
     const MoeKs none{};
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.total_bytes);

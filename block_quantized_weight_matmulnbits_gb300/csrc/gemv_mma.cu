@@ -41,15 +41,37 @@ static const char* sched_env() {
 }
 
 // The k-chunk schedule: the default unless another one is forced.
-static bool ks_ok(const MatmulParams& p, gks::KGeom* out) {
-    const char* sc = sched_env();
-    if (sc && std::strcmp(sc, "ks") != 0) return false;
-    if (!sc && std::getenv("MNB_GEMV_PERS")) return false;
+static bool ks_geom(const MatmulParams& p, gks::KGeom* out) {
     if ((reinterpret_cast<uintptr_t>(p.scales) & 15) != 0) return false;
     if (p.zp && (reinterpret_cast<uintptr_t>(p.zp) & 15) != 0) return false;
     if ((reinterpret_cast<uintptr_t>(p.x) & 3) != 0) return false;
     const int sms = device_info().sm_count > 0 ? device_info().sm_count : 148;
     return gks::make_kgeom(p.L, p.M, sms, device_info().smem_optin, p.scale_dtype == kF32 ? 4 : 2, out);
+}
+
+static bool ks_ok(const MatmulParams& p, gks::KGeom* out) {
+    const char* sc = sched_env();
+    if (sc && std::strcmp(sc, "ks") != 0) return false;
+    if (!sc && std::getenv("MNB_GEMV_PERS")) return false;
+    return ks_geom(p, out);
+}
+
+bool gemv_ks_kperm_supported(const MatmulParams& p) {
+    if (p.M < 1 || p.M > 8 || p.g_idx != nullptr) return false;
+    if (p.act_dtype != kBF16 && p.act_dtype != kF16) return false;
+    gks::KGeom kg;
+    return ks_geom(p, &kg);
+}
+
+cudaError_t launch_gemv_ks_kperm(const MatmulParams& p, cudaStream_t s) {
+    gks::KGeom kg;
+    if (!gemv_ks_kperm_supported(p) || !ks_geom(p, &kg)) return cudaErrorNotSupported;
+    switch (p.L.bits) {
+        case 2: return launch_gemv_ks_b2(p, kg, s);
+        case 4: return launch_gemv_ks_b4(p, kg, s);
+        case 8: return launch_gemv_ks_b8(p, kg, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 // The register-X schedule (opt-in with MNB_GEMV_SCHED=xr; measured slower

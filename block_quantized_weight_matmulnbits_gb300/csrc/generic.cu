@@ -1,7 +1,7 @@
 // Generic CUDA-core kernel: any M, any activation / scale / output dtype,
 // optional g_idx and bias.  It is the correctness baseline of the library and
 // the path for shapes the specialised kernels do not take (f32 activations
-// with M > 1, g_idx).  Weights are dequantised into shared memory tile by tile
+// with M > 1, g_idx, act-order packs outside the decode GEMV's shapes).  Weights are dequantised into shared memory tile by tile
 // as w = (f32(q) - f32(zp)) * f32(scale) (onnx-runtime-ep-cpu 0.1.0-dev.5,
 // src/kernels/matmul_nbits.rs, fn dequantize_nbits_value; with g_idx the
 // scale and zero point follow g_idx[k] while the code keeps its block
@@ -36,7 +36,7 @@ __global__ __launch_bounds__(256) void generic_kernel(MatmulParams p) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const int mask = code_mask(L.bits);
     if (tid == 0) bad_gidx = 0;
-    if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) verify_header(p.packed_hdr, L, p.status);
+    if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) verify_header(p.packed_hdr, L, p.status, kWfInt, p.kperm != nullptr);
     __syncthreads();
 
     for (int64_t k0 = 0; k0 < L.K; k0 += TK) {
@@ -47,6 +47,7 @@ __global__ __launch_bounds__(256) void generic_kernel(MatmulParams p) {
             if (n < L.N && k < L.K) {
                 const int64_t bit = L.bit_of(n, k);
                 const int q = (p.packed[bit >> 3] >> (bit & 7)) & mask;
+                // act-order pack: stored depth k is in group k / bs (its X depth is kperm[k], below)
                 const int64_t g = p.g_idx ? (int64_t)p.g_idx[k] : k / L.bs;
                 if (g >= 0 && g < L.KB) {
                     const int z = load_zp(p.zp, L, n, g);
@@ -61,7 +62,12 @@ __global__ __launch_bounds__(256) void generic_kernel(MatmulParams p) {
         for (int i = tid; i < TM * TK; i += 256) {
             const int r = i / TK, c = i % TK;
             const int64_t m = m0 + r, k = k0 + c;
-            xs[r][c] = (m < p.M && k < L.K) ? load_f32(p.x, m * L.K + k, p.act_dtype) : 0.f;
+            int64_t kx = k;
+            if (p.kperm != nullptr && k < L.K) {
+                const int64_t v = p.kperm[k];
+                kx = v < 0 ? 0 : (v >= L.K ? L.K - 1 : v);  // a bad pack's permutation never indexes past X
+            }
+            xs[r][c] = (m < p.M && k < L.K) ? load_f32(p.x, m * L.K + kx, p.act_dtype) : 0.f;
         }
         __syncthreads();
 #pragma unroll 8

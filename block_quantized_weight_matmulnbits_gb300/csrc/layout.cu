@@ -31,8 +31,9 @@ __device__ __forceinline__ int kn_code(const uint8_t* w, const Layout& L, int fm
 // One thread per 32-bit word of tile data.  fmt kWfInt reads ORT codes (the
 // padded depths [K, KB*bs) included); the floating-point formats read the
 // [K, N] source and zero-fill depths past K (a zero code decodes to +0).
+// perm (act-order pack): stored depth j holds the code of depth perm[j].
 __global__ void pack_kernel(const uint8_t* __restrict__ b_ort, uint32_t* __restrict__ out, Layout L,
-                            int64_t words, int fmt) {
+                            int64_t words, int fmt, const int32_t* __restrict__ perm) {
     const int64_t wi = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (wi >= words) return;
     const int64_t tile = wi >> 7;  // 128 words per tile
@@ -45,6 +46,10 @@ __global__ void pack_kernel(const uint8_t* __restrict__ b_ort, uint32_t* __restr
         int64_t n, k;
         L.field_coords(nt, kt, lane, j, f, &n, &k);
         if (fmt == kWfInt) {
+            if (perm != nullptr && k < L.Kpad) {
+                const int64_t src = perm[k];
+                k = src < 0 ? 0 : (src >= L.Kpad ? L.Kpad - 1 : src);  // a bad g_idx sets the status word
+            }
             if (n < L.N && k < L.Kpad) word |= (uint32_t)ort_code(b_ort, L, n, k) << (f * L.bits);
         } else if (n < L.N && k < L.K) {
             word |= (uint32_t)kn_code(b_ort, L, fmt, n, k) << (f * L.bits);
@@ -53,7 +58,7 @@ __global__ void pack_kernel(const uint8_t* __restrict__ b_ort, uint32_t* __restr
     out[wi] = word;
 }
 
-__global__ void header_kernel(uint8_t* hdr, Layout L, int fmt) {
+__global__ void header_kernel(uint8_t* hdr, Layout L, int fmt, int kperm) {
     const int i = threadIdx.x;
     if (i < kHeaderBytes / 4) reinterpret_cast<uint32_t*>(hdr)[i] = 0;
     __syncthreads();
@@ -66,7 +71,40 @@ __global__ void header_kernel(uint8_t* hdr, Layout L, int fmt) {
         h->bits = L.bits;
         h->block_size = L.bs;
         h->format = fmt;
+        h->kperm = kperm;
     }
+}
+
+// Act-order pack: the depths sorted by their g_idx group (stable), so that
+// group g occupies stored depths [g * bs, g * bs + size_g).  One thread per
+// original depth k: its rank among the earlier depths of its group gives its
+// stored position g * bs + rank, and perm[position] = k.  The
+// groups must have the block sizes (bs, the last one K - (KB - 1) * bs), as
+// MatMulNBits' g_idx describes a permutation of whole blocks; a value outside
+// [0, KB) or a group with too many depths sets MNB_ERR_INVALID_ARG in the
+// device status word (so every group then has exactly its size).  Depths
+// [K, Kpad) keep their place.
+__global__ void gidx_perm_kernel(const int32_t* __restrict__ g_idx, int32_t* __restrict__ perm, Layout L,
+                                 int* status) {
+    const int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (k >= L.Kpad) return;
+    if (k >= L.K) {
+        perm[k] = (int32_t)k;
+        return;
+    }
+    const int32_t g = g_idx[k];
+    if (g < 0 || g >= L.KB) {
+        set_status(status, 1 /* MNB_ERR_INVALID_ARG */);
+        return;
+    }
+    int64_t rank = 0;
+    for (int64_t j = 0; j < k; ++j) rank += g_idx[j] == g ? 1 : 0;
+    const int64_t size = L.K - (int64_t)g * L.bs < L.bs ? L.K - (int64_t)g * L.bs : L.bs;
+    if (rank >= size) {
+        set_status(status, 1 /* MNB_ERR_INVALID_ARG */);
+        return;
+    }
+    perm[(int64_t)g * L.bs + rank] = (int32_t)k;
 }
 
 // One thread per ORT byte.
@@ -108,11 +146,23 @@ unsigned blocks_for(int64_t n, int threads) { return (unsigned)((n + threads - 1
 }  // namespace
 
 cudaError_t launch_pack(const uint8_t* b_ort, uint8_t* packed_hdr, const Layout& L, cudaStream_t s, int fmt) {
-    header_kernel<<<1, 64, 0, s>>>(packed_hdr, L, fmt);
+    header_kernel<<<1, 64, 0, s>>>(packed_hdr, L, fmt, 0);
     const int64_t words = (int64_t)(L.data_bytes() / 4);
     if (words > 0)
         pack_kernel<<<blocks_for(words, 256), 256, 0, s>>>(
-            b_ort, reinterpret_cast<uint32_t*>(packed_hdr + kHeaderBytes), L, words, fmt);
+            b_ort, reinterpret_cast<uint32_t*>(packed_hdr + kHeaderBytes), L, words, fmt, nullptr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_gidx(const uint8_t* b_ort, const int32_t* g_idx, uint8_t* packed_hdr, const Layout& L,
+                             cudaStream_t s) {
+    int32_t* perm = reinterpret_cast<int32_t*>(packed_hdr + kHeaderBytes + L.data_bytes());
+    header_kernel<<<1, 64, 0, s>>>(packed_hdr, L, kWfInt, 1);
+    if (L.Kpad > 0) gidx_perm_kernel<<<blocks_for(L.Kpad, 256), 256, 0, s>>>(g_idx, perm, L, device_status_word());
+    const int64_t words = (int64_t)(L.data_bytes() / 4);
+    if (words > 0)
+        pack_kernel<<<blocks_for(words, 256), 256, 0, s>>>(
+            b_ort, reinterpret_cast<uint32_t*>(packed_hdr + kHeaderBytes), L, words, kWfInt, perm);
     return cudaGetLastError();
 }
 

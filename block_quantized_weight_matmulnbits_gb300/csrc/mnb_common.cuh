@@ -52,6 +52,7 @@ struct PackedHeader {
     int32_t bits;
     int32_t block_size;
     int32_t format;  // 0: MatMulNBits integer codes; else a floating-point weight format (WFormat)
+    int32_t kperm;   // 1: depths stored in g_idx group order, the permutation after the tiles (act-order pack)
 };
 
 // Weight formats of a packed buffer.  kWfInt: MatMulNBits codes (ORT source
@@ -271,10 +272,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
 // with the call's shape; a mismatch sets MNB_ERR_LAYOUT_MISMATCH.  Kernels run
 // it from one thread, after their main work, so it costs one 32-byte read.
 __device__ __forceinline__ void verify_header(const void* packed_hdr, const Layout& L, int* status,
-                                              int format = kWfInt) {
+                                              int format = kWfInt, int kperm = 0) {
     const PackedHeader* h = reinterpret_cast<const PackedHeader*>(packed_hdr);
     if (h->magic != kMagic || h->version != kLayoutVersion || h->N != L.N || h->K != L.K || h->bits != L.bits ||
-        h->block_size != L.bs || h->format != format)
+        h->block_size != L.bs || h->format != format || h->kperm != kperm)
         set_status(status, 6 /* MNB_ERR_LAYOUT_MISMATCH */);
 }
 

@@ -18,6 +18,7 @@ struct MatmulParams {
     const void* scales;
     const uint8_t* zp;
     const int32_t* g_idx;
+    const int32_t* kperm;    // act-order pack (MNB_FLAG_KPERM): original depth of each stored depth, or null
     const void* bias;
     void* y;
     int64_t M;
@@ -36,7 +37,8 @@ struct MatmulParams {
 // wait that is not already satisfied run out).
 void wait_limits(uint32_t* limit, uint32_t* hint_ns);
 
-constexpr int kFlagPDL = 1;  // == MNB_FLAG_PDL
+constexpr int kFlagPDL = 1;    // == MNB_FLAG_PDL
+constexpr int kFlagKPerm = 2;  // == MNB_FLAG_KPERM
 
 // A matmul with a floating-point weight format (WFormat kWfE4M3, kWfE5M2,
 // kWfNVFP4): FP8 scales are f32 [N] or null, NVFP4 scales are E4M3 bytes
@@ -80,6 +82,10 @@ cudaError_t launch_gemm_a8(const MatmulParams& p, cudaStream_t s);
 
 cudaError_t launch_pack(const uint8_t* b_ort, uint8_t* packed_hdr, const Layout& L, cudaStream_t s,
                         int fmt = kWfInt);
+// Act-order pack: depths in g_idx group order, the int32 permutation (Kpad entries) after the tiles.
+cudaError_t launch_pack_gidx(const uint8_t* b_ort, const int32_t* g_idx, uint8_t* packed_hdr, const Layout& L,
+                             cudaStream_t s);
+inline size_t kperm_bytes(const Layout& L) { return ((size_t)L.Kpad * 4 + 255) & ~size_t(255); }
 cudaError_t launch_unpack(const uint8_t* packed, uint8_t* b_ort, const Layout& L, cudaStream_t s);
 cudaError_t launch_dequant(const uint8_t* packed, const void* scales, int scale_dtype, const uint8_t* zp,
                            float* w, const Layout& L, cudaStream_t s);
@@ -93,6 +99,9 @@ cudaError_t launch_gemv(const MatmulParams& p, cudaStream_t s);
 
 bool gemv_mma_supported(const MatmulParams& p);
 cudaError_t launch_gemv_mma(const MatmulParams& p, cudaStream_t s);
+// act-order pack (p.kperm set): the K-chunk decode GEMV gathering X through the permutation
+bool gemv_ks_kperm_supported(const MatmulParams& p);
+cudaError_t launch_gemv_ks_kperm(const MatmulParams& p, cudaStream_t s);
 
 bool gemm_tc_supported(const MatmulParams& p);
 cudaError_t launch_gemm_tc(const MatmulParams& p, cudaStream_t s);

@@ -96,6 +96,10 @@ typedef enum mnb_kernel {
  * MNB_KERNEL_GEMV_I8 and the FP8 / NVFP4 decode GEMVs (mnb_matmul_fp_ex);
  * other kernels ignore it. */
 #define MNB_FLAG_PDL 1
+/* MNB_FLAG_KPERM: packed_b comes from mnb_pack_weights_gidx (act-order); the
+ * permutation stored in it replaces g_idx, which must be NULL.  Not with
+ * accuracy_level 4 (MNB_ERR_UNSUPPORTED). */
+#define MNB_FLAG_KPERM 2
 
 /* ---- weight layout (one-time re-tiling) -------------------------------- */
 
@@ -114,6 +118,29 @@ MNB_API size_t mnb_packed_size(int64_t N, int64_t K, int bits, int block_size);
  * onnx-runtime-ep-cpu matmul_nbits.rs (module doc, fn dequantize_nbits_value). */
 MNB_API mnb_status mnb_pack_weights(const uint8_t* b_ort, void* packed_b, size_t packed_bytes,
                             int64_t N, int64_t K, int bits, int block_size, mnb_stream_t stream);
+
+/* Act-order (g_idx) weights.  MatMulNBits' g_idx[k] names the quantisation
+ * block (scale and zero-point column) of depth k while the code keeps its
+ * place (onnx-runtime-ep-cpu matmul_nbits.rs, MatMulNBitsKernel::
+ * dequantize_weight).  mnb_pack_weights_gidx re-tiles B with its depths sorted
+ * by group (stable), so that group g occupies the stored depths of block g,
+ * and stores that permutation (int32, one entry per padded depth) after the
+ * tiles.  A call with MNB_FLAG_KPERM then runs the decode GEMV on it, gathering
+ * X through the permutation (or the generic kernel for other shapes), with no
+ * g_idx argument.
+ *   g_idx   device int32 [K] (4-byte aligned), values in [0, KB), each block
+ *           holding exactly its depths (bs, the last K - (KB - 1) * bs): a
+ *           permutation of whole blocks, as act-order quantisers write it.
+ *           Another g_idx sets MNB_ERR_INVALID_ARG in the device status word
+ *           (the buffer is then unusable); it stays usable with the plain
+ *           mnb_pack_weights and g_idx in mnb_matmul_ex (generic kernel).
+ * The size is mnb_packed_size_gidx(); unpack and dequantize take only buffers
+ * from mnb_pack_weights.  The header records the act-order pack, so a call
+ * whose MNB_FLAG_KPERM does not match it sets MNB_ERR_LAYOUT_MISMATCH. */
+MNB_API size_t mnb_packed_size_gidx(int64_t N, int64_t K, int bits, int block_size);
+MNB_API mnb_status mnb_pack_weights_gidx(const uint8_t* b_ort, const int32_t* g_idx, void* packed_b,
+                                 size_t packed_bytes, int64_t N, int64_t K, int bits, int block_size,
+                                 mnb_stream_t stream);
 
 /* Inverse of mnb_pack_weights: write the ORT-layout bytes of B (device,
  * [N, KB, blob] uint8) back from packed_b.  pack followed by unpack returns

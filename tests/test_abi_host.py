@@ -193,3 +193,19 @@ def _host_io(lib, **kw):
 def test_host_io_rejects_invalid_arguments_on_the_host(lib, kw, want):
     assert _host_io(lib, **kw) == want
     assert lib.mnb_matmul_host_io(None) == mnb.MNB_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("N,K,bits,bs", [(4096, 4096, 4, 32), (77, 1000, 2, 64), (300, 11008, 8, 128), (16, 17, 4, 16)])
+def test_act_order_packed_size(N, K, bits, bs):
+    """The act-order pack adds the permutation, one int32 per padded depth, in whole 256-byte units."""
+    kpad = -(-K // bs) * bs
+    assert mnb.mnb_packed_size_gidx(N, K, bits, bs) == mnb.mnb_packed_size(N, K, bits, bs) + -(-(4 * kpad) // 256) * 256
+    assert mnb.mnb_packed_size_gidx(N, K, 3, bs) == 0
+
+
+def test_act_order_pack_rejects_invalid_before_cuda():
+    """Argument errors of mnb_pack_weights_gidx come back before any CUDA call."""
+    lib = mnb.load()
+    assert lib.mnb_pack_weights_gidx(None, None, None, 0, 16, 64, 4, 32, None) == mnb.MNB_ERR_INVALID_ARG
+    assert lib.mnb_pack_weights_gidx(None, None, None, 0, 16, 64, 5, 32, None) == mnb.MNB_ERR_INVALID_ARG
+
