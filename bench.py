@@ -333,17 +333,31 @@ def run_ours(args):
         ck = clocks.stop()
         return max_over_ranks(ev0.elapsed_time(ev1) / 1e3, dist), ck
 
-    def measure(w: wl.Workload, steps: int, warmup: int, kernel: str, want_e2e: bool, acc: int = 0):
+    def measure(w: wl.Workload, steps: int, warmup: int, kernel: str, want_e2e: bool, acc: int = 0,
+                act_order: bool = False):
         data = wl.generate(w)
         x = to_dev(data["x"], w.act_dtype)
         b = torch.from_numpy(np.ascontiguousarray(data["b"])).cuda()
         s0 = to_dev(data["scales"], w.scale_dtype)
         zp0 = None if data["zp"] is None else torch.from_numpy(np.ascontiguousarray(data["zp"])).cuda()
-        packed = aligned_empty(mnb.mnb_packed_size(w.N, w.K, w.bits, w.bs))
-        mnb.mnb_pack_weights(b, packed, w.N, w.K, w.bits, w.bs)
+        call_flags = flags
+        if act_order:
+            # act-order weights: a seeded g_idx (a permutation of the depths cut into blocks), packed with
+            # the permutation stored in the buffer, run with MNB_FLAG_KPERM
+            order = np.random.default_rng(w.seed + 7).permutation(w.K)
+            g = np.empty(w.K, dtype=np.int32)
+            g[order] = np.arange(w.K, dtype=np.int32) // w.bs
+            packed = aligned_empty(mnb.mnb_packed_size_gidx(w.N, w.K, w.bits, w.bs))
+            mnb.mnb_pack_weights_gidx(b, torch.from_numpy(g).cuda(), packed, w.N, w.K, w.bits, w.bs)
+            call_flags = flags | mnb.MNB_FLAG_KPERM
+        else:
+            packed = aligned_empty(mnb.mnb_packed_size(w.N, w.K, w.bits, w.bs))
+            mnb.mnb_pack_weights(b, packed, w.N, w.K, w.bits, w.bs)
         del b
         chosen = kernel if kernel != "auto" else mnb.mnb_select_kernel(w.M, w.N, w.K, w.bits, w.bs,
                                                                        w.act_dtype, acc)
+        if act_order:
+            chosen = "gemv_ks_kperm"
         ws_bytes = mnb.mnb_workspace_size(w.M, w.N, w.K, w.bits, w.bs, acc)
         ws = aligned_empty(ws_bytes) if ws_bytes else None
         # weight copies so that each step streams from HBM
@@ -361,11 +375,13 @@ def run_ours(args):
         def call(i):
             pb, s, zp = copies[i % R]
             mnb.mnb_matmul_ex(x, pb, s, zp, yb, w.M, w.N, w.K, w.bits, w.bs, w.act_dtype, w.out_dtype,
-                              w.scale_dtype, kernel=kernel, stream=stream, flags=flags, accuracy_level=acc,
+                              w.scale_dtype, kernel=kernel, stream=stream, flags=call_flags, accuracy_level=acc,
                               workspace=ws)
 
         t, ck = replay_timed(call, steps, warmup, stream)
         unit, per_step = metric_of(w)
+        if act_order:
+            per_step += 4 * w.K / 1e9  # the stored permutation, read once per call
         value = whole_job_value(world, steps, per_step, t)
         per_launch_s = t / steps
         # accuracy level 4: activation quantisation + product, except at M <= 4 with 32 <= bs <= 256, where
@@ -378,7 +394,7 @@ def run_ours(args):
             out["roofline"] = {"bound": "hbm", "achieved": per_step / per_launch_s, "peak": peak, "unit": "GB/s",
                                "frac": per_step / per_launch_s / peak,
                                "traffic": traffic_for(f"{chosen}:{w.name}" + (":acc4" if acc == 4 else "")),
-                               "algorithmic_bytes": w.algorithmic_bytes(),
+                               "algorithmic_bytes": w.algorithmic_bytes() + (4 * w.K if act_order else 0),
                                "peak_source": f"{pk_src} hbm_gbs"}
         else:
             peak = pk["bf16_tflops"]
@@ -525,8 +541,8 @@ def run_ours(args):
         "gpu_launches": main["launches"] + main.get("e2e_launches", 0),
     }
 
-    def secondary(key, wk, steps, warmup, acc=0, extra=None):
-        sec, _ = measure(wk, steps, warmup, "auto", False, acc)
+    def secondary(key, wk, steps, warmup, acc=0, extra=None, act_order=False):
+        sec, _ = measure(wk, steps, warmup, "auto", False, acc, act_order=act_order)
         obj = {"workload": wk.name, "value": sec["value"], "unit": sec["unit"], "kernel": sec["kernel"],
                "steps": sec["steps"], "ms_per_step": sec["ms_per_step"], "roofline": sec["roofline"],
                "clocks": sec["clocks"]}
@@ -543,6 +559,8 @@ def run_ours(args):
                   extra={"accuracy_level": 4, "launches_per_step": 1})
         secondary("a8_m512", wl.config(4), max(20, args.steps // 20), max(3, args.warmup // 20), acc=4,
                   extra={"accuracy_level": 4, "launches_per_step": 2})
+        secondary("act_order", w, max(20, args.steps // 4), sw, act_order=True,
+                  extra={"g_idx": "act-order (a seeded permutation of the depths in blocks), MNB_FLAG_KPERM"})
         moe, n = measure_moe(wl.MOE_CONFIGS[0], max(20, args.steps // 10), max(3, args.warmup // 10))
         res["moe"] = moe
         res["gpu_launches"] += n
