@@ -51,6 +51,9 @@ struct KGeom {
     size_t x_bytes, red_bytes, total_bytes;
 };
 
+// Act-order pack: X as given (M rows of K 16-bit values) in shared memory after the partials.
+inline size_t kperm_x_bytes(const Layout& L, int64_t M) { return (size_t)M * (size_t)L.K * 2; }
+
 // k-steps per chunk for a code width: 4 packed tiles.
 __host__ __device__ constexpr int chunk_steps(int bits) { return kTilesPerChunk * (16 / bits); }
 
@@ -545,6 +548,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
         // (x[k0 + 2tt..], x[k0 + 8 + 2tt..], x[k0 + 16 + 2tt..], x[k0 + 24 + 2tt..])
         const uint32_t* x32 = static_cast<const uint32_t*>(p.x);  // K even: rows are 4-byte aligned
         const int64_t kw = L.K / 2;
+        // act-order pack: X is copied as it is (coalesced, 16 bytes a thread) into shared memory after the
+        // partials, and gathered from there through the permutation
+        const uint16_t* xraw = reinterpret_cast<const uint16_t*>(smem + geo.x_bytes + geo.red_bytes);
+        if constexpr (KP) {
+            const uint4* xg = static_cast<const uint4*>(p.x);  // 16-byte aligned rows (K % 8 == 0)
+            uint4* xw = reinterpret_cast<uint4*>(smem + geo.x_bytes + geo.red_bytes);
+            for (int o = tid; o < M * (int)(L.K / 8); o += kThreads) xw[o] = __ldg(xg + o);
+            __syncthreads();
+        }
         // every row's words of a thread are requested before any is stored, so
         // the M rows cost one round trip, not M
         for (int r0 = 0; r0 < pairs * 4; r0 += kThreads) {
@@ -559,15 +571,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ks_kernel(MatmulParams p, KG
                         const int v = r0 == 0 ? kk0[KP ? e : 0] : __ldg(p.kperm + 32 * P + 2 * tt + 8 * (e >> 1) + (e & 1));
                         kk[e] = min(max(v, 0), (int)L.K - 1);  // a bad pack's permutation never indexes past X
                     }
-                    const uint16_t* x16 = static_cast<const uint16_t*>(p.x);
-                    // two rows per round trip (16 gathered values in flight)
                     for (int m0 = 0; m0 < M; m0 += 2) {
                         uint32_t hv[2][8];
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
 #pragma unroll
                             for (int e = 0; e < 8; ++e)
-                                hv[h][e] = m0 + h < M ? __ldg(x16 + (int64_t)(m0 + h) * L.K + kk[e]) : 0u;
+                                hv[h][e] = m0 + h < M ? (uint32_t)xraw[(int64_t)(m0 + h) * L.K + kk[e]] : 0u;
                         }
 #pragma unroll
                         for (int h = 0; h < 2; ++h)
@@ -766,25 +776,27 @@ cudaError_t launch_k(const MatmulParams& p, const KGeom& geo, cudaStream_t s, co
     } else {
         if (a8) return cudaErrorNotSupported;
     }
+    KGeom gk = geo;
     if (p.kperm != nullptr) {
         if (moe || a8) return cudaErrorNotSupported;
         kern = p.M == 1 ? gemv_ks_kernel<BITS, BF16X, SPB_LOG, SDT, true, false, false, true>
                         : gemv_ks_kernel<BITS, BF16X, SPB_LOG, SDT, false, false, false, true>;
+        gk.total_bytes = geo.x_bytes + geo.red_bytes + kperm_x_bytes(p.L, p.M);  // X as given, for the gather
     }
     const MoeKs none{};
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.total_bytes);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gk.total_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)geo.G);
+    cfg.gridDim = dim3((unsigned)gk.G);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = geo.total_bytes;
+    cfg.dynamicSmemBytes = gk.total_bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, p, geo, pdl, moe ? *moe : none);
+    return cudaLaunchKernelEx(&cfg, kern, p, gk, pdl, moe ? *moe : none);
 }
 
 template <int BITS, bool BF16X, int SPB_LOG>

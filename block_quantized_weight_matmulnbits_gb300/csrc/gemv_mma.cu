@@ -59,8 +59,10 @@ static bool ks_ok(const MatmulParams& p, gks::KGeom* out) {
 bool gemv_ks_kperm_supported(const MatmulParams& p) {
     if (p.M < 1 || p.M > 8 || p.g_idx != nullptr) return false;
     if (p.act_dtype != kBF16 && p.act_dtype != kF16) return false;
+    if ((reinterpret_cast<uintptr_t>(p.x) & 15) != 0) return false;  // X copied 16 bytes at a time
     gks::KGeom kg;
-    return ks_geom(p, &kg);
+    if (!ks_geom(p, &kg)) return false;
+    return kg.x_bytes + kg.red_bytes + gks::kperm_x_bytes(p.L, p.M) <= device_info().smem_optin;
 }
 
 cudaError_t launch_gemv_ks_kperm(const MatmulParams& p, cudaStream_t s) {
