@@ -181,3 +181,30 @@ def test_worst_case_grouped(G, mnb, oracle_mod, x_mode):
     ref, mag = oracle_mod.matmul_grouped(wl.widen_f64(x, BF16), ids, np.stack([d["b"] for d in ds]),
                                          wl.widen_f32(s_all, F16), z_all, E, N, K, bits, bs)
     G.assert_within(y.cpu().numpy().astype(np.float64), ref, mag, F32, f"grouped {x_mode}")
+
+
+@pytest.mark.parametrize("x_mode", ["one_hot", "positive"])
+@pytest.mark.parametrize("bits,bs,act,sdt,zpm", [KS_SHAPES[0], KS_SHAPES[2], KS_SHAPES[5], KS_SHAPES[7]])
+@pytest.mark.parametrize("M", [1, 5])
+def test_worst_case_act_order(G, M, bits, bs, act, sdt, zpm, x_mode):
+    """The act-order decode (mnb_pack_weights_gidx + MNB_FLAG_KPERM) on the same inputs, with a seeded act-order
+    g_idx: the scale and zero point of each depth follow g_idx, so one-hot rows read single weights of the page's
+    act-order dequantisation."""
+    import block_quantized_weight_matmulnbits_gb300 as mnb
+    N, K = 150, 3 * (1024 // bits)
+    extra = F32_EXTRA if sdt == F32 else ()
+    data = build(M, N, K, bits, bs, act, sdt, zpm, x_mode, 4600 + M + bits + bs, extra)
+    w = _wl(M, N, K, bits, bs, act, sdt, zpm)
+    P = G.Problem(w, data)
+    order = np.random.default_rng(4700 + K).permutation(K)
+    g = np.empty(K, dtype=np.int32)
+    g[order] = np.arange(K, dtype=np.int32) // bs
+    packed = G.aligned_empty(mnb.mnb_packed_size_gidx(N, K, bits, bs))
+    mnb.mnb_pack_weights_gidx(P.b, torch.from_numpy(g).cuda(), packed, N, K, bits, bs)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    mnb.mnb_matmul_ex(P.x, packed, P.s, P.zp, y, M, N, K, bits, bs, act, F32, sdt, flags=mnb.MNB_FLAG_KPERM)
+    torch.cuda.synchronize()
+    assert mnb.mnb_get_device_error() == mnb.MNB_OK
+    ref, mag = P.oracle_full(g_idx=g)
+    G.assert_within(P.y64(y), ref, mag, F32, f"act-order {x_mode} {w.name}")
+
