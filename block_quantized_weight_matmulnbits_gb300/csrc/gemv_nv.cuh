@@ -95,7 +95,9 @@ __device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t lo, uint32_t hi) {
     const unsigned short pair = (unsigned short)((lo & 0xFFu) | ((hi & 0xFFu) << 8));
     uint32_t h;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(pair));
-    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+    const __half h0 = __ushort_as_half((unsigned short)(h & 0xFFFFu));
+    const __half h1 = __ushort_as_half((unsigned short)(h >> 16));
+    return make_float2(__half2float(h0), __half2float(h1));
 }
 
 template <bool BF16X>
