@@ -29,7 +29,7 @@ EXPORTS = [
     "mnb_matmul_ex", "mnb_workspace_size", "mnb_quantize_activations", "mnb_select_kernel",
     "mnb_get_device_error", "mnb_status_string", "mnb_kernel_name", "mnb_abi_version", "mnb_matmul_a8_static",
     "mnb_matmul_host_io", "mnb_matmul_grouped", "mnb_fp_packed_size", "mnb_pack_fp_weights", "mnb_matmul_fp",
-    "mnb_matmul_fp_ex", "mnb_packed_size_gidx", "mnb_pack_weights_gidx",
+    "mnb_matmul_fp_ex", "mnb_packed_size_gidx", "mnb_pack_weights_gidx", "mnb_workspace_size_ex",
 ]
 MNB_A8_STATIC_SCRATCH_BYTES = 1 << 20
 MNB_HOST_IO_X_BYTES = 8 << 20
@@ -74,6 +74,7 @@ def load(build: bool = True):
             "mnb_packed_size": (sz, [i64, i64, ci, ci]),
             "mnb_pack_weights": (ci, [vp, vp, sz, i64, i64, ci, ci, vp]),
             "mnb_packed_size_gidx": (sz, [i64, i64, ci, ci]),
+            "mnb_workspace_size_ex": (sz, [i64, i64, i64, ci, ci, ci, ci]),
             "mnb_pack_weights_gidx": (ci, [vp, vp, vp, sz, i64, i64, ci, ci, vp]),
             "mnb_unpack_codes": (ci, [vp, vp, i64, i64, ci, ci, vp]),
             "mnb_dequantize": (ci, [vp, vp, vp, vp, i64, i64, ci, ci, ci, vp]),
@@ -240,6 +241,10 @@ def mnb_matmul_fp(x, packed, scales, global_scale, y, M, N, K, fmt, act_dtype, o
         return
     _check(load().mnb_matmul_fp(_ptr(x), _ptr(packed), _ptr(scales), float(global_scale), _ptr(y), M, N, K, fmt,
                                 act_dtype, out_dtype, _stream(stream)), "mnb_matmul_fp")
+
+
+def mnb_workspace_size_ex(M, N, K, bits, block_size, accuracy_level, flags) -> int:
+    return load().mnb_workspace_size_ex(M, N, K, bits, block_size, accuracy_level, flags)
 
 
 def mnb_workspace_size(M, N, K, bits, block_size, accuracy_level) -> int:

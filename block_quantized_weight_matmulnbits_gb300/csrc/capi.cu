@@ -346,6 +346,16 @@ mnb_status mnb_matmul_fp_ex(const void* x, const void* packed, const void* scale
     return from_cuda(fast ? launch_gemv_fp(p, (cudaStream_t)stream) : launch_fp_generic(p, (cudaStream_t)stream));
 }
 
+size_t mnb_workspace_size_ex(int64_t M, int64_t N, int64_t K, int bits, int block_size, int accuracy_level,
+                             int flags) {
+    const size_t base = mnb_workspace_size(M, N, K, bits, block_size, accuracy_level);
+    if (!(flags & kFlagKPerm) || accuracy_level == 4 || !valid_shape(N, K, bits, block_size) || M <= 8) return base;
+    Layout L;
+    L.init(N, K, bits, block_size);
+    const size_t g = kperm_gemm_workspace_bytes(M, L);  // the act-order prefill's X in the pack's order
+    return g > base ? g : base;
+}
+
 size_t mnb_workspace_size(int64_t M, int64_t N, int64_t K, int bits, int block_size, int accuracy_level) {
     if (!valid_shape(N, K, bits, block_size) || M < 0) return 0;
     if (accuracy_level != 4) return 0;
@@ -413,13 +423,33 @@ mnb_status mnb_matmul_ex(const mnb_matmul_args* a) {
         if (a->g_idx) return MNB_ERR_INVALID_ARG;
         if (a->accuracy_level == 4) return MNB_ERR_UNSUPPORTED;
         p.kperm = reinterpret_cast<const int32_t*>(p.packed + p.L.data_bytes());
+        // prefill: X put in the pack's depth order in the workspace, then the tensor-core GEMM
+        const bool gemm_ok = (a->act_dtype == MNB_BF16 || a->act_dtype == MNB_F16) && a->K % 8 == 0 &&
+                             gemm_tc_supported(p);
+        const size_t gneed = kperm_gemm_workspace_bytes(a->M, p.L);
+        const bool ws_ok = a->workspace && a->workspace_bytes >= gneed && aligned(a->workspace, 256);
         mnb_kernel kk = a->kernel;
-        if (kk == MNB_KERNEL_AUTO) kk = gemv_ks_kperm_supported(p) ? MNB_KERNEL_GEMV_MMA : MNB_KERNEL_GENERIC;
+        if (kk == MNB_KERNEL_AUTO)
+            kk = gemv_ks_kperm_supported(p) ? MNB_KERNEL_GEMV_MMA
+                 : (a->M > 8 && gemm_ok && ws_ok) ? MNB_KERNEL_GEMM_TC : MNB_KERNEL_GENERIC;
         cudaError_t ek;
         if (kk == MNB_KERNEL_GEMV_MMA) {
             if (!gemv_ks_kperm_supported(p)) return MNB_ERR_UNSUPPORTED;
             if (inject_launch_failure()) return MNB_ERR_CUDA;
             ek = launch_gemv_ks_kperm(p, (cudaStream_t)a->stream);
+        } else if (kk == MNB_KERNEL_GEMM_TC) {
+            if (!gemm_ok) return MNB_ERR_UNSUPPORTED;
+            if (!a->workspace || a->workspace_bytes < gneed) return MNB_ERR_NO_MEM;
+            if (!aligned(a->workspace, 256)) return MNB_ERR_INVALID_ARG;
+            if (inject_launch_failure()) return MNB_ERR_CUDA;
+            ek = launch_gather_kperm(a->x, p.kperm, a->workspace, a->M, p.L, (a->flags & kFlagPDL) != 0,
+                                     (cudaStream_t)a->stream);
+            if (ek == cudaSuccess) {
+                MatmulParams q = p;
+                q.x = a->workspace;  // X in the pack's depth order; q.kperm stays set for the header check
+                q.flags |= kFlagPDL;  // the GEMM's weight stream overlaps the gather
+                ek = launch_gemm_tc(q, (cudaStream_t)a->stream);
+            }
         } else if (kk == MNB_KERNEL_GENERIC) {
             if (inject_launch_failure()) return MNB_ERR_CUDA;
             ek = launch_generic(p, (cudaStream_t)a->stream);

@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bs_kernel(MatmulParams p, Ge
         tc::fence_after();
         tc::dealloc(tmem, (uint32_t)geo.tmem_cols);
     }
-    if (blockIdx.x == 0 && tid == 0) verify_header(p.packed_hdr, L, p.status);
+    if (blockIdx.x == 0 && tid == 0) verify_header(p.packed_hdr, L, p.status, kWfInt, p.kperm != nullptr ? 1 : 0);
 }
 
 template <int BITS, bool BF16X>

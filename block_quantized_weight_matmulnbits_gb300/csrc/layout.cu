@@ -141,6 +141,29 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ packed, const void* _
     w[i] = __fmul_rn(__fsub_rn((float)q, (float)z), s);
 }
 
+// Act-order prefill: X's depths put in the packed buffer's order, xp[m, j] = x[m, perm[j]] (16-bit
+// activations), so that the tensor-core GEMM reads contiguous quantisation blocks.  One thread per 8
+// stored depths of a row: 16-byte stores, gathered loads (X is a few MB and sits in L2).  A
+// programmatic dependent: X is read after the dependency wait.
+__global__ void gather_kperm_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
+                                    uint16_t* __restrict__ xp, int64_t M, int64_t K) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    const int64_t per_row = K / 8;
+    if (t >= M * per_row) return;
+    const int64_t m = t / per_row, j0 = (t - m * per_row) * 8;
+    uint32_t h[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        int64_t k = perm[j0 + e];
+        k = k < 0 ? 0 : (k >= K ? K - 1 : k);  // a bad pack's permutation never indexes past X
+        h[e] = x[m * K + k];
+    }
+    *reinterpret_cast<uint4*>(xp + m * K + j0) =
+        make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+}
+
 unsigned blocks_for(int64_t n, int threads) { return (unsigned)((n + threads - 1) / threads); }
 
 }  // namespace
@@ -164,6 +187,23 @@ cudaError_t launch_pack_gidx(const uint8_t* b_ort, const int32_t* g_idx, uint8_t
         pack_kernel<<<blocks_for(words, 256), 256, 0, s>>>(
             b_ort, reinterpret_cast<uint32_t*>(packed_hdr + kHeaderBytes), L, words, kWfInt, perm);
     return cudaGetLastError();
+}
+
+cudaError_t launch_gather_kperm(const void* x, const int32_t* perm, void* xp, int64_t M, const Layout& L,
+                                bool pdl, cudaStream_t s) {
+    const int64_t n = M * (L.K / 8);
+    if (n <= 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks_for(n, 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gather_kperm_kernel, static_cast<const uint16_t*>(x), perm,
+                              static_cast<uint16_t*>(xp), M, L.K);
 }
 
 cudaError_t launch_unpack(const uint8_t* packed, uint8_t* b_ort, const Layout& L, cudaStream_t s) {

@@ -86,6 +86,12 @@ cudaError_t launch_pack(const uint8_t* b_ort, uint8_t* packed_hdr, const Layout&
 cudaError_t launch_pack_gidx(const uint8_t* b_ort, const int32_t* g_idx, uint8_t* packed_hdr, const Layout& L,
                              cudaStream_t s);
 inline size_t kperm_bytes(const Layout& L) { return ((size_t)L.Kpad * 4 + 255) & ~size_t(255); }
+// Act-order prefill: X's depths in the pack's order (16-bit activations, K % 8 == 0) into xp [M, K].
+cudaError_t launch_gather_kperm(const void* x, const int32_t* perm, void* xp, int64_t M, const Layout& L,
+                                bool pdl, cudaStream_t s);
+inline size_t kperm_gemm_workspace_bytes(int64_t M, const Layout& L) {
+    return ((size_t)M * (size_t)L.K * 2 + 255) & ~size_t(255);
+}
 cudaError_t launch_unpack(const uint8_t* packed, uint8_t* b_ort, const Layout& L, cudaStream_t s);
 cudaError_t launch_dequant(const uint8_t* packed, const void* scales, int scale_dtype, const uint8_t* zp,
                            float* w, const Layout& L, cudaStream_t s);

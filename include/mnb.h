@@ -126,8 +126,9 @@ MNB_API mnb_status mnb_pack_weights(const uint8_t* b_ort, void* packed_b, size_t
  * by group (stable), so that group g occupies the stored depths of block g,
  * and stores that permutation (int32, one entry per padded depth) after the
  * tiles.  A call with MNB_FLAG_KPERM then runs the decode GEMV on it, gathering
- * X through the permutation (or the generic kernel for other shapes), with no
- * g_idx argument.
+ * X through the permutation (M <= 8), the tensor-core prefill GEMM after a
+ * gather of X into the workspace (M > 8, see mnb_workspace_size_ex), or the
+ * generic kernel for other shapes, with no g_idx argument.
  *   g_idx   device int32 [K] (4-byte aligned), values in [0, KB), each block
  *           holding exactly its depths (bs, the last K - (KB - 1) * bs): a
  *           permutation of whole blocks, as act-order quantisers write it.
@@ -222,6 +223,14 @@ MNB_API mnb_status mnb_matmul_ex(const mnb_matmul_args* args);
 
 /* Scratch bytes mnb_matmul_ex needs for this call (0 for the float path). */
 MNB_API size_t mnb_workspace_size(int64_t M, int64_t N, int64_t K, int bits, int block_size, int accuracy_level);
+
+/* The same for a call with these MNB_FLAG_* flags: with MNB_FLAG_KPERM and
+ * M > 8 the act-order prefill needs X in the pack's depth order,
+ * ceil256(M * K * 2) bytes (bf16 / f16 X).  Given that workspace, such a call
+ * gathers X into it and runs the tensor-core prefill GEMM; without it, the
+ * generic kernel (a forced MNB_KERNEL_GEMM_TC returns MNB_ERR_NO_MEM). */
+MNB_API size_t mnb_workspace_size_ex(int64_t M, int64_t N, int64_t K, int bits, int block_size,
+                             int accuracy_level, int flags);
 
 /* Per-(row, K-block) int8 activation quantisation on its own (the first step
  * of accuracy_level 4): qa device int8 [M, KB*bs] (tail past K zero), sa

@@ -209,3 +209,13 @@ def test_act_order_pack_rejects_invalid_before_cuda():
     assert lib.mnb_pack_weights_gidx(None, None, None, 0, 16, 64, 4, 32, None) == mnb.MNB_ERR_INVALID_ARG
     assert lib.mnb_pack_weights_gidx(None, None, None, 0, 16, 64, 5, 32, None) == mnb.MNB_ERR_INVALID_ARG
 
+
+def test_act_order_workspace_size():
+    """The act-order prefill's workspace: X in the pack's depth order (M * K 16-bit values, whole 256-byte units)
+    for M > 8 with MNB_FLAG_KPERM; otherwise mnb_workspace_size."""
+    assert mnb.mnb_workspace_size_ex(512, 4096, 4096, 4, 32, 0, mnb.MNB_FLAG_KPERM) == 512 * 4096 * 2
+    assert mnb.mnb_workspace_size_ex(17, 100, 1000, 4, 128, 0, mnb.MNB_FLAG_KPERM) == -(-(17 * 1000 * 2) // 256) * 256
+    assert mnb.mnb_workspace_size_ex(8, 4096, 4096, 4, 32, 0, mnb.MNB_FLAG_KPERM) == 0
+    assert mnb.mnb_workspace_size_ex(512, 4096, 4096, 4, 32, 0, 0) == 0
+    assert mnb.mnb_workspace_size_ex(512, 4096, 4096, 4, 32, 4, 0) == mnb.mnb_workspace_size(512, 4096, 4096, 4, 32, 4)
+

@@ -106,7 +106,8 @@ def test_act_order_identity_gidx_is_bit_identical(G, mnb, M, bits, bs, dt, asym,
 
 
 def test_act_order_forced_kernels(G, mnb):
-    """Forced families: the decode GEMV and the generic kernel take an act-order pack; the prefill GEMM does not."""
+    """Forced families: the decode GEMV and the generic kernel take an act-order pack; the prefill GEMM needs the
+    workspace for the gathered X."""
     w = _w(2, 256, 512, 4, 32, (BF16, F16, BF16), True, 1700)
     P = G.Problem(w)
     g = act_order_gidx(512, 32, 5)
@@ -154,3 +155,39 @@ def test_act_order_pack_rejects_bad_gidx(G, mnb, bad):
     assert mnb.mnb_get_device_error() == mnb.MNB_ERR_INVALID_ARG
     _run(mnb, P, packed, mnb.MNB_FLAG_KPERM)  # permutation entries are clamped before use
     assert mnb.mnb_get_device_error() == 0
+
+
+PREFILL_CASES = [
+    # M, bits, bs, (act, scale, out), asym, N, K
+    (64, 4, 32, (BF16, F16, BF16), True, 512, 1024),
+    (200, 2, 64, (BF16, BF16, F32), True, 300, 2048),
+    (33, 8, 128, (F16, F32, F16), True, 250, 1024),
+    (512, 4, 32, (BF16, F16, BF16), False, 256, 4096),
+]
+
+
+@pytest.mark.parametrize("M,bits,bs,dt,asym,N,K", PREFILL_CASES)
+def test_act_order_prefill_on_tensor_cores(G, mnb, M, bits, bs, dt, asym, N, K):
+    """M > 8 with the workspace of mnb_workspace_size_ex: X gathered into the pack's depth order, then the
+    tensor-core prefill GEMM; against the oracle with g_idx. Without the workspace the call takes the generic
+    kernel, and a forced GEMM reports MNB_ERR_NO_MEM."""
+    w = _w(M, N, K, bits, bs, dt, asym, 2100 + M + bits)
+    P = G.Problem(w)
+    g = act_order_gidx(K, bs, 31 + K)
+    packed = _pack_gidx(G, mnb, P, g)
+    need = mnb.mnb_workspace_size_ex(M, N, K, bits, bs, 0, mnb.MNB_FLAG_KPERM)
+    assert need == -(-(M * K * 2) // 256) * 256
+    ws = G.aligned_empty(need)
+    ref, mag = P.oracle_full(g_idx=g)
+    for flags in (mnb.MNB_FLAG_KPERM, mnb.MNB_FLAG_KPERM | mnb.MNB_FLAG_PDL):
+        y = torch.empty((M, N), dtype=wl_torch(w.out_dtype), device="cuda")
+        mnb.mnb_matmul_ex(P.x, packed, P.s, P.zp, y, M, N, K, bits, bs, w.act_dtype, w.out_dtype, w.scale_dtype,
+                          workspace=ws, flags=flags)
+        torch.cuda.synchronize()
+        assert mnb.mnb_get_device_error() == 0
+        G.assert_within(P.y64(y), ref, mag, w.out_dtype, f"act-order prefill {w.name} flags={flags}")
+    y2 = _run(mnb, P, packed, mnb.MNB_FLAG_KPERM)  # no workspace: generic
+    G.assert_within(P.y64(y2), ref, mag, w.out_dtype, f"act-order generic {w.name}")
+    with pytest.raises(mnb.MnbError):
+        _run(mnb, P, packed, mnb.MNB_FLAG_KPERM, kernel="gemm_tc")
+
