@@ -357,8 +357,8 @@ def run_ours(args):
         chosen = kernel if kernel != "auto" else mnb.mnb_select_kernel(w.M, w.N, w.K, w.bits, w.bs,
                                                                        w.act_dtype, acc)
         if act_order:
-            chosen = "gemv_ks_kperm"
-        ws_bytes = mnb.mnb_workspace_size(w.M, w.N, w.K, w.bits, w.bs, acc)
+            chosen = "gemv_ks_kperm" if w.M <= 8 else "gather_kperm+gemm_tc"
+        ws_bytes = mnb.mnb_workspace_size_ex(w.M, w.N, w.K, w.bits, w.bs, acc, call_flags)
         ws = aligned_empty(ws_bytes) if ws_bytes else None
         # weight copies so that each step streams from HBM
         l2 = torch.cuda.get_device_properties(local).L2_cache_size
@@ -380,13 +380,15 @@ def run_ours(args):
 
         t, ck = replay_timed(call, steps, warmup, stream)
         unit, per_step = metric_of(w)
-        if act_order:
+        if act_order and unit == "GB/s":
             per_step += 4 * w.K / 1e9  # the stored permutation, read once per call
         value = whole_job_value(world, steps, per_step, t)
         per_launch_s = t / steps
         # accuracy level 4: activation quantisation + product, except at M <= 4 with 32 <= bs <= 256, where
         # the decode GEMV quantises X itself
         kernels_per_step = 2 if acc == 4 and not (w.M <= 4 and 32 <= w.bs <= 256) else 1
+        if act_order and w.M > 8:
+            kernels_per_step = 2  # the gather of X into the pack's depth order, then the GEMM
         out = {"workload": w.name, "value": value, "unit": unit, "steps": steps, "ms_per_step": per_launch_s * 1e3,
                "kernel": chosen, "clocks": ck, "weight_copies": R, "launches": steps * kernels_per_step}
         if unit == "GB/s":
@@ -565,6 +567,9 @@ def run_ours(args):
                   extra={"accuracy_level": 4, "launches_per_step": 2})
         secondary("act_order", w, max(20, args.steps // 4), sw, act_order=True,
                   extra={"g_idx": "act-order (a seeded permutation of the depths in blocks), MNB_FLAG_KPERM"})
+        secondary("act_order_m512", wl.config(4), max(20, args.steps // 20), max(3, args.warmup // 20),
+                  act_order=True, extra={"g_idx": "act-order, MNB_FLAG_KPERM: X gathered into the pack's order, "
+                                                  "then the prefill GEMM", "launches_per_step": 2})
         moe, n = measure_moe(wl.MOE_CONFIGS[0], max(20, args.steps // 10), max(3, args.warmup // 10))
         res["moe"] = moe
         res["gpu_launches"] += n
