@@ -62,7 +62,7 @@ def parse():
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-secondary", action="store_true")
-    ap.add_argument("--only", default=None, choices=["moe", "fp8", "nvfp4", "act_order"],
+    ap.add_argument("--only", default=None, choices=["moe", "fp8", "nvfp4", "act_order", "act_order_m512"],
                     help="diagnostic: time only this secondary object (for profiling its kernel alone)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--accuracy-level", type=int, default=0, choices=[0, 4],
@@ -519,8 +519,9 @@ def run_ours(args):
     if args.only:
         if args.only == "moe":
             obj, n = measure_moe(wl.MOE_CONFIGS[0], args.steps, args.warmup)
-        elif args.only == "act_order":
-            sec, _ = measure(wl.config(1), args.steps, args.warmup, "auto", False, 0, act_order=True)
+        elif args.only in ("act_order", "act_order_m512"):
+            wk = wl.config(1 if args.only == "act_order" else 4)
+            sec, _ = measure(wk, args.steps, args.warmup, "auto", False, 0, act_order=True)
             obj, n = {k: sec[k] for k in ("workload", "value", "unit", "kernel", "steps", "ms_per_step", "roofline",
                                           "clocks")}, sec["launches"]
         else:
