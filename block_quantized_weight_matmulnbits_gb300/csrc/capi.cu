@@ -241,7 +241,10 @@ mnb_status mnb_pack_weights_gidx(const uint8_t* b_ort, const int32_t* g_idx, voi
     if (packed_bytes < L.total_bytes() + kperm_bytes(L)) return MNB_ERR_NO_MEM;
     if (!per_device()) return from_cuda(cudaGetLastError());
     if (inject_launch_failure()) return MNB_ERR_CUDA;
-    return from_cuda(launch_pack_gidx(b_ort, g_idx, static_cast<uint8_t*>(packed_b), L, (cudaStream_t)stream));
+    ProfileScope prof("mnb_pack_weights_gidx", (cudaStream_t)stream);
+    const cudaError_t e = launch_pack_gidx(b_ort, g_idx, static_cast<uint8_t*>(packed_b), L, (cudaStream_t)stream);
+    if (e == cudaSuccess) prof.done("pack_gidx");
+    return from_cuda(e);
 }
 
 mnb_status mnb_pack_weights(const uint8_t* b_ort, void* packed_b, size_t packed_bytes, int64_t N, int64_t K,
@@ -252,7 +255,10 @@ mnb_status mnb_pack_weights(const uint8_t* b_ort, void* packed_b, size_t packed_
     L.init(N, K, bits, block_size);
     if (packed_bytes < L.total_bytes()) return MNB_ERR_NO_MEM;
     if (inject_launch_failure()) return MNB_ERR_CUDA;
-    return from_cuda(launch_pack(b_ort, static_cast<uint8_t*>(packed_b), L, (cudaStream_t)stream));
+    ProfileScope prof("mnb_pack_weights", (cudaStream_t)stream);
+    const cudaError_t e = launch_pack(b_ort, static_cast<uint8_t*>(packed_b), L, (cudaStream_t)stream);
+    if (e == cudaSuccess) prof.done("pack");
+    return from_cuda(e);
 }
 
 mnb_status mnb_unpack_codes(const void* packed_b, uint8_t* b_ort, int64_t N, int64_t K, int bits,
@@ -302,7 +308,10 @@ mnb_status mnb_pack_fp_weights(const uint8_t* w_kn, void* packed, size_t packed_
     fp_layout(&L, N, K, format);
     if (packed_bytes < L.total_bytes()) return MNB_ERR_NO_MEM;
     if (inject_launch_failure()) return MNB_ERR_CUDA;
-    return from_cuda(launch_pack(w_kn, static_cast<uint8_t*>(packed), L, (cudaStream_t)stream, format));
+    ProfileScope prof("mnb_pack_fp_weights", (cudaStream_t)stream);
+    const cudaError_t e = launch_pack(w_kn, static_cast<uint8_t*>(packed), L, (cudaStream_t)stream, format);
+    if (e == cudaSuccess) prof.done("pack_fp");
+    return from_cuda(e);
 }
 
 mnb_status mnb_matmul_fp(const void* x, const void* packed, const void* scales, float global_scale, void* y,
@@ -340,10 +349,14 @@ mnb_status mnb_matmul_fp_ex(const void* x, const void* packed, const void* scale
     p.flags = flags;
     if (inject_launch_failure()) return MNB_ERR_CUDA;
     const bool fast = gemv_fp_supported(p);
+    const char* kname = fast ? (gemv_nv_selected(p) ? "gemv_nv" : "gemv_fp") : "fp_generic";
     if (log_enabled())
         std::fprintf(stderr, "[mnb] matmul_fp M=%lld N=%lld K=%lld format=%d kernel=%s\n", (long long)M,
-                     (long long)N, (long long)K, (int)format, fast ? (gemv_nv_selected(p) ? "gemv_nv" : "gemv_fp") : "fp_generic");
-    return from_cuda(fast ? launch_gemv_fp(p, (cudaStream_t)stream) : launch_fp_generic(p, (cudaStream_t)stream));
+                     (long long)N, (long long)K, (int)format, kname);
+    ProfileScope prof("mnb_matmul_fp", (cudaStream_t)stream);
+    const cudaError_t e = fast ? launch_gemv_fp(p, (cudaStream_t)stream) : launch_fp_generic(p, (cudaStream_t)stream);
+    if (e == cudaSuccess) prof.done(kname);
+    return from_cuda(e);
 }
 
 size_t mnb_workspace_size_ex(int64_t M, int64_t N, int64_t K, int bits, int block_size, int accuracy_level,
@@ -380,7 +393,12 @@ mnb_kernel mnb_select_kernel(int64_t M, int64_t N, int64_t K, int bits, int bloc
     return MNB_KERNEL_GEMM_TC;
 }
 
-mnb_status mnb_matmul_ex(const mnb_matmul_args* a) {
+}  // extern "C"
+
+namespace {
+
+// The body of mnb_matmul_ex; on a launch, *family names the kernel family that ran.
+mnb_status matmul_ex_impl(const mnb_matmul_args* a, const char** family) {
     if (!a) return MNB_ERR_INVALID_ARG;
     if (!valid_shape(a->N, a->K, a->bits, a->block_size) || a->M < 0) return MNB_ERR_INVALID_ARG;
     if (!valid_dtype(a->act_dtype) || !valid_dtype(a->out_dtype) || !valid_dtype(a->scale_dtype))
@@ -425,7 +443,7 @@ mnb_status mnb_matmul_ex(const mnb_matmul_args* a) {
         p.kperm = reinterpret_cast<const int32_t*>(p.packed + p.L.data_bytes());
         // prefill: X put in the pack's depth order in the workspace, then the tensor-core GEMM
         const bool gemm_ok = (a->act_dtype == MNB_BF16 || a->act_dtype == MNB_F16) && a->K % 8 == 0 &&
-                             gemm_tc_supported(p);
+                             (size_t)a->K * 2 <= device_info().smem_optin && gemm_tc_supported(p);
         const size_t gneed = kperm_gemm_workspace_bytes(a->M, p.L);
         const bool ws_ok = a->workspace && a->workspace_bytes >= gneed && aligned(a->workspace, 256);
         mnb_kernel kk = a->kernel;
@@ -460,6 +478,8 @@ mnb_status mnb_matmul_ex(const mnb_matmul_args* a) {
             std::fprintf(stderr, "[mnb] matmul M=%lld N=%lld K=%lld bits=%d bs=%d kernel=%s (act-order pack)\n",
                          (long long)a->M, (long long)a->N, (long long)a->K, a->bits, a->block_size,
                          mnb_kernel_name(kk));
+        *family = kk == MNB_KERNEL_GEMV_MMA ? "gemv_mma/act-order"
+                  : kk == MNB_KERNEL_GEMM_TC ? "gemm_tc/act-order" : "generic/act-order";
         return from_cuda(ek);
     }
 
@@ -525,7 +545,20 @@ mnb_status mnb_matmul_ex(const mnb_matmul_args* a) {
     if (log_enabled())
         std::fprintf(stderr, "[mnb] matmul M=%lld N=%lld K=%lld bits=%d bs=%d kernel=%s\n", (long long)a->M,
                      (long long)a->N, (long long)a->K, a->bits, a->block_size, mnb_kernel_name(k));
+    *family = a->accuracy_level == 4 ? (k == MNB_KERNEL_GEMV_I8 ? "gemv_i8/acc4" : "gemm_tc/acc4") : mnb_kernel_name(k);
     return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+mnb_status mnb_matmul_ex(const mnb_matmul_args* a) {
+    ProfileScope prof("mnb_matmul_ex", a ? (cudaStream_t)a->stream : nullptr);
+    const char* family = nullptr;
+    const mnb_status st = matmul_ex_impl(a, &family);
+    if (st == MNB_OK && family) prof.done(family);
+    return st;
 }
 
 mnb_status mnb_matmul(const void* x, const void* packed_b, const void* scales, const uint8_t* zero_points,

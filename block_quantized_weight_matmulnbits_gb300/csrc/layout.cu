@@ -142,26 +142,47 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ packed, const void* _
 }
 
 // Act-order prefill: X's depths put in the packed buffer's order, xp[m, j] = x[m, perm[j]] (16-bit
-// activations), so that the tensor-core GEMM reads contiguous quantisation blocks.  One thread per 8
-// stored depths of a row: 16-byte stores, gathered loads (X is a few MB and sits in L2).  A
-// programmatic dependent: X is read after the dependency wait.
-__global__ void gather_kperm_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
-                                    uint16_t* __restrict__ xp, int64_t M, int64_t K) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-    const int64_t per_row = K / 8;
-    if (t >= M * per_row) return;
-    const int64_t m = t / per_row, j0 = (t - m * per_row) * 8;
+// activations), so that the tensor-core GEMM reads contiguous quantisation blocks.  A CTA takes rows in a
+// grid-stride loop: the row is copied into shared memory with 16-byte loads, then each thread gathers 8 stored
+// depths from there and writes them with one 16-byte store.  The permutation belongs to the packed weights, so
+// a thread's first 8 entries are read once, before the dependency wait, and serve every row; X is read after it.
+__device__ __forceinline__ void load_perm8(const int32_t* perm, int64_t i, int64_t K, int (&pk)[8]) {
+    const int4 p0 = reinterpret_cast<const int4*>(perm)[2 * i];  // the permutation is 256-byte aligned
+    const int4 p1 = reinterpret_cast<const int4*>(perm)[2 * i + 1];
+    const int v[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) pk[e] = v[e] < 0 ? 0 : (v[e] >= K ? (int)K - 1 : v[e]);  // a bad pack reads in X
+}
+
+__device__ __forceinline__ uint4 gather8(const uint16_t* row, const int (&pk)[8]) {
     uint32_t h[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        int64_t k = perm[j0 + e];
-        k = k < 0 ? 0 : (k >= K ? K - 1 : k);  // a bad pack's permutation never indexes past X
-        h[e] = x[m * K + k];
+    for (int e = 0; e < 8; ++e) h[e] = row[pk[e]];
+    return make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+}
+
+__global__ void gather_kperm_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
+                                    uint16_t* __restrict__ xp, int64_t M, int64_t K) {
+    extern __shared__ __align__(16) uint16_t row[];
+    const int64_t k8 = K / 8;
+    const int64_t i0 = threadIdx.x;
+    int pk0[8];
+    if (i0 < k8) load_perm8(perm, i0, K, pk0);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + m * K);
+        for (int64_t i = i0; i < k8; i += blockDim.x) reinterpret_cast<uint4*>(row)[i] = src[i];
+        __syncthreads();
+        uint4* dst = reinterpret_cast<uint4*>(xp + m * K);
+        if (i0 < k8) dst[i0] = gather8(row, pk0);
+        for (int64_t i = i0 + blockDim.x; i < k8; i += blockDim.x) {
+            int pk[8];
+            load_perm8(perm, i, K, pk);
+            dst[i] = gather8(row, pk);
+        }
+        __syncthreads();  // the row buffer is reused
     }
-    *reinterpret_cast<uint4*>(xp + m * K + j0) =
-        make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
 }
 
 unsigned blocks_for(int64_t n, int threads) { return (unsigned)((n + threads - 1) / threads); }
@@ -191,11 +212,19 @@ cudaError_t launch_pack_gidx(const uint8_t* b_ort, const int32_t* g_idx, uint8_t
 
 cudaError_t launch_gather_kperm(const void* x, const int32_t* perm, void* xp, int64_t M, const Layout& L,
                                 bool pdl, cudaStream_t s) {
-    const int64_t n = M * (L.K / 8);
-    if (n <= 0) return cudaSuccess;
+    if (M <= 0 || L.K <= 0) return cudaSuccess;
+    const size_t smem = (size_t)L.K * 2;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(gather_kperm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(blocks_for(n, 256));
-    cfg.blockDim = dim3(256);
+    // one 16-byte output per thread for K <= 8192: 32..1024 threads
+    const int64_t k8 = L.K / 8;
+    const unsigned threads = (unsigned)(k8 >= 1024 ? 1024 : ((k8 + 31) / 32) * 32);
+    cfg.gridDim = dim3((unsigned)(M < 65535 ? M : 65535));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

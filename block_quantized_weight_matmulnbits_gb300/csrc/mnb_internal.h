@@ -6,6 +6,7 @@
 #include <cstddef>
 #include <mutex>
 #include <cuda_runtime.h>
+#include <utility>
 
 #include "mnb_common.cuh"
 
@@ -132,6 +133,25 @@ int* device_status_word();
 
 // MNB_FAIL_LAUNCH=1: entry points report MNB_ERR_CUDA instead of launching.
 bool inject_launch_failure();
+
+// MNB_PROFILE=1 (read on every call): an NVTX range around the entry point and
+// per-kernel-family host and device timers, reported on stderr every
+// MNB_PROFILE_EVERY calls (default 512).  A scope does nothing when disabled.
+bool profile_enabled();
+class ProfileScope {
+public:
+    ProfileScope(const char* range, cudaStream_t s);
+    ~ProfileScope();
+    void done(const char* kernel);  // the call launched its work under this family name
+    ProfileScope(const ProfileScope&) = delete;
+    ProfileScope& operator=(const ProfileScope&) = delete;
+
+private:
+    bool on_ = false, done_ = false;
+    cudaStream_t stream_ = nullptr;
+    double t0_ = 0;
+    std::pair<cudaEvent_t, cudaEvent_t> ev_{nullptr, nullptr};
+};
 
 // Identifier of the CUDA context current on the calling thread (the driver's
 // context id, unique for the life of the process, so a context created after

@@ -228,7 +228,11 @@ MNB_API size_t mnb_workspace_size(int64_t M, int64_t N, int64_t K, int bits, int
  * M > 8 the act-order prefill needs X in the pack's depth order,
  * ceil256(M * K * 2) bytes (bf16 / f16 X).  Given that workspace, such a call
  * gathers X into it and runs the tensor-core prefill GEMM; without it, the
- * generic kernel (a forced MNB_KERNEL_GEMM_TC returns MNB_ERR_NO_MEM). */
+ * generic kernel (a forced MNB_KERNEL_GEMM_TC returns MNB_ERR_NO_MEM).  The
+ * gather holds one row of X in shared memory, so K * 2 bytes must fit in a
+ * CTA's opt-in shared memory (K up to about 116000 on this part); longer rows
+ * take the generic kernel (a forced MNB_KERNEL_GEMM_TC returns
+ * MNB_ERR_UNSUPPORTED). */
 MNB_API size_t mnb_workspace_size_ex(int64_t M, int64_t N, int64_t K, int bits, int block_size,
                              int accuracy_level, int flags);
 
@@ -382,6 +386,14 @@ MNB_API mnb_status mnb_matmul_fp_ex(const void* x, const void* packed, const voi
 /* Environment overrides, read at each call (none changes a result beyond
  * rounding order; none is needed for normal use):
  *   MNB_LOG=1              print the kernel family chosen for each call
+ *   MNB_PROFILE=1          an NVTX range around each mnb_matmul_ex /
+ *                          mnb_matmul_fp call and each pack, and per
+ *                          kernel family ("pack" for the packs) the
+ *                          host time in the call and the device time between
+ *                          CUDA events recorded around its launches (none
+ *                          under graph capture), printed on stderr every
+ *                          MNB_PROFILE_EVERY calls (default 512).  The events
+ *                          cost the calls their programmatic-launch overlap.
  *   MNB_GEMV_MAX_M         largest M routed to the decode GEMV (default 16)
  *   MNB_GEMV_SCHED=ks|tile|pers|stream|xr
  *                          force one schedule of the tensor-core decode GEMV
